@@ -1,0 +1,482 @@
+"""Throughput of XAttention BSA chunked prefill (estimate + select + attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload q06b_32k] [--tau 0.9]
+
+One step = one layer's whole chunked prefill of the workload: for each chunk,
+xattn_estimate -> xattn_select -> bsa_chunk_attention through the C ABI, on
+one stream, inputs resident in HBM.  Prints one JSON line (rank 0).
+
+Default workload: Qwen3-0.6B-like layer at 32K context (16 Q / 8 KV heads,
+head_dim 128, 8 chunks of 4096 tokens, 128-token pages in a seeded random
+permutation addressed through a [1, 256] block table, stride 8, tau 0.9).
+Multi-GPU runs independent replicas (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "prefill tokens/s per layer at 32K ctx (estimate+select+BSA), % of GB300 roofline"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_desc(name, tau):
+    from xattention_block_sparse_gb300 import inputs as I
+    c = I.CONFIGS[name]
+    return (f"{name}: {c.H} Q / {c.Hkv} KV heads, head_dim {c.D}, {c.L}-token context in "
+            f"{c.L // c.chunk} chunks of {c.chunk}, block {c.block}, stride {c.stride}, "
+            f"tau {tau}, pages permuted via block_table [1, {c.L // c.block}]")
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work (per chunk): the counts the method must do
+# ---------------------------------------------------------------------------
+
+def chunk_work(cfg, c, chunk, n_sel):
+    H, Hkv, D, S, Bk = cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block
+    Lh, Lc = c * chunk, chunk
+    rq, ch = Lc // S, Lh // S
+    cells = H * (rq * ch + rq * (rq + 1) // 2)
+    f_est = 2 * S * D * cells
+    b_est_gemm = 2 * Hkv * D * (Lh + Lc) * 2 + 2 * H * Lc * D + 4 * cells
+    qb, kb = Lc // Bk, (Lh + Lc) // Bk
+    b_bsum = 4 * cells + 4 * H * qb * kb
+    f_att = 4 * H * D * Lc * (n_sel * Bk) + 4 * H * D * Lc * (Lc + 1) // 2
+    b_att = 2 * 2 * Hkv * D * (n_sel * Bk + Lc) + 2 * 2 * H * Lc * D + 4 * H * Lc
+    return dict(f_est=f_est, b_est=b_est_gemm, b_bsum=b_bsum, f_att=f_att, b_att=b_att,
+                cells=cells)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.idx = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def traffic_for(kernel_file, kernel_name):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel's file; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "xattention_block_sparse_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_name \
+                    and parts[1] == sha:
+                return float(parts[2])
+    return None
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+    from xattention_block_sparse_gb300 import inputs as I
+    from xattention_block_sparse_gb300 import runner as RN
+    from xattention_block_sparse_gb300 import xattn as X
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from __graft_entry__ import build
+    if rank == 0 or ws == 1:
+        build()
+    if ws > 1:
+        dist.barrier()
+    X.load_library()
+
+    wl = I.make_workload(args.workload)
+    cfg = wl.cfg
+    L, chunk = cfg.L, cfg.chunk
+    nchunk = L // chunk
+    up = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    Q, K, V = up(wl.q_bits), up(wl.k_bits), up(wl.v_bits)
+    KP, VP = up(wl.kpool_bits), up(wl.vpool_bits)
+    BT = torch.from_numpy(wl.block_table).to(dev)
+    seq = RN.SequencePrefill(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, L, chunk, BT,
+                             KP.shape[0])
+    O_ = torch.empty((cfg.H, L, cfg.D), dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty((cfg.H, L), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    tau = args.tau
+
+    def step(ev=None):
+        for c in range(nchunk):
+            p = seq.problems[c]
+            t0 = c * chunk
+            b = seq.bufs
+            if ev is not None:
+                ev[c][0].record(stream)
+            X.xattn_estimate(p, Q[:, t0:], K[:, t0:], KP, RN.estimation_scale(cfg.D, cfg.stride),
+                             b.workspace, b.block_sums, stream)
+            if ev is not None:
+                ev[c][1].record(stream)
+            X.xattn_select(p, b.block_sums, tau, b.workspace, None, b.sel_idx, b.sel_page,
+                           b.n_sel, stream)
+            if ev is not None:
+                ev[c][2].record(stream)
+            X.bsa_chunk_attention(p, Q[:, t0:], K[:, t0:], V[:, t0:], KP, VP, b.sel_page,
+                                  b.n_sel, 1.0 / math.sqrt(cfg.D), O_[:, t0:], LSE[:, t0:],
+                                  stream)
+            if ev is not None:
+                ev[c][3].record(stream)
+
+    # selection per chunk (deterministic): one untimed pass that reads n_sel
+    n_sel = []
+    with torch.cuda.stream(stream):
+        for c in range(nchunk):
+            p = seq.problems[c]
+            t0 = c * chunk
+            RN.prefill_chunk(p, Q[:, t0:], K[:, t0:], V[:, t0:], KP, VP, tau, seq.bufs,
+                             O_[:, t0:], LSE[:, t0:], stream=stream)
+            n_sel.append(int(seq.bufs.n_sel[0].item()))
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step()
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nchunk)]
+              for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            flush.zero_()  # L2 flush between steps (outside the step events)
+            step(events[s])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clocks = clk.stop()
+    if ws > 1:
+        dist.barrier()
+
+    est_ms = sel_ms = att_ms = 0.0
+    step_ms = []
+    for s in range(args.steps):
+        tot = 0.0
+        for c in range(nchunk):
+            e = events[s][c]
+            a, b_, d = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])
+            est_ms += a
+            sel_ms += b_
+            att_ms += d
+        step_ms.append(events[s][0][0].elapsed_time(events[s][nchunk - 1][3]))
+    ms = float(np.mean(step_ms))
+    t_max = sum(step_ms) / 1e3
+    if ws > 1:
+        t = torch.tensor([t_max], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+
+    work = [chunk_work(cfg, c, chunk, n_sel[c]) for c in range(nchunk)]
+    K_ = args.steps
+    f_att = sum(w["f_att"] for w in work)
+    f_est = sum(w["f_est"] for w in work)
+    b_bs = sum(w["b_bsum"] for w in work)
+    peaks, peak_src = load_peaks()
+    att_launch_ms = att_ms / (K_ * nchunk)
+    att_tflops = (f_att / nchunk) / (att_launch_ms * 1e-3) / 1e12
+    est_tflops = (f_est / nchunk) / ((est_ms / (K_ * nchunk)) * 1e-3) / 1e12
+    stage = {"estimate_ms_per_step": est_ms / K_, "select_ms_per_step": sel_ms / K_,
+             "attention_ms_per_step": att_ms / K_}
+    tokens = L * ws * K_
+    value = tokens / t_max
+
+    # roofline of the step: algorithmic time at peak over measured time
+    t_roof = sum(max(w["f_est"] / (peaks["bf16_tflops"] * 1e12),
+                     (w["b_est"] + w["b_bsum"]) / (peaks["hbm_gbs"] * 1e9))
+                 + max(w["f_att"] / (peaks["bf16_tflops"] * 1e12),
+                       w["b_att"] / (peaks["hbm_gbs"] * 1e9)) for w in work)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk)
+
+    density = sum(n_sel) / max(1, sum(c * chunk // cfg.block for c in range(nchunk)))
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": K_,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 with RoPE theta 1e6; no model weights)",
+        "config": {"workload": workload_desc(args.workload, tau), "tokens_per_step": L,
+                   "chunks": nchunk, "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "tensor", "kernel": "attn_kernel (bsa_chunk_attention)",
+                     "achieved": att_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": att_tflops / peaks["bf16_tflops"],
+                     "frac_sustained": att_tflops / peaks["bf16_tflops_sustained"],
+                     "peak_source": peak_src,
+                     "traffic": traffic_for("attention.cu", "attn_kernel"),
+                     "launch_ms": att_launch_ms},
+        "step_roofline": {"t_roof_ms": t_roof * 1e3, "t_meas_ms": ms,
+                          "frac": t_roof * 1e3 / ms},
+        "kernels": {"estimate": {"achieved_tflops": est_tflops,
+                                 "frac": est_tflops / peaks["bf16_tflops"]},
+                    "block_sum_bytes_per_step": b_bs, **stage},
+        "density": density,
+        "n_sel_per_chunk": n_sel,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 5 * nchunk * K_,
+        "wall_s_timed": wall,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args, wl, n_sel)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk):
+    """Same metric through the public API with pinned HOST buffers: every step
+    copies the layer's inputs host->device and reads O and LSE back."""
+    pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(
+        torch.bfloat16).pin_memory()
+    hQ, hK, hV = pin(wl.q_bits), pin(wl.k_bits), pin(wl.v_bits)
+    hKP, hVP = pin(wl.kpool_bits), pin(wl.vpool_bits)
+    dQ, dK, dV = (torch.empty_like(t, device=dev) for t in (hQ, hK, hV))
+    dKP, dVP = torch.empty_like(hKP, device=dev), torch.empty_like(hVP, device=dev)
+    L = cfg.L
+    dO = torch.empty((cfg.H, L, cfg.D), dtype=torch.bfloat16, device=dev)
+    dL = torch.empty((cfg.H, L), dtype=torch.float32, device=dev)
+    hO = torch.empty((cfg.H, L, cfg.D), dtype=torch.bfloat16).pin_memory()
+    hL = torch.empty((cfg.H, L), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hKP, hVP))
+    d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
+
+    def one():
+        for dst, src in ((dQ, hQ), (dK, hK), (dV, hV), (dKP, hKP), (dVP, hVP)):
+            dst.copy_(src, non_blocking=True)
+        seq.run(dQ, dK, dV, dKP, dVP, tau, dO, dL, stream=stream)
+        hO.copy_(dO, non_blocking=True)
+        hL.copy_(dL, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, args.steps)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    return {"value": L * steps / t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3 / steps}
+
+
+# ---------------------------------------------------------------------------
+# Oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_chunk_sample(wl, cfg, c, chunk, tau, rows_per_chunk, oracle):
+    """Estimate + select on the whole chunk c; attention on `rows_per_chunk`
+    evenly spread query rows, extrapolated to the chunk.  Returns
+    (tokens represented, seconds, seconds measured)."""
+    O = oracle
+    t0, t1 = c * chunk, (c + 1) * chunk
+    q = wl._f64_cache["q"]
+    k = wl._f64_cache["k"]
+    v = wl._f64_cache["v"]
+    kp, vp = wl._f64_cache["kpool"], wl._f64_cache["vpool"]
+    s0 = time.perf_counter()
+    bs = O.estimate_request(q[:, t0:t1], k[:, t0:t1], kp, wl.block_table[0], t0, cfg.H, cfg.Hkv,
+                            cfg.stride, cfg.block, O.default_estimation_scale(cfg.D, cfg.stride))
+    _, _, pages = O.select_request(bs.astype(np.float32), tau, cfg.Hkv, t0 // cfg.block,
+                                   wl.block_table[0])
+    s1 = time.perf_counter()
+    rows = np.linspace(0, chunk - 1, rows_per_chunk).astype(int)
+    O.attend_request(q[:, t0:t1], k[:, t0:t1], v[:, t0:t1], kp, vp, pages, cfg.H, cfg.Hkv,
+                     1 / math.sqrt(cfg.D), rows=rows)
+    s2 = time.perf_counter()
+    est = (s1 - s0) + (s2 - s1) * chunk / rows_per_chunk
+    return chunk, est, s2 - s0
+
+
+def _prep_oracle(wl):
+    wl._f64_cache = {n: wl.f64(n) for n in ("q", "k", "v", "kpool", "vpool")}
+
+
+def _blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max((i.get("num_threads", 0) for i in info), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(args, wl, n_sel):
+    from oracle import xattn_oracle as O
+    cfg = wl.cfg
+    chunk = cfg.chunk
+    nchunk = cfg.L // chunk
+    _prep_oracle(wl)
+    rows = 32
+    tok = sec = meas = 0.0
+    for c in range(nchunk):
+        a, b, m = oracle_chunk_sample(wl, cfg, c, chunk, args.tau, rows, O)
+        tok += a
+        sec += b
+        meas += m
+    return {"value": tok / sec, "unit": "tokens/s", "cores": _blas_threads(),
+            "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": (f"float64 oracle on all {nchunk} chunks: estimate + select in full, "
+                       f"attention on {rows} of {chunk} query rows per chunk extrapolated "
+                       f"linearly to the chunk; {meas:.1f} s measured")}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from oracle import xattn_oracle as O
+    from xattention_block_sparse_gb300 import inputs as I
+    wl = I.make_workload(args.workload)
+    cfg = wl.cfg
+    chunk = cfg.chunk
+    nchunk = cfg.L // chunk
+    _prep_oracle(wl)
+    rows = 16
+    for s in range(args.warmup):
+        oracle_chunk_sample(wl, cfg, s % nchunk, chunk, args.tau, rows, O)
+    tok = sec = meas = 0.0
+    for s in range(args.steps):
+        a, b, m = oracle_chunk_sample(wl, cfg, s % nchunk, chunk, args.tau, rows, O)
+        tok += a
+        sec += b
+        meas += m
+    value = tok / sec
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, args.tau)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": (f"each step: one chunk (chunk index = step mod {nchunk}), "
+                                    f"estimate + select in full, attention on {rows} query rows "
+                                    f"extrapolated to the chunk; {meas:.1f} s measured")},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="q06b_32k")
+    ap.add_argument("--tau", type=float, default=0.9)
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

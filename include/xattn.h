@@ -1,0 +1,198 @@
+/*
+ * libxattn -- XAttention block-sparse attention (BSA) for chunked prefill,
+ * single GPU, sm_103a.
+ *
+ * One chunk of prefill is three steps, each an entry point below, all issued
+ * on one caller-given CUDA stream in this order:
+ *
+ *   xattn_estimate       block importance: stride-reshaped Q.K^T scores,
+ *                        softmax statistics merged across KV tiles, and
+ *                        per-(query block, KV block) attention mass
+ *   xattn_select         cumulative-attention threshold per (head, query block),
+ *                        GQA "any" per KV-head group, majority vote, sink and
+ *                        last history block forced, block_table lookup
+ *   bsa_chunk_attention  attention over the selected history pages
+ *                        (non-causal) and the current chunk (causal), merged
+ *                        by log-sum-exp, with the output's LSE
+ *
+ * and lse_merge, the stand-alone merge of two partial attention results.
+ *
+ * Sources: "XAttention BSA Policy 设计文档" (nano-vllm
+ * docs/xattn_bsa_policy_design.md), sections 核心算法 1 select_blocks (Steps 1-4)
+ * and 2 compute_chunked_prefill; "XAttention Offload Stream Synchronization
+ * Fix" (docs/xattn_offload_stream_sync_fix.md), section 技术细节 (three-stage
+ * KV chunking, stream configuration); "Atenção paginada" (transformers docs
+ * paged_attention.md), Caminho Varlen / Caminho de decodificação (cu_seq_lens,
+ * block_table).
+ *
+ * Conventions common to every entry point
+ * ---------------------------------------
+ * Memory:    every pointer marked DEVICE is global memory of the current
+ *            device, owned by the caller; the library allocates nothing and
+ *            frees nothing.  HOST pointers are read during the call only.
+ * Streams:   all work is enqueued on `stream`; no call synchronises the host,
+ *            touches the default stream or records events.  Data produced on
+ *            another stream must be ordered by the caller (an event wait on
+ *            `stream`) before the call -- the ordering bug the stream-sync
+ *            page documents cannot occur inside the library.
+ * Tokens:    a chunk packs B requests along the token axis (B = 1 for a plain
+ *            chunked prefill).  Request r owns query tokens
+ *            [cu_seqlens_q[r], cu_seqlens_q[r+1]) of q, k_cur, v_cur, o, lse,
+ *            and has cu_seqlens_kh[r+1]-cu_seqlens_kh[r] history tokens stored
+ *            in the paged pool.  Every length is a multiple of block_size.
+ * Layouts:   q, o      bf16 [H, tokens, D]   (head h at h*q_head_stride)
+ *            k_cur,v_cur bf16 [Hkv, tokens, D] (head at h*kv_head_stride)
+ *            lse       fp32 [H, tokens]      (head at h*lse_head_stride)
+ *            k_pool,v_pool bf16 [num_pages, block_size, Hkv, D]
+ *            block_table int32 [B, bt_stride]; history token t of request r is
+ *                      row t % block_size of page block_table[r][t / block_size];
+ *                      -1 marks an unallocated page.
+ *            GQA:      query head h reads KV head h / (H / Hkv).
+ * Errors:    argument checks happen on the host before any launch and return a
+ *            negative status with nothing enqueued.  Faults found by kernels
+ *            (a page id outside [0, num_pages) reached through block_table or
+ *            the selection) never trap: the kernel skips the page, records the
+ *            first such fault in a device error word and continues; read it
+ *            with xattn_device_error.
+ */
+#ifndef XATTN_H
+#define XATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *xattn_stream_t; /* identical to cudaStream_t */
+
+typedef enum xattn_status {
+  XATTN_OK = 0,
+  XATTN_EINVAL = -1,          /* null pointer, bad size or divisibility */
+  XATTN_EALIGN = -2,          /* pointer or stride not 16-byte aligned */
+  XATTN_EPAGE = -3,           /* (device word) page id out of range */
+  XATTN_ECUDA = -4,           /* a CUDA runtime call or launch failed */
+  XATTN_EUNSUPPORTED = -5,    /* head_dim / block geometry not built */
+  XATTN_EWORKSPACE = -6       /* workspace smaller than xattn_workspace_size */
+} xattn_status;
+
+#define XATTN_MAX_REQUESTS 64
+#define XATTN_MAX_BLOCKS_PER_ROW 8192 /* history + current blocks of one request */
+
+/* Problem description shared by every entry point (host memory).
+ * Constraints (XATTN_EINVAL / XATTN_EUNSUPPORTED otherwise):
+ *   1 <= num_requests <= XATTN_MAX_REQUESTS; num_heads % num_kv_heads == 0;
+ *   head_dim in {64, 128}; block_size % 64 == 0; block_size % stride == 0;
+ *   (block_size / stride) % 4 == 0; 1 <= stride <= 64;
+ *   every query and history length a multiple of block_size;
+ *   history blocks + query blocks of a request <= XATTN_MAX_BLOCKS_PER_ROW;
+ *   history blocks of a request <= bt_stride. */
+typedef struct xattn_problem {
+  int32_t num_requests;           /* B */
+  int32_t num_heads;              /* H, query heads */
+  int32_t num_kv_heads;           /* Hkv */
+  int32_t head_dim;               /* D */
+  int32_t stride;                 /* S, XAttention stride ("stride reshape") */
+  int32_t block_size;             /* Bk: BSA block == KV page size (tokens) */
+  const int32_t *cu_seqlens_q;    /* HOST [B+1] cumulative query-chunk lengths */
+  const int32_t *cu_seqlens_kh;   /* HOST [B+1] cumulative history lengths */
+  const int32_t *block_table;     /* DEVICE [B, bt_stride] physical page ids */
+  int32_t bt_stride;              /* row pitch of block_table (>= history blocks) */
+  int32_t num_pages;              /* pages in k_pool / v_pool */
+  int64_t q_head_stride;          /* elements between heads of q and o */
+  int64_t kv_head_stride;         /* elements between heads of k_cur and v_cur */
+  int64_t lse_head_stride;        /* elements between heads of lse */
+} xattn_problem;
+
+/* Bytes of scratch the caller must provide to xattn_estimate / xattn_select
+ * for this problem (0 on invalid problems).  The workspace holds the fp32
+ * reshaped score matrix, per-tile and merged softmax statistics and the vote
+ * counters; its contents between calls are unspecified. */
+size_t xattn_workspace_size(const xattn_problem *p);
+
+/* Number of fp32 elements of block_sums (and bytes of the optional mask):
+ * request by request, [H, Qb_r, Kb_r] with Qb_r = q_len_r / block_size and
+ * Kb_r = (kh_len_r + q_len_r) / block_size (history blocks first, then the
+ * current chunk's blocks), requests packed back to back. */
+size_t xattn_block_sums_count(const xattn_problem *p);
+
+/* Element offset of request r's [H, Qb_r, Kb_r] slab inside block_sums. */
+size_t xattn_block_sums_offset(const xattn_problem *p, int32_t r);
+
+/* Estimation (BSA policy page, select_blocks Steps 1-2; stream-sync page,
+ * three-stage KV chunking).  For every query head h (KV head h / G), reshaped
+ * row a < q_len/S and reshaped column b over [history ; current chunk]:
+ *   s[a,b] = scale * sum_{i<S} q[S a + S-1-i] . k[S b + i]        (antidiagonal)
+ * current-chunk column b' is visible from row a iff b' <= a; history is all
+ * visible.  Per row, softmax statistics (max, sum of exp) are taken per
+ * 128-column tile, merged across tiles, and
+ *   block_sums[h, qb, kb] = sum over the (block/S)^2 visible cells of the
+ *                           block of exp(s - m_row) / l_row.
+ *   q       DEVICE bf16, layout above      k_cur  DEVICE bf16
+ *   k_pool  DEVICE bf16 paged history keys
+ *   scale   logit scale; the usual choice is 1 / (sqrt(D) * S)
+ *   workspace, workspace_bytes   DEVICE scratch >= xattn_workspace_size(p)
+ *   block_sums  DEVICE fp32 [xattn_block_sums_count(p)], written fully. */
+xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k_cur,
+                            const void *k_pool, float scale, void *workspace,
+                            size_t workspace_bytes, float *block_sums,
+                            xattn_stream_t stream);
+
+/* Selection (BSA policy page, select_blocks Steps 3-4).
+ * Per (request, head, query block) row, with integer masses
+ * q_j = round_half_even(block_sums_j * 2^32), T = sum_j q_j, R = fl64(threshold*T):
+ * blocks are visited by (q_j descending, j ascending) and block j is kept iff
+ * the integer mass visited before it is < R (threshold >= 1 keeps every q_j > 0).
+ * Then, over history blocks only: a KV-head group keeps a block if any of its
+ * query heads does; a block is selected when 2*votes > Hkv * Qb_r (votes over
+ * KV heads x query blocks); history block 0 and block Kb_h-1 are always added.
+ *   threshold   > 0 (0.9 and 0.95 are the pages' settings)
+ *   mask        DEVICE u8 [xattn_block_sums_count(p)] or NULL: per-head keep flags
+ *   sel_idx     DEVICE int32 [B, bt_stride]: ascending logical history block ids
+ *   sel_page    DEVICE int32 [B, bt_stride]: block_table[r][sel_idx]
+ *   n_sel       DEVICE int32 [B]: number of valid entries per request
+ * Entries past n_sel[r] are left untouched. */
+xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,
+                          void *workspace, size_t workspace_bytes, uint8_t *mask,
+                          int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
+                          xattn_stream_t stream);
+
+/* Sparse chunk attention (BSA policy page, compute_chunked_prefill).  For each
+ * query token i of request r and head h, softmax attention with scale
+ * softmax_scale over the keys of the selected history pages
+ * (sel_page[r][0..n_sel[r]), all visible) and the current-chunk keys j <= i;
+ * the history and causal parts are merged online by log-sum-exp, so the result
+ * equals flash_attn_with_lse(history) merged with flash_attn_with_lse(causal).
+ *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
+ *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE */
+xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
+                                 const void *v_cur, const void *k_pool, const void *v_pool,
+                                 const int32_t *sel_page, const int32_t *n_sel,
+                                 float softmax_scale, void *o, float *lse,
+                                 xattn_stream_t stream);
+
+/* merge_attention_outputs (BSA policy page, compute_chunked_prefill): for each
+ * of `rows` rows, lse = log(exp(lse1) + exp(lse2)) and
+ * o = o1 * exp(lse1 - lse) + o2 * exp(lse2 - lse); two empty parts (-inf, -inf)
+ * give o = 0, lse = -inf.
+ *   o1, o2   DEVICE fp32 [rows, head_dim]; lse1, lse2 DEVICE fp32 [rows]
+ *   o_out    DEVICE [rows, head_dim], fp32, or bf16 when o_out_bf16 != 0
+ *   lse_out  DEVICE fp32 [rows]; o_out / lse_out may alias o1 / lse1. */
+xattn_status lse_merge(const float *o1, const float *lse1, const float *o2,
+                       const float *lse2, int64_t rows, int32_t head_dim, void *o_out,
+                       int32_t o_out_bf16, float *lse_out, xattn_stream_t stream);
+
+/* Reads (and, if clear != 0, resets) the device error word of the current
+ * device after synchronising `stream`.  *code is XATTN_OK or the first fault
+ * status recorded by a kernel.  Diagnostic call: it blocks the host. */
+xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t clear);
+
+/* Static description of a status code. */
+const char *xattn_status_string(xattn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XATTN_H */

@@ -112,7 +112,7 @@ def stride_reshape(x: np.ndarray, stride: int, reverse: bool) -> np.ndarray:
 
 
 def estimation_scores(q, k_hist, k_cur, stride: int, scale: float,
-                      mode: str = "antidiag", include_current: bool = True):
+                      mode: str = "antidiag", include_current: bool = True, row0: int = 0):
     """Reshaped scores s[a, b] of one query head, with masked cells at -inf.
 
     q: [Lq, D] query chunk; k_hist: [Lh, D] history keys (all visible:
@@ -120,7 +120,9 @@ def estimation_scores(q, k_hist, k_cur, stride: int, scale: float,
     appended after the history ([SYNC] Pass 1/Pass 2 "当前 chunk").  Current
     column b (chunk-local) is visible from reshaped row a iff b <= a.
     mode "antidiag": s = scale * sum_i q[S a + S-1-i] . k[S b + i];
-    mode "diag":     s = scale * sum_i q[S a + i]     . k[S b + i]."""
+    mode "diag":     s = scale * sum_i q[S a + i]     . k[S b + i].
+    ``row0`` is the reshaped index of q's first row when q is a slice of the
+    chunk (the causal test then uses the row's index in the whole chunk)."""
     keys = [k_hist] + ([k_cur] if include_current else [])
     K = np.concatenate(keys, axis=0) if len(keys) > 1 else keys[0]
     Qr = stride_reshape(q, stride, reverse=(mode == "antidiag"))
@@ -129,8 +131,8 @@ def estimation_scores(q, k_hist, k_cur, stride: int, scale: float,
     if include_current:
         ch = k_hist.shape[0] // stride
         rq = Qr.shape[0]
-        a = np.arange(rq)[:, None]
-        b = np.arange(s.shape[1] - ch)[None, :]
+        a = row0 + np.arange(rq)[:, None]
+        b = np.arange(k_cur.shape[0] // stride)[None, :]
         s[:, ch:][b > a] = NEG_INF
     return s
 
@@ -182,6 +184,20 @@ def block_sums_one_head(q, k_hist, k_cur, stride, block, scale, mode="antidiag",
     s = estimation_scores(q, k_hist, k_cur, stride, scale, mode, include_current)
     m, l = softmax_stats(s)
     return normalized_block_sums(s, m, l, block // stride)
+
+
+def block_sums_qblocks(q, k_hist, k_cur, stride, block, scale, qblocks, mode="antidiag"):
+    """Rows ``qblocks`` of block_sums_one_head, computed from those query blocks
+    alone: softmax statistics are per reshaped row, so a row needs only its own
+    scores.  Returns [len(qblocks), Kb_h + Kb_c]."""
+    rb = block // stride
+    out = []
+    for qb in qblocks:
+        s = estimation_scores(q[qb * block:(qb + 1) * block], k_hist, k_cur, stride, scale,
+                              mode, row0=qb * rb)
+        m, l = softmax_stats(s)
+        out.append(normalized_block_sums(s, m, l, rb)[0])
+    return np.stack(out)
 
 
 def block_sums_chunked(q, k_hist, k_cur, stride, block, scale, col_chunks,

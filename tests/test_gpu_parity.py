@@ -1,0 +1,232 @@
+"""GPU-vs-oracle parity of the whole chunked-prefill path, through the C-ABI.
+
+Block sums within 1e-3 relative; the oracle's selection applied to the GPU's
+block sums equals the GPU's mask, block ids and pages bit for bit; attention
+output within 2e-2 max-abs and LSE within 1e-3 against the oracle over the
+same selection."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import xattn_oracle as O
+from xattention_block_sparse_gb300 import inputs as I
+from xattention_block_sparse_gb300 import runner as RN
+from xattention_block_sparse_gb300 import xattn as X
+
+from gpu_common import (SequenceCase, check_attention, check_block_sums, check_selection, dev,
+                        to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_all_chunks_full_parity():
+    case = SequenceCase("tiny")
+    tau = case.cfg.taus[0]
+    n = case.L // case.chunk
+    O_, LSE, cap = case.run(tau, capture=range(n))
+    for c in range(n):
+        case.check_chunk(c, cap[c], O_, LSE, tau)
+
+
+def test_tiny_ragged_chunk_of_one_block():
+    """Chunks of one 64-token block: a query tile shorter than the CTA tile
+    and reshaped rows fewer than one GEMM tile."""
+    case = SequenceCase("tiny", L=512, chunk=64)
+    tau = 0.9
+    n = case.L // case.chunk
+    O_, LSE, cap = case.run(tau, capture=range(n))
+    for c in range(n):
+        case.check_chunk(c, cap[c], O_, LSE, tau)
+
+
+def test_tiny_tau_one_is_dense_causal_attention():
+    """threshold 1.0 keeps every history block (FullAttentionPolicy): the output
+    equals dense causal attention over the whole prefix."""
+    case = SequenceCase("tiny")
+    O_, LSE, cap = case.run(1.0, capture=range(4))
+    q, k, v, _, _ = case.oracle_inputs()
+    for c in range(4):
+        assert cap[c]["n_sel"] == c * case.chunk // case.cfg.block
+    L, D = case.L, case.cfg.D
+    for h in range(case.cfg.H):
+        vis = np.arange(L)[None, :] <= np.arange(L)[:, None]
+        o_ref, l_ref = O.attention_with_lse(q[h], k[0], v[0], 1 / math.sqrt(D), vis)
+        check_attention(O_[h], LSE[h], o_ref, l_ref, f"head {h}")
+
+
+def test_q06b_4k_all_chunks_full_parity():
+    case = SequenceCase("q06b_4k")
+    tau = 0.9
+    n = case.L // case.chunk
+    O_, LSE, cap = case.run(tau, capture=range(n))
+    for c in range(n):
+        case.check_chunk(c, cap[c], O_, LSE, tau)
+
+
+@pytest.mark.parametrize("tau", [0.9, 0.95])
+def test_q06b_32k_sampled_parity(tau):
+    """Full 32K context in 4096-token chunks through the permuted page pool;
+    block sums on sampled query blocks, selection on every row, attention on
+    sampled query rows (first, last and spread)."""
+    case = SequenceCase("q06b_32k")
+    n = case.L // case.chunk
+    chunks = [0, 1, n - 1]
+    O_, LSE, cap = case.run(tau, capture=chunks)
+    rng = np.random.default_rng(0)
+    for c in chunks:
+        qblocks = sorted({0, case.chunk // case.cfg.block - 1,
+                          int(rng.integers(1, case.chunk // case.cfg.block - 1))})
+        rows = sorted({0, case.chunk - 1, *rng.integers(0, case.chunk, 14).tolist()})
+        case.check_chunk(c, cap[c], O_, LSE, tau, qblocks=qblocks, rows=rows)
+
+
+def test_varlen_batch_parity():
+    wl = I.make_workload("varlen")
+    cfg = wl.cfg
+    call = wl.calls[0]
+    d = dev()
+    Q, K, V = to_dev_bf16(wl.q_bits), to_dev_bf16(wl.k_bits), to_dev_bf16(wl.v_bits)
+    KP, VP = to_dev_bf16(wl.kpool_bits), to_dev_bf16(wl.vpool_bits)
+    BT = torch.from_numpy(wl.block_table).to(d)
+    prob = X.Problem(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, call.q_lens, call.kh_lens, BT,
+                     KP.shape[0])
+    bufs = RN.ChunkBuffers.for_problems([prob], d, with_mask=True)
+    tot = sum(call.q_lens)
+    O_ = torch.empty((cfg.H, tot, cfg.D), dtype=torch.bfloat16, device=d)
+    LSE = torch.empty((cfg.H, tot), dtype=torch.float32, device=d)
+    tau = cfg.taus[0]
+    RN.prefill_chunk(prob, Q, K, V, KP, VP, tau, bufs, O_, LSE)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    bs_all = bufs.block_sums.cpu().numpy()
+    mask_all = bufs.mask.cpu().numpy()
+    sel_all, page_all = bufs.sel_idx.cpu().numpy(), bufs.sel_page.cpu().numpy()
+    nsel = bufs.n_sel.cpu().numpy()
+    Og, Lg = O_.float().cpu().numpy(), LSE.cpu().numpy()
+    q, k, v = wl.f64("q"), wl.f64("k"), wl.f64("v")
+    kp, vp = wl.f64("kpool"), wl.f64("vpool")
+    scale = O.default_estimation_scale(cfg.D, cfg.stride)
+    br = cfg.block // cfg.stride
+    G = cfg.H // cfg.Hkv
+    rng = np.random.default_rng(1)
+    for r in range(3):
+        q0, q1 = int(call.cu_q[r]), int(call.cu_q[r + 1])
+        kh = call.kh_lens[r]
+        kbh, qb_n = kh // cfg.block, (q1 - q0) // cfg.block
+        off = X.xattn_block_sums_offset(prob, r)
+        bs = bs_all[off:off + cfg.H * qb_n * (kbh + qb_n)].reshape(cfg.H, qb_n, kbh + qb_n)
+        mk = mask_all[off:off + bs.size].reshape(bs.shape)
+        qblocks = sorted({0, qb_n - 1, int(rng.integers(0, qb_n))})
+        for h in range(cfg.H):
+            hist = O.gather_history(kp, wl.block_table[r], kh, h // G)
+            ref = O.block_sums_qblocks(q[h, q0:q1], hist, k[h // G, q0:q1], cfg.stride,
+                                       cfg.block, scale, qblocks)
+            check_block_sums(bs[h, qblocks], ref, br, f"request {r} head {h}")
+        sel, pages = check_selection(bs, mk, sel_all[r], page_all[r], int(nsel[r]), tau,
+                                     cfg.Hkv, kbh, wl.block_table[r], f"request {r}")
+        rows = sorted({0, q1 - q0 - 1, *rng.integers(0, q1 - q0, 10).tolist()})
+        o_ref, l_ref = O.attend_request(q[:, q0:q1], k[:, q0:q1], v[:, q0:q1], kp, vp, pages,
+                                        cfg.H, cfg.Hkv, 1 / math.sqrt(cfg.D), rows=rows)
+        idx = q0 + np.asarray(rows)
+        check_attention(Og[:, idx], Lg[:, idx], o_ref, l_ref, f"request {r}")
+    assert nsel[0] == 0  # no history, no selection
+
+
+def test_lse_merge_matches_oracle():
+    rng = np.random.default_rng(4)
+    rows, D = 1000, 128
+    o1, o2 = rng.standard_normal((rows, D)), rng.standard_normal((rows, D))
+    l1, l2 = rng.standard_normal(rows) * 3, rng.standard_normal(rows) * 3
+    l1[:5] = -np.inf
+    l2[3:8] = -np.inf
+    d = dev()
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(d)
+    oo = torch.empty((rows, D), dtype=torch.float32, device=d)
+    lo = torch.empty(rows, dtype=torch.float32, device=d)
+    X.lse_merge(t(o1), t(l1), t(o2), t(l2), oo, lo)
+    ob = torch.empty((rows, D), dtype=torch.bfloat16, device=d)
+    lb = torch.empty(rows, dtype=torch.float32, device=d)
+    X.lse_merge(t(o1), t(l1), t(o2), t(l2), ob, lb)
+    torch.cuda.synchronize()
+    f32 = lambda a: a.astype(np.float32).astype(np.float64)
+    o_ref, l_ref = O.lse_merge(f32(o1), f32(l1), f32(o2), f32(l2))
+    assert np.abs(oo.cpu().numpy() - o_ref).max() < 1e-5
+    assert np.abs(ob.float().cpu().numpy() - o_ref).max() < 2e-2
+    lg = lo.cpu().numpy()
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    assert np.abs(lg[fin] - l_ref[fin]).max() < 1e-5
+    # in place: o_out aliases o1, lse_out aliases lse1
+    a, la = t(o1), t(l1)
+    X.lse_merge(a, la, t(o2), t(l2), a, la)
+    torch.cuda.synchronize()
+    assert np.abs(a.cpu().numpy() - o_ref).max() < 1e-5
+    assert np.abs(la.cpu().numpy()[fin] - l_ref[fin]).max() < 1e-5
+
+
+def test_unallocated_page_is_reported_not_trapped():
+    """A block-table entry of -1 inside the history is recorded in the device
+    error word; kernels skip the page and the context stays usable."""
+    case = SequenceCase("tiny")
+    X.xattn_device_error()  # clear
+    bt = case.BT.clone()
+    bt[0, 1] = -1
+    prob = X.Problem(case.cfg.H, case.cfg.Hkv, case.cfg.D, case.cfg.stride, case.cfg.block,
+                     [case.chunk], [2 * case.chunk], bt, case.KP.shape[0],
+                     q_head_stride=case.L * case.cfg.D, kv_head_stride=case.L * case.cfg.D,
+                     lse_head_stride=case.L)
+    bufs = RN.ChunkBuffers.for_problems([prob], dev())
+    O_ = torch.empty((case.cfg.H, case.L, case.cfg.D), dtype=torch.bfloat16, device=dev())
+    LSE = torch.empty((case.cfg.H, case.L), dtype=torch.float32, device=dev())
+    t0 = 2 * case.chunk
+    X.xattn_device_error(clear=True)  # clear anything an earlier test left
+    RN.prefill_chunk(prob, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], case.KP, case.VP, 0.9,
+                     bufs, O_[:, t0:], LSE[:, t0:])
+    code = X.xattn_device_error(clear=True)
+    assert code == -3
+    assert X.xattn_device_error() == 0
+    assert torch.isfinite(LSE[:, t0:]).all()
+
+
+def test_stream_ordering_side_stream_copy():
+    """History pages are written on a side stream and published with an event;
+    the compute stream waits on the event before estimation (the ordering the
+    stream-sync page prescribes).  Results equal a run with the pool already
+    resident."""
+    case = SequenceCase("tiny")
+    d = dev()
+    c = 3
+    t0 = c * case.chunk
+    ref = {}
+    prob = case.seq.problems[c]
+    host_k = case.KP.cpu().pin_memory()
+    host_v = case.VP.cpu().pin_memory()
+    for mode in ("resident", "side"):
+        kp = torch.zeros_like(case.KP)
+        vp = torch.zeros_like(case.VP)
+        bufs = RN.ChunkBuffers.for_problems([prob], d, with_mask=True)
+        O_ = torch.zeros((case.cfg.H, case.L, case.cfg.D), dtype=torch.bfloat16, device=d)
+        LSE = torch.zeros((case.cfg.H, case.L), dtype=torch.float32, device=d)
+        if mode == "resident":
+            kp.copy_(case.KP)
+            vp.copy_(case.VP)
+        torch.cuda.synchronize()
+        side, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        if mode == "side":
+            ev = torch.cuda.Event()
+            with torch.cuda.stream(side):
+                kp.copy_(host_k, non_blocking=True)
+                vp.copy_(host_v, non_blocking=True)
+                ev.record(side)
+            comp.wait_event(ev)
+        with torch.cuda.stream(comp):
+            RN.prefill_chunk(prob, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], kp, vp, 0.9,
+                             bufs, O_[:, t0:], LSE[:, t0:], stream=comp)
+        torch.cuda.synchronize()
+        ref[mode] = (bufs.block_sums.cpu().numpy(), bufs.sel_idx.cpu().numpy(),
+                     O_.float().cpu().numpy())
+    assert np.array_equal(ref["resident"][0], ref["side"][0])
+    assert np.array_equal(ref["resident"][1], ref["side"][1])
+    assert np.array_equal(ref["resident"][2], ref["side"][2])

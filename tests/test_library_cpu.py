@@ -1,0 +1,129 @@
+"""Host-side checks of libxattn that need no GPU: the library builds and loads,
+exports every entry point include/xattn.h declares, sizes its workspace as
+documented, and rejects invalid problems before touching CUDA.
+
+Every call below fails argument validation, which happens before any CUDA
+runtime call, so nothing here can reach a device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from xattention_block_sparse_gb300 import build as B
+from xattention_block_sparse_gb300 import xattn as X
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return X.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "xattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:size_t|xattn_status|const char \*)\s*(\w+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "xattn_estimate" in names and "bsa_chunk_attention" in names and "lse_merge" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(X.EXPORTED)
+
+
+class _FakeBT:
+    """Stands in for a device block table: only data_ptr/stride are read, and
+    only by validation that fails first."""
+
+    def __init__(self, B, W):
+        self.dtype = "torch.int32"
+        self._s = (W, 1)
+
+    def dim(self):
+        return 2
+
+    def stride(self, i):
+        return self._s[i]
+
+    def data_ptr(self):
+        return 0x10000
+
+
+def _prob(q_lens, kh_lens, H=16, Hkv=8, D=128, S=8, Bk=128, W=512, pages=1024, **kw):
+    return X.Problem(H, Hkv, D, S, Bk, q_lens, kh_lens, _FakeBT(len(q_lens), W), pages, **kw)
+
+
+def test_workspace_and_block_sum_sizes(lib):
+    # one 4096-token chunk with 28672 history tokens (last chunk of the 32K case)
+    p = _prob([4096], [28672])
+    H, rq, ncol = 16, 4096 // 8, 32768 // 8
+    scores = H * rq * ncol * 4
+    tstat = H * rq * (ncol // 128) * 8
+    rstat = H * rq * 8
+    al = lambda x: (x + 255) // 256 * 256
+    expect = al(al(al(scores) + tstat) + rstat) + al(512 * 4)
+    assert X.xattn_workspace_size(p) == expect
+    assert X.xattn_block_sums_count(p) == H * 32 * 256
+    # varlen batch: slabs packed request after request
+    v = _prob([8192, 3072, 1024], [0, 16384, 65536])
+    sizes = [16 * 64 * 64, 16 * 24 * (128 + 24), 16 * 8 * (512 + 8)]
+    assert X.xattn_block_sums_count(v) == sum(sizes)
+    assert [X.xattn_block_sums_offset(v, r) for r in range(3)] == [0, sizes[0], sizes[0] + sizes[1]]
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q_lens=[100], kh_lens=[0]),                 # not a multiple of the block
+    dict(q_lens=[128], kh_lens=[64]),
+    dict(q_lens=[128], kh_lens=[0], H=6, Hkv=4),     # H % Hkv
+    dict(q_lens=[128], kh_lens=[0], D=96),           # head_dim not built
+    dict(q_lens=[128], kh_lens=[0], S=3),            # block % stride
+    dict(q_lens=[128], kh_lens=[0], S=64),           # block/stride < 4
+    dict(q_lens=[128], kh_lens=[128 * 600], W=512),  # history beyond the table row
+    dict(q_lens=[128] * 65, kh_lens=[0] * 65),       # too many requests
+    dict(q_lens=[128], kh_lens=[0], q_head_stride=100),  # head stride too small
+    dict(q_lens=[128], kh_lens=[128 * 8200], W=9000),    # > 8192 blocks in a row
+])
+def test_invalid_problems_rejected(lib, kw):
+    p = _prob(**kw)
+    assert X.xattn_workspace_size(p) == 0
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.xattn_estimate(p.ref(), fake, fake, fake, 0.1, fake, 1 << 40, fake, None)
+    assert st in (-1, -5), st
+    st = lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,
+                                 fake, None)
+    assert st in (-1, -5), st
+
+
+def test_entry_point_argument_errors(lib):
+    p = _prob([1024], [1024])
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10002)
+    # null outputs, bad threshold, unaligned pointers, small workspace
+    assert lib.xattn_estimate(p.ref(), fake, fake, fake, 0.1, fake, 1 << 40, None, None) == -1
+    assert lib.xattn_estimate(p.ref(), odd, fake, fake, 0.1, fake, 1 << 40, fake, None) == -2
+    assert lib.xattn_estimate(p.ref(), fake, fake, fake, float("nan"), fake, 1 << 40, fake,
+                              None) == -1
+    assert lib.xattn_estimate(p.ref(), fake, fake, fake, 0.1, fake, 16, fake, None) == -6
+    for tau in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.xattn_select(p.ref(), fake, tau, fake, 1 << 40, None, fake, fake, fake,
+                                None) == -1
+    assert lib.xattn_select(p.ref(), fake, 0.9, fake, 16, None, fake, fake, fake, None) == -6
+    assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, odd,
+                                   fake, None) == -2
+    assert lib.lse_merge(fake, fake, fake, fake, 10, 6, fake, 0, fake, None) == -1
+    assert lib.lse_merge(fake, fake, fake, fake, -1, 128, fake, 0, fake, None) == -1
+    assert lib.lse_merge(odd, fake, fake, fake, 10, 128, fake, 0, fake, None) == -2
+    assert lib.lse_merge(None, None, None, None, 0, 128, None, 0, None, None) == 0
+    assert lib.xattn_status_string(-3) == b"page id outside the pool"
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        X.load_library(str(tmp_path / "nope.so"))

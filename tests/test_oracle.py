@@ -231,6 +231,13 @@ def test_block_sums_uniform_scores_closed_form():
     assert np.allclose(bs, exp, rtol=1e-14, atol=1e-15)
 
 
+def test_block_sums_of_sampled_query_blocks_match_full():
+    q, kh, kc, S, block = _rand_problem(5, lh=32, lq=32, S=4, block=8)
+    full = O.block_sums_one_head(q, kh, kc, S, block, 0.45)
+    part = O.block_sums_qblocks(q, kh, kc, S, block, 0.45, [0, 2, 3])
+    assert np.allclose(part, full[[0, 2, 3]], rtol=1e-13, atol=0)
+
+
 # ---------------------------------------------------------------------------
 # Threshold selection (find_blocks_chunked) by brute force
 # ---------------------------------------------------------------------------

@@ -1,0 +1,283 @@
+// C ABI of libxattn: argument validation, per-request geometry, workspace
+// layout and kernel launches.  See include/xattn.h for the contract.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace xattn {
+
+// Device error word: the first fault a kernel finds (XATTN_EPAGE, ...).
+__device__ int32_t g_err_word = 0;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  Geo geo;
+  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0;
+  int max_kb = 0;
+  size_t bs_count = 0;
+  WsLayout ws{};
+};
+
+inline bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Validates the problem and fills the plan (host only; no CUDA calls).
+xattn_status make_plan(const xattn_problem *p, Plan &pl) {
+  if (!p) return XATTN_EINVAL;
+  const int B = p->num_requests, H = p->num_heads, Hkv = p->num_kv_heads, D = p->head_dim,
+            S = p->stride, Bk = p->block_size;
+  if (B < 1 || B > kMaxReq || H < 1 || Hkv < 1 || H % Hkv != 0) return XATTN_EINVAL;
+  if (D != 64 && D != 128) return XATTN_EUNSUPPORTED;
+  if (S < 1 || S > 64 || Bk < 64 || Bk % 64 != 0 || Bk % S != 0) return XATTN_EUNSUPPORTED;
+  const int br = Bk / S;
+  if (!pow2(br) || br < 4 || br > 128) return XATTN_EUNSUPPORTED;
+  if (!p->cu_seqlens_q || !p->cu_seqlens_kh) return XATTN_EINVAL;
+  if (p->cu_seqlens_q[0] != 0) return XATTN_EINVAL;
+
+  Geo &g = pl.geo;
+  memset(&g, 0, sizeof(g));
+  g.B = B;
+  g.H = H;
+  g.Hkv = Hkv;
+  g.D = D;
+  g.S = S;
+  g.Bk = Bk;
+  g.bt_stride = p->bt_stride;
+  g.num_pages = p->num_pages;
+  g.q_hs = p->q_head_stride;
+  g.kv_hs = p->kv_head_stride;
+  g.lse_hs = p->lse_head_stride;
+  g.block_table = p->block_table;
+
+  int64_t gemm = 0, bsum = 0, sel = 0, att = 0;
+  size_t scores = 0, tstat = 0, rstat = 0, bs = 0;
+  bool any_hist = false;
+  for (int r = 0; r < B; ++r) {
+    const int64_t q0 = p->cu_seqlens_q[r], q1 = p->cu_seqlens_q[r + 1];
+    const int64_t kh = (int64_t)p->cu_seqlens_kh[r + 1] - p->cu_seqlens_kh[r];
+    const int64_t lq = q1 - q0;
+    if (lq < 0 || kh < 0 || lq % Bk || kh % Bk) return XATTN_EINVAL;
+    if (q1 > (int64_t)1 << 30 || kh > (int64_t)1 << 30) return XATTN_EINVAL;
+    const int64_t kbh = kh / Bk, qb = lq / Bk;
+    if (kbh + qb > XATTN_MAX_BLOCKS_PER_ROW) return XATTN_EUNSUPPORTED;
+    if (kbh > 0) {
+      any_hist = true;
+      if (kbh > p->bt_stride) return XATTN_EINVAL;
+    }
+    ReqDesc &d = g.req[r];
+    d.q0 = (int32_t)q0;
+    d.lq = (int32_t)lq;
+    d.kh = (int32_t)kh;
+    d.gemm0 = (int32_t)gemm;
+    d.bsum0 = (int32_t)bsum;
+    d.sel0 = (int32_t)sel;
+    d.att0 = (int32_t)att;
+    d.score_off = (int64_t)scores;
+    d.tstat_off = (int64_t)tstat;
+    d.rstat_off = (int64_t)rstat;
+    d.bs_off = (int64_t)bs;
+    const int64_t rq = lq / S, ncol = (kh + lq) / S;
+    const int64_t ntile = (ncol + kTileCols - 1) / kTileCols;
+    if (lq > 0) {
+      gemm += (int64_t)H * ((rq + 63) / 64) * ntile;
+      bsum += (int64_t)H * qb;
+      sel += (int64_t)Hkv * qb;
+      att += (int64_t)H * ((lq + 127) / 128);
+    }
+    scores += (size_t)H * rq * ncol;
+    tstat += (size_t)H * rq * ntile;
+    rstat += (size_t)H * rq;
+    bs += (size_t)H * qb * (kbh + qb);
+    if (kbh + qb > pl.max_kb) pl.max_kb = (int)(kbh + qb);
+  }
+  if (gemm > INT32_MAX || bsum > INT32_MAX || att > INT32_MAX) return XATTN_EUNSUPPORTED;
+  if (any_hist && (!p->block_table || p->num_pages < 1)) return XATTN_EINVAL;
+  if (p->bt_stride < 0) return XATTN_EINVAL;
+  const int64_t tot_q = p->cu_seqlens_q[B];
+  if (p->q_head_stride < tot_q * D || p->kv_head_stride < tot_q * D ||
+      p->lse_head_stride < tot_q)
+    return XATTN_EINVAL;
+  if (p->q_head_stride % 8 || p->kv_head_stride % 8) return XATTN_EALIGN;
+
+  pl.gemm_ctas = (int)gemm;
+  pl.bsum_ctas = (int)bsum;
+  pl.sel_ctas = (int)sel;
+  pl.att_ctas = (int)att;
+  pl.bs_count = bs;
+  WsLayout &w = pl.ws;
+  w.scores = 0;
+  w.tstat = align_up(w.scores + scores * sizeof(float));
+  w.rstat = align_up(w.tstat + tstat * sizeof(float2));
+  w.counts = align_up(w.rstat + rstat * sizeof(float2));
+  w.total = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
+                                    sizeof(int32_t));
+  return XATTN_OK;
+}
+
+inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+// Device address of the error word for the current device (cached per device).
+std::atomic<int32_t *> g_err_addr[64];
+
+xattn_status err_word(int32_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return XATTN_ECUDA;
+  if (dev < 64) {
+    int32_t *c = g_err_addr[dev].load(std::memory_order_acquire);
+    if (c) {
+      *out = c;
+      return XATTN_OK;
+    }
+  }
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_err_word) != cudaSuccess) return XATTN_ECUDA;
+  if (dev < 64) g_err_addr[dev].store(static_cast<int32_t *>(ptr), std::memory_order_release);
+  *out = static_cast<int32_t *>(ptr);
+  return XATTN_OK;
+}
+
+inline xattn_status cu(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XATTN_ECUDA; }
+
+}  // namespace
+}  // namespace xattn
+
+using namespace xattn;
+
+extern "C" {
+
+size_t xattn_workspace_size(const xattn_problem *p) {
+  Plan pl;
+  if (make_plan(p, pl) != XATTN_OK) return 0;
+  return pl.ws.total;
+}
+
+size_t xattn_block_sums_count(const xattn_problem *p) {
+  Plan pl;
+  if (make_plan(p, pl) != XATTN_OK) return 0;
+  return pl.bs_count;
+}
+
+size_t xattn_block_sums_offset(const xattn_problem *p, int32_t r) {
+  Plan pl;
+  if (make_plan(p, pl) != XATTN_OK || r < 0 || r >= p->num_requests) return 0;
+  return (size_t)pl.geo.req[r].bs_off;
+}
+
+xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k_cur,
+                            const void *k_pool, float scale, void *workspace,
+                            size_t workspace_bytes, float *block_sums, xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!q || !k_cur || !workspace || !block_sums) return XATTN_EINVAL;
+  if (!k_pool && pl.geo.num_pages > 0) return XATTN_EINVAL;
+  if (!isfinite(scale)) return XATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k_cur) || (k_pool && !aligned16(k_pool)) ||
+      !aligned16(workspace) || !aligned16(block_sums))
+    return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  char *ws = static_cast<char *>(workspace);
+  float *scores = reinterpret_cast<float *>(ws + pl.ws.scores);
+  float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
+  float2 *rstat = reinterpret_cast<float2 *>(ws + pl.ws.rstat);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, static_cast<const __nv_bfloat16 *>(q),
+                           static_cast<const __nv_bfloat16 *>(k_cur),
+                           static_cast<const __nv_bfloat16 *>(k_pool), scale, scores, tstat, st));
+  if (s != XATTN_OK) return s;
+  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, scores, tstat, rstat, block_sums, st));
+}
+
+xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,
+                          void *workspace, size_t workspace_bytes, uint8_t *mask,
+                          int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
+                          xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!block_sums || !workspace || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
+  if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
+  if (p->bt_stride < 1) return XATTN_EINVAL;
+  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_sums) & 3)) return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + pl.ws.counts);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  s = cu(cudaMemsetAsync(counts, 0, (size_t)pl.geo.B * p->bt_stride * sizeof(int32_t), st));
+  if (s != XATTN_OK) return s;
+  s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
+  if (s != XATTN_OK) return s;
+  return cu(launch_vote(pl.geo, counts, sel_idx, sel_page, n_sel, st));
+}
+
+xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
+                                 const void *v_cur, const void *k_pool, const void *v_pool,
+                                 const int32_t *sel_page, const int32_t *n_sel,
+                                 float softmax_scale, void *o, float *lse, xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse) return XATTN_EINVAL;
+  if ((!k_pool || !v_pool) && pl.geo.num_pages > 0) return XATTN_EINVAL;
+  if (p->bt_stride < 1) return XATTN_EINVAL;
+  if (!isfinite(softmax_scale)) return XATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(o) ||
+      (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)))
+    return XATTN_EALIGN;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cu(launch_attention(pl.geo, pl.att_ctas, static_cast<const __nv_bfloat16 *>(q),
+                             static_cast<const __nv_bfloat16 *>(k_cur),
+                             static_cast<const __nv_bfloat16 *>(v_cur),
+                             static_cast<const __nv_bfloat16 *>(k_pool),
+                             static_cast<const __nv_bfloat16 *>(v_pool), sel_page, n_sel,
+                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse, st));
+}
+
+xattn_status lse_merge(const float *o1, const float *lse1, const float *o2, const float *lse2,
+                       int64_t rows, int32_t head_dim, void *o_out, int32_t o_out_bf16,
+                       float *lse_out, xattn_stream_t stream) {
+  if (rows < 0 || head_dim < 4 || head_dim % 4 != 0) return XATTN_EINVAL;
+  if (rows == 0) return XATTN_OK;
+  if (!o1 || !lse1 || !o2 || !lse2 || !o_out || !lse_out) return XATTN_EINVAL;
+  if (!aligned16(o1) || !aligned16(o2) || !aligned16(o_out)) return XATTN_EALIGN;
+  if (o_out_bf16 && head_dim % 8 != 0) return XATTN_EALIGN;
+  return cu(launch_lse_merge(o1, lse1, o2, lse2, rows, head_dim, o_out, o_out_bf16 ? 1 : 0,
+                             lse_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t clear) {
+  if (!code) return XATTN_EINVAL;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return XATTN_ECUDA;
+  int32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(v)) != cudaSuccess) return XATTN_ECUDA;
+  if (clear) {
+    const int32_t z = 0;
+    if (cudaMemcpyToSymbol(g_err_word, &z, sizeof(z)) != cudaSuccess) return XATTN_ECUDA;
+  }
+  *code = v;
+  return XATTN_OK;
+}
+
+const char *xattn_status_string(xattn_status s) {
+  switch (s) {
+    case XATTN_OK: return "ok";
+    case XATTN_EINVAL: return "invalid argument";
+    case XATTN_EALIGN: return "pointer or stride not 16-byte aligned";
+    case XATTN_EPAGE: return "page id outside the pool";
+    case XATTN_ECUDA: return "CUDA runtime error";
+    case XATTN_EUNSUPPORTED: return "unsupported geometry";
+    case XATTN_EWORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Internal definitions shared by the libxattn translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "xattn.h"
+
+namespace xattn {
+
+constexpr int kMaxReq = XATTN_MAX_REQUESTS;
+constexpr int kTileCols = 128;  // columns of one softmax-statistics tile (score GEMM N tile)
+
+// Per-request geometry of one chunk call (host-computed, passed by value).
+struct ReqDesc {
+  int32_t q0;      // first query token of the request in the packed token axis
+  int32_t lq;      // query tokens (current chunk)
+  int32_t kh;      // history tokens
+  int32_t gemm0;   // first CTA of the request in the score-GEMM grid
+  int32_t bsum0;   // ... in the block-sum grid
+  int32_t sel0;    // ... in the selection grid
+  int32_t att0;    // ... in the attention grid
+  int32_t pad_;
+  int64_t score_off;  // float offset of the request's [H, lq/S, (kh+lq)/S] scores
+  int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
+  int64_t rstat_off;  // float2 offset of its [H, lq/S] merged statistics
+  int64_t bs_off;     // offset of its [H, Qb, Kb] block sums / mask
+};
+
+struct Geo {
+  int32_t B, H, Hkv, D, S, Bk, bt_stride, num_pages;
+  int64_t q_hs, kv_hs, lse_hs;
+  const int32_t *block_table;
+  int32_t *err;  // device error word
+  ReqDesc req[kMaxReq];
+};
+
+// Request owning CTA `cta` of the grid whose per-request start is selected by F.
+template <typename F>
+__device__ __forceinline__ int find_req(const Geo &g, int cta, F start) {
+  int r = 0;
+  for (int i = 1; i < g.B; ++i)
+    if (cta >= start(g.req[i])) r = i;
+  return r;
+}
+
+__device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
+  atomicCAS(err, 0, code);
+}
+
+// Page id of logical block j of request r, or -1 (and an error record) when the
+// block table entry is outside [0, num_pages).
+__device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
+  int p = __ldg(g.block_table + (int64_t)r * g.bt_stride + j);
+  if (p < 0 || p >= g.num_pages) {
+    record_error(g.err, XATTN_EPAGE);
+    return -1;
+  }
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// Launch entry points implemented in the kernel translation units.
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  size_t scores, tstat, rstat, counts, total;
+};
+
+cudaError_t launch_score_gemm(const Geo &g, int nctas, const __nv_bfloat16 *q,
+                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
+                              float *scores, float2 *tstat, cudaStream_t st);
+cudaError_t launch_block_sum(const Geo &g, int nctas, const float *scores, const float2 *tstat,
+                             float2 *rstat, float *block_sums, cudaStream_t st);
+cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
+                          double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st);
+cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx,
+                        int32_t *sel_page, int32_t *n_sel, cudaStream_t st);
+cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
+                             const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
+                             const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,
+                             const int32_t *sel_page, const int32_t *n_sel, float scale,
+                             __nv_bfloat16 *o, float *lse, cudaStream_t st);
+cudaError_t launch_lse_merge(const float *o1, const float *l1, const float *o2, const float *l2,
+                             int64_t rows, int D, void *o_out, int bf16_out, float *l_out,
+                             cudaStream_t st);
+
+}  // namespace xattn

@@ -1,0 +1,194 @@
+// Selection kernels of XAttention BSA ("XAttention BSA Policy 设计文档",
+// select_blocks Step 3 find_blocks_chunked and Step 4 GQA-aware aggregation +
+// majority voting).
+//
+//   select_kernel  one CTA per (request, KV head, query block).  For each query
+//                  head of the group: integer masses q_j = rne(bs_j * 2^32),
+//                  bitonic sort of (q_j desc, j asc), exclusive prefix of the
+//                  sorted masses, keep iff prefix < fl64(tau * T).  The group's
+//                  "any" over its heads then votes once per history block.
+//   vote_kernel    one CTA per request: majority test 2*votes > Hkv*Qb, sink and
+//                  last history block forced, ascending compaction, page lookup.
+//
+// Every step is integer or exactly rounded, so the result does not depend on
+// the order in which threads add or compare.
+#include "common.cuh"
+
+namespace xattn {
+namespace {
+
+constexpr int STHR = 512;
+constexpr int SWARPS = STHR / 32;
+
+__device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive block-wide prefix of one value per thread; *total gets the sum.
+__device__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long *wbuf,
+                                              unsigned long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long incl = warp_incl_scan(v, lane);
+  if (lane == 31) wbuf[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < SWARPS ? wbuf[lane] : 0ull;
+    const unsigned long long wi = warp_incl_scan(w, lane);
+    if (lane < SWARPS) wbuf[lane] = wi - w;
+    if (lane == SWARPS - 1) wbuf[SWARPS] = wi;
+  }
+  __syncthreads();
+  const unsigned long long res = wbuf[warp] + incl - v;
+  *total = wbuf[SWARPS];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Geo g,
+                                                      const float *__restrict__ bs, double tau,
+                                                      uint8_t *__restrict__ mask,
+                                                      int32_t *__restrict__ counts) {
+  extern __shared__ unsigned long long keys[];  // [npad] then any-flags
+  __shared__ unsigned long long wbuf[SWARPS + 1];
+  const int cta = blockIdx.x;
+  const int r = find_req(g, cta, [](const ReqDesc &d) { return d.sel0; });
+  const ReqDesc &R = g.req[r];
+  const int Qb = R.lq / g.Bk, kbh = R.kh / g.Bk, Kb = kbh + Qb;
+  const int local = cta - R.sel0;
+  const int qb = local % Qb, kvh = local / Qb;
+  const int G = g.H / g.Hkv;
+  int npad = 1;
+  while (npad < Kb) npad <<= 1;
+  uint8_t *anyf = reinterpret_cast<uint8_t *>(keys + npad);
+  const int tid = threadIdx.x;
+
+  for (int j = tid; j < kbh; j += STHR) anyf[j] = 0;
+
+  for (int gi = 0; gi < G; ++gi) {
+    const int h = kvh * G + gi;
+    const int64_t row_off = R.bs_off + ((int64_t)h * Qb + qb) * Kb;
+    const float *row = bs + row_off;
+    unsigned long long tsum = 0;
+    for (int j = tid; j < npad; j += STHR) {
+      unsigned long long key = 0ull;
+      if (j < Kb) {
+        const float v = row[j];
+        // v * 2^32 is exact in fp32; the conversion rounds half to even
+        const unsigned long long qv = v > 0.f ? __float2ull_rn(v * 4294967296.0f) : 0ull;
+        tsum += qv;
+        key = (qv << 16) | (unsigned long long)(0xFFFF - j);
+      }
+      keys[j] = key;
+    }
+    unsigned long long T;
+    block_excl_scan(tsum, wbuf, &T);  // also orders the key writes before the sort
+
+    // bitonic sort, descending
+    for (int k = 2; k <= npad; k <<= 1) {
+      for (int jj = k >> 1; jj > 0; jj >>= 1) {
+        for (int i = tid; i < npad; i += STHR) {
+          const int ixj = i ^ jj;
+          if (ixj > i) {
+            const unsigned long long x = keys[i], y = keys[ixj];
+            const bool desc = (i & k) == 0;
+            if (desc ? (x < y) : (x > y)) {
+              keys[i] = y;
+              keys[ixj] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+
+    // exclusive prefix of the sorted masses; each thread owns a contiguous run
+    const int per = (npad + STHR - 1) / STHR;
+    const int beg = min(tid * per, npad), end = min(beg + per, npad);
+    unsigned long long run = 0;
+    for (int i = beg; i < end; ++i) run += keys[i] >> 16;
+    unsigned long long tot;
+    unsigned long long pre = block_excl_scan(run, wbuf, &tot);
+    const double Rth = __dmul_rn(tau, (double)T);
+    for (int i = beg; i < end; ++i) {
+      const unsigned long long key = keys[i];
+      const unsigned long long qv = key >> 16;
+      const int idx = 0xFFFF - (int)(key & 0xFFFFull);
+      if (idx < Kb) {
+        const bool keep = tau >= 1.0 ? (qv > 0ull) : ((double)pre < Rth);
+        if (mask) mask[row_off + idx] = keep ? 1 : 0;
+        if (keep && idx < kbh) anyf[idx] = 1;
+      }
+      pre += qv;
+    }
+    __syncthreads();
+  }
+  for (int j = tid; j < kbh; j += STHR)
+    if (anyf[j]) atomicAdd(counts + (int64_t)r * g.bt_stride + j, 1);
+}
+
+constexpr int VTHR = 512;
+
+__global__ void __launch_bounds__(VTHR) vote_kernel(const __grid_constant__ Geo g,
+                                                    const int32_t *__restrict__ counts,
+                                                    int32_t *__restrict__ sel_idx,
+                                                    int32_t *__restrict__ sel_page,
+                                                    int32_t *__restrict__ n_sel) {
+  __shared__ unsigned long long wbuf[SWARPS + 1];
+  const int r = blockIdx.x;
+  const ReqDesc &R = g.req[r];
+  const int kbh = R.kh / g.Bk, Qb = R.lq / g.Bk;
+  const int votes_total = g.Hkv * Qb;
+  const int tid = threadIdx.x;
+  const int per = (kbh + VTHR - 1) / VTHR;
+  const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
+  const int32_t *cnt = counts + (int64_t)r * g.bt_stride;
+  auto keep = [&](int j) { return 2 * cnt[j] > votes_total || j == 0 || j == kbh - 1; };
+  unsigned long long mine = 0;
+  for (int j = beg; j < end; ++j) mine += keep(j) ? 1 : 0;
+  unsigned long long total;
+  unsigned long long pos = block_excl_scan(mine, wbuf, &total);
+  for (int j = beg; j < end; ++j) {
+    if (keep(j)) {
+      const int64_t o = (int64_t)r * g.bt_stride + (int64_t)pos;
+      sel_idx[o] = j;
+      int p = g.block_table[(int64_t)r * g.bt_stride + j];
+      if (p < 0 || p >= g.num_pages) {
+        record_error(g.err, XATTN_EPAGE);
+        p = -1;
+      }
+      sel_page[o] = p;
+      ++pos;
+    }
+  }
+  if (tid == 0) n_sel[r] = (int32_t)total;
+}
+
+}  // namespace
+
+cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
+                          double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st) {
+  if (nctas == 0) return cudaSuccess;
+  int npad = 1;
+  while (npad < max_kb) npad <<= 1;
+  const size_t smem = (size_t)npad * sizeof(unsigned long long) + (size_t)npad;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx, int32_t *sel_page,
+                        int32_t *n_sel, cudaStream_t st) {
+  vote_kernel<<<g.B, VTHR, 0, st>>>(g, counts, sel_idx, sel_page, n_sel);
+  return cudaGetLastError();
+}
+
+}  // namespace xattn

@@ -1,0 +1,216 @@
+"""ctypes binding of libxattn (include/xattn.h), same names as the C ABI.
+
+Argument marshalling only: tensors are passed as raw pointers of torch CUDA
+tensors and every step runs in the library's kernels.  The library must have
+been built (``__graft_entry__.build()`` or ``python -m
+xattention_block_sparse_gb300.build``); a missing library raises, there is no
+other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libxattn.so")
+
+XATTN_MAX_REQUESTS = 64
+XATTN_MAX_BLOCKS_PER_ROW = 8192
+
+STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAGE",
+          -4: "XATTN_ECUDA", -5: "XATTN_EUNSUPPORTED", -6: "XATTN_EWORKSPACE"}
+
+EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
+            "xattn_estimate", "xattn_select", "bsa_chunk_attention", "lse_merge",
+            "xattn_device_error", "xattn_status_string"]
+
+
+class XattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class xattn_problem(ctypes.Structure):
+    _fields_ = [
+        ("num_requests", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("stride", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
+        ("cu_seqlens_kh", ctypes.POINTER(ctypes.c_int32)),
+        ("block_table", ctypes.c_void_p),
+        ("bt_stride", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("q_head_stride", ctypes.c_int64),
+        ("kv_head_stride", ctypes.c_int64),
+        ("lse_head_stride", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Open libxattn (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"libxattn not built ({p} missing): run __graft_entry__.build() first")
+    lib = ctypes.CDLL(p)
+    P = ctypes.POINTER(xattn_problem)
+    vp, i32, i64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+    sig = {
+        "xattn_workspace_size": (sz, [P]),
+        "xattn_block_sums_count": (sz, [P]),
+        "xattn_block_sums_offset": (sz, [P, i32]),
+        "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
+        "xattn_select": (ctypes.c_int, [P, vp, f64, vp, sz, vp, vp, vp, vp, vp]),
+        "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp]),
+        "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
+        "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
+        "xattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# Problem description
+# ---------------------------------------------------------------------------
+
+
+class Problem:
+    """Host-side xattn_problem plus the host arrays it points to.
+
+    q_lens / kh_lens: per-request query-chunk and history token counts;
+    block_table: DEVICE int32 tensor [B, bt_stride] (or None without history);
+    strides are element strides between heads of q/o, k_cur/v_cur and lse."""
+
+    def __init__(self, num_heads, num_kv_heads, head_dim, stride, block_size, q_lens, kh_lens,
+                 block_table=None, num_pages=0, q_head_stride=None, kv_head_stride=None,
+                 lse_head_stride=None):
+        self.q_lens = [int(x) for x in q_lens]
+        self.kh_lens = [int(x) for x in kh_lens]
+        B = len(self.q_lens)
+        self.cu_q = np.zeros(B + 1, dtype=np.int32)
+        self.cu_kh = np.zeros(B + 1, dtype=np.int32)
+        self.cu_q[1:] = np.cumsum(self.q_lens)
+        self.cu_kh[1:] = np.cumsum(self.kh_lens)
+        tot = int(self.cu_q[-1])
+        self.block_table = block_table
+        bt_ptr, bt_stride = None, 0
+        if block_table is not None:
+            assert block_table.dtype.__str__().endswith("int32") and block_table.dim() == 2
+            assert block_table.stride(1) == 1
+            bt_ptr, bt_stride = block_table.data_ptr(), block_table.stride(0)
+        self.c = xattn_problem(
+            B, num_heads, num_kv_heads, head_dim, stride, block_size,
+            self.cu_q.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            self.cu_kh.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            bt_ptr, bt_stride, num_pages,
+            q_head_stride if q_head_stride is not None else tot * head_dim,
+            kv_head_stride if kv_head_stride is not None else tot * head_dim,
+            lse_head_stride if lse_head_stride is not None else tot)
+
+    @property
+    def B(self):
+        return self.c.num_requests
+
+    @property
+    def bt_stride(self):
+        return self.c.bt_stride
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status, what):
+    if status != 0:
+        raise XattnError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+
+
+def xattn_workspace_size(problem: Problem) -> int:
+    return int(load_library().xattn_workspace_size(problem.ref()))
+
+
+def xattn_block_sums_count(problem: Problem) -> int:
+    return int(load_library().xattn_block_sums_count(problem.ref()))
+
+
+def xattn_block_sums_offset(problem: Problem, r: int) -> int:
+    return int(load_library().xattn_block_sums_offset(problem.ref(), r))
+
+
+def xattn_estimate(problem, q, k_cur, k_pool, scale, workspace, block_sums, stream=None):
+    st = load_library().xattn_estimate(problem.ref(), _ptr(q), _ptr(k_cur), _ptr(k_pool),
+                                       float(scale), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _ptr(block_sums), _stream(stream))
+    _check(st, "xattn_estimate")
+
+
+def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_page, n_sel,
+                 stream=None):
+    st = load_library().xattn_select(problem.ref(), _ptr(block_sums), float(threshold),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _ptr(mask), _ptr(sel_idx), _ptr(sel_page), _ptr(n_sel),
+                                     _stream(stream))
+    _check(st, "xattn_select")
+
+
+def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
+                        o, lse, stream=None):
+    st = load_library().bsa_chunk_attention(problem.ref(), _ptr(q), _ptr(k_cur), _ptr(v_cur),
+                                            _ptr(k_pool), _ptr(v_pool), _ptr(sel_page),
+                                            _ptr(n_sel), float(softmax_scale), _ptr(o), _ptr(lse),
+                                            _stream(stream))
+    _check(st, "bsa_chunk_attention")
+
+
+def lse_merge(o1, lse1, o2, lse2, o_out, lse_out, stream=None):
+    rows, d = o1.shape[0], o1.shape[-1]
+    bf16 = 1 if str(o_out.dtype).endswith("bfloat16") else 0
+    st = load_library().lse_merge(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), rows, d,
+                                  _ptr(o_out), bf16, _ptr(lse_out), _stream(stream))
+    _check(st, "lse_merge")
+
+
+def xattn_device_error(stream=None, clear: bool = True) -> int:
+    code = ctypes.c_int32(0)
+    st = load_library().xattn_device_error(_stream(stream), ctypes.byref(code), 1 if clear else 0)
+    _check(st, "xattn_device_error")
+    return int(code.value)
+
+
+def xattn_status_string(status: int) -> str:
+    return load_library().xattn_status_string(status).decode()
