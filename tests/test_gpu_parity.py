@@ -225,7 +225,8 @@ def test_stream_ordering_side_stream_copy():
             RN.prefill_chunk(prob, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], kp, vp, 0.9,
                              bufs, O_[:, t0:], LSE[:, t0:], stream=comp)
         torch.cuda.synchronize()
-        ref[mode] = (bufs.block_sums.cpu().numpy(), bufs.sel_idx.cpu().numpy(),
+        n = int(bufs.n_sel[0].item())
+        ref[mode] = (bufs.block_sums.cpu().numpy(), bufs.sel_idx[0, :n].cpu().numpy(),
                      O_.float().cpu().numpy())
     assert np.array_equal(ref["resident"][0], ref["side"][0])
     assert np.array_equal(ref["resident"][1], ref["side"][1])
