@@ -158,6 +158,32 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
                           int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
                           xattn_stream_t stream);
 
+/* Capacity of the fixed counter array behind xattn_select_noalloc:
+ * num_requests * bt_stride must not exceed it (1 MiB of int32 counters). */
+#define XATTN_NOALLOC_MAX_COUNTERS 262144
+
+/* Selection for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this exists for integrations where the caller has no
+ * allocator to give the library scratch -- a serving process that hands all
+ * free HBM to its KV-page pool and weights at start-up, or a C caller without
+ * a caching allocator, for whom a cudaMalloc on the prefill path would block
+ * the device or fail.  Same arguments, semantics and outputs as xattn_select
+ * minus the workspace: the per-request vote counters live in a static device
+ * array inside the library (XATTN_NOALLOC_MAX_COUNTERS int32, held by every
+ * GPU that loads the library until the process exits).
+ *  - Sizes: num_requests * bt_stride > XATTN_NOALLOC_MAX_COUNTERS returns
+ *    XATTN_EWORKSPACE with nothing enqueued.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call clears the counters it uses on `stream`, then reuses the one
+ *    array: calls that can overlap on the GPU (other streams, other host
+ *    threads) race on it and must be ordered by the caller.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
+                                  double threshold, uint8_t *mask, int32_t *sel_idx,
+                                  int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream);
+
 /* Sparse chunk attention (BSA policy page, compute_chunked_prefill).  For each
  * query token i of request r and head h, softmax attention with scale
  * softmax_scale over the keys of the selected history pages

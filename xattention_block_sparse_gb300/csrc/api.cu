@@ -147,6 +147,38 @@ inline xattn_status cu(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XAT
 }  // namespace
 }  // namespace xattn
 
+// Vote counters of xattn_select_noalloc: a fixed array the library owns, for
+// callers that cannot hand it any scratch.  Shared by every call on a device.
+static __device__ __align__(256) int32_t xattn_noalloc_counters[XATTN_NOALLOC_MAX_COUNTERS];
+
+namespace xattn {
+namespace {
+
+// Device address of xattn_noalloc_counters for the current device, looked up
+// once per device (the host-side symbol is not a device address).
+std::atomic<int32_t *> g_noalloc_addr[64];
+
+xattn_status noalloc_counters(int32_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return XATTN_ECUDA;
+  if (dev < 64) {
+    int32_t *c = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (c) {
+      *out = c;
+      return XATTN_OK;
+    }
+  }
+  int32_t *ptr = nullptr;
+  if (cudaGetSymbolAddress((void **)&ptr, xattn_noalloc_counters) != cudaSuccess || !ptr)
+    return XATTN_ECUDA;
+  if (dev < 64) g_noalloc_addr[dev].store(ptr, std::memory_order_release);
+  *out = ptr;
+  return XATTN_OK;
+}
+
+}  // namespace
+}  // namespace xattn
+
 using namespace xattn;
 
 extern "C" {
@@ -211,6 +243,30 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
   int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + pl.ws.counts);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   s = cu(cudaMemsetAsync(counts, 0, (size_t)pl.geo.B * p->bt_stride * sizeof(int32_t), st));
+  if (s != XATTN_OK) return s;
+  s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
+  if (s != XATTN_OK) return s;
+  return cu(launch_vote(pl.geo, counts, sel_idx, sel_page, n_sel, st));
+}
+
+xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
+                                  double threshold, uint8_t *mask, int32_t *sel_idx,
+                                  int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!block_sums || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
+  if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
+  if (p->bt_stride < 1) return XATTN_EINVAL;
+  if (reinterpret_cast<uintptr_t>(block_sums) & 3) return XATTN_EALIGN;
+  const size_t n_counters = (size_t)pl.geo.B * (size_t)p->bt_stride;
+  if (n_counters > (size_t)XATTN_NOALLOC_MAX_COUNTERS) return XATTN_EWORKSPACE;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  int32_t *counts = nullptr;
+  if ((s = noalloc_counters(&counts)) != XATTN_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's votes: clear the part this call uses
+  s = cu(cudaMemsetAsync(counts, 0, n_counters * sizeof(int32_t), st));
   if (s != XATTN_OK) return s;
   s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
   if (s != XATTN_OK) return s;

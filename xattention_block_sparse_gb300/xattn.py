@@ -18,12 +18,14 @@ LIB_PATH = os.path.join(_PKG, "_build", "libxattn.so")
 
 XATTN_MAX_REQUESTS = 64
 XATTN_MAX_BLOCKS_PER_ROW = 8192
+XATTN_NOALLOC_MAX_COUNTERS = 262144
 
 STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAGE",
           -4: "XATTN_ECUDA", -5: "XATTN_EUNSUPPORTED", -6: "XATTN_EWORKSPACE"}
 
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
-            "xattn_estimate", "xattn_select", "bsa_chunk_attention", "lse_merge",
+            "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
+            "lse_merge",
             "xattn_device_error", "xattn_status_string"]
 
 
@@ -74,6 +76,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "xattn_block_sums_offset": (sz, [P, i32]),
         "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
         "xattn_select": (ctypes.c_int, [P, vp, f64, vp, sz, vp, vp, vp, vp, vp]),
+        "xattn_select_noalloc": (ctypes.c_int, [P, vp, f64, vp, vp, vp, vp, vp]),
         "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp]),
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
@@ -186,6 +189,17 @@ def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_p
                                      _ptr(mask), _ptr(sel_idx), _ptr(sel_page), _ptr(n_sel),
                                      _stream(stream))
     _check(st, "xattn_select")
+
+
+def xattn_select_noalloc(problem, block_sums, threshold, mask, sel_idx, sel_page, n_sel,
+                         stream=None):
+    """xattn_select without a workspace, for callers that cannot allocate device
+    memory on the prefill path; its vote counters live in a fixed array inside
+    the library (one per GPU), so calls that overlap on the GPU race."""
+    st = load_library().xattn_select_noalloc(problem.ref(), _ptr(block_sums), float(threshold),
+                                             _ptr(mask), _ptr(sel_idx), _ptr(sel_page),
+                                             _ptr(n_sel), _stream(stream))
+    _check(st, "xattn_select_noalloc")
 
 
 def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
