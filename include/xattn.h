@@ -53,7 +53,8 @@
  *            (a page id outside [0, num_pages) reached through block_table or
  *            the selection) never trap: the kernel skips the page, records the
  *            first such fault in a device error word and continues; read it
- *            with xattn_device_error.
+ *            with xattn_device_error.  Every wait inside a kernel is bounded:
+ *            one that runs out records XATTN_ETIMEOUT and the kernel returns.
  */
 #ifndef XATTN_H
 #define XATTN_H
@@ -74,7 +75,9 @@ typedef enum xattn_status {
   XATTN_EPAGE = -3,           /* (device word) page id out of range */
   XATTN_ECUDA = -4,           /* a CUDA runtime call or launch failed */
   XATTN_EUNSUPPORTED = -5,    /* head_dim / block geometry not built */
-  XATTN_EWORKSPACE = -6       /* workspace smaller than xattn_workspace_size */
+  XATTN_EWORKSPACE = -6,      /* workspace smaller than xattn_workspace_size */
+  XATTN_ETIMEOUT = -7         /* (device word) a kernel pipeline wait ran out; the
+                                 kernel stopped early and its outputs are invalid */
 } xattn_status;
 
 #define XATTN_MAX_REQUESTS 64

@@ -332,6 +332,7 @@ const char *xattn_status_string(xattn_status s) {
     case XATTN_ECUDA: return "CUDA runtime error";
     case XATTN_EUNSUPPORTED: return "unsupported geometry";
     case XATTN_EWORKSPACE: return "workspace too small";
+    case XATTN_ETIMEOUT: return "kernel pipeline wait timed out";
   }
   return "unknown status";
 }

@@ -21,7 +21,8 @@ XATTN_MAX_BLOCKS_PER_ROW = 8192
 XATTN_NOALLOC_MAX_COUNTERS = 262144
 
 STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAGE",
-          -4: "XATTN_ECUDA", -5: "XATTN_EUNSUPPORTED", -6: "XATTN_EWORKSPACE"}
+          -4: "XATTN_ECUDA", -5: "XATTN_EUNSUPPORTED", -6: "XATTN_EWORKSPACE",
+          -7: "XATTN_ETIMEOUT"}
 
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
             "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
