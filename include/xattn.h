@@ -193,6 +193,7 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
  * (sel_page[r][0..n_sel[r]), all visible) and the current-chunk keys j <= i;
  * the history and causal parts are merged online by log-sum-exp, so the result
  * equals flash_attn_with_lse(history) merged with flash_attn_with_lse(causal).
+ *   softmax_scale  > 0 (usually 1/sqrt(D)); XATTN_EINVAL otherwise
  *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
  *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE */
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,

@@ -88,7 +88,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
       gemm += (int64_t)H * ((rq + 63) / 64) * ntile;
       bsum += (int64_t)H * qb;
       sel += (int64_t)Hkv * qb;
-      att += (int64_t)H * ((lq + 127) / 128);
+      att += (int64_t)H * ((lq + kAttnRows - 1) / kAttnRows);
     }
     scores += (size_t)H * rq * ncol;
     tstat += (size_t)H * rq * ntile;
@@ -283,7 +283,7 @@ xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const vo
   if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse) return XATTN_EINVAL;
   if ((!k_pool || !v_pool) && pl.geo.num_pages > 0) return XATTN_EINVAL;
   if (p->bt_stride < 1) return XATTN_EINVAL;
-  if (!isfinite(softmax_scale)) return XATTN_EINVAL;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return XATTN_EINVAL;
   if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(o) ||
       (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)))
     return XATTN_EALIGN;

@@ -5,20 +5,27 @@
 // flash_attn_with_lse(history) merged with flash_attn_with_lse(current, causal)
 // by merge_attention_outputs.
 //
-// tcgen05 design.  One CTA = 128 query rows of one (request, head).
-//   warp 0       TMA producer: Q tile once, then K and V tiles (one page of up to
-//                128 keys each) through an NST-stage ring; history tiles are
-//                gathered page by page from the pool through the selection's
-//                page list, then the current chunk up to the diagonal.
-//   warp 1       MMA issuer: S = Q K^T into one of two TMEM buffers (128 lanes x
-//                NK fp32 columns), then O += P V into a TMEM accumulator.
-//   warps 4..7   softmax: thread i owns query row i (TMEM lane i).  It loads its
-//                S row, applies scale and causal mask, keeps a running max
-//                (rescaling O in TMEM only when the max grows by more than
-//                2^8), writes P as bf16 into 128B-swizzled shared memory for
-//                the P V MMA, and finally normalises O and writes O and LSE.
+// tcgen05 design.  One CTA = two 128-row query tiles (A and B) of one
+// (request, head), sharing every K/V tile:
+//   warp 0        TMA producer: both Q tiles once, then K(t), V(t) for each KV
+//                 tile t (one page of up to 128 keys) through a 3-slot ring of
+//                 128B-swizzled tiles.  History tiles are gathered page by page
+//                 through the selection's page list, then the current chunk up
+//                 to the diagonal.
+//   warp 1        MMA issuer, in the order PV_A(t), S_A(t+1), PV_B(t), S_B(t+1):
+//                 S_x = Q_x K^T into TMEM (128 lanes x NK fp32 columns), then
+//                 O_x += P_x V into a TMEM accumulator.  While one tile's
+//                 softmax runs, the tensor pipe works for the other tile.
+//   warps 4..7    softmax of tile A, warps 8..11 softmax of tile B: thread i
+//                 owns query row i (TMEM lane i).  It loads its S row, masks
+//                 the causal diagonal tile, keeps a running max (rescaling O in
+//                 TMEM only when the max grows by more than 2^8), writes P as
+//                 bf16 into swizzled shared memory for the P V MMA, and at the
+//                 end normalises O and writes O and LSE.
+// Because each thread's tcgen05 ops complete in issue order, S_x(t) being
+// ready implies PV_x(t-1) has finished: P_x and O_x are free at that point.
 // Every mbarrier wait is bounded; a timeout records XATTN_ETIMEOUT and the CTA
-// unwinds (waiting for its own TMA loads and MMAs, then freeing TMEM).
+// unwinds (draining its TMA loads and MMAs, then freeing TMEM).
 #include <cudaTypedefs.h>
 
 #include "tc_common.cuh"
@@ -27,36 +34,34 @@ namespace xattn {
 namespace {
 using namespace tc;
 
-constexpr int BM = 128;      // query rows per CTA
-constexpr int NST = 2;       // K/V pipeline stages
-constexpr int THREADS = 256;
-constexpr int TMEM_COLS = 512;
-constexpr int TM_S = 0;      // S buffers at columns 0 and 128
-constexpr int TM_O = 256;    // O accumulator at columns 256 .. 256+D
+constexpr int BM = 128;       // rows per query tile (MMA M)
+constexpr int ROWS = 2 * BM;  // query rows per CTA
+static_assert(ROWS == kAttnRows, "host grid sizing assumes kAttnRows rows per CTA");
+constexpr int NSLOT = 3;      // K/V ring slots
+constexpr int THREADS = 384;
+constexpr int TMEM_COLS = 512;  // S_A | S_B | O_A | O_B, 128 columns each
 
 template <int D, int NK>
 struct Layout {
-  static constexpr int HALVES = D / 64;             // 64-element (128 B) column blocks
+  static constexpr int HALVES = D / 64;  // 64-element (128 B) column blocks
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = NK * D * 2;
   static constexpr int P_BYTES = BM * NK * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_Q = 0;                       // Q_A, Q_B
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
+  static constexpr int OFF_KV = OFF_P + 2 * P_BYTES;    // ring
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
   static constexpr int BYTES = OFF_BAR + 256;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[NST];
-  uint64_t v_full[NST];
-  uint64_t kv_empty[NST];
+  uint64_t full[NSLOT];
+  uint64_t empty[NSLOT];
   uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -65,6 +70,19 @@ struct Bars {
 struct TMaps {
   CUtensorMap q, kc, vc, kp, vp;
 };
+
+// 8-wide tree reductions keep the dependency chains short.
+template <int N>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[N]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = __uint_as_float(s[i]);
+#pragma unroll
+  for (int j = 8; j < N; ++j) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(s[j]));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
 
 template <int D, int NK>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -82,33 +100,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int cta = blockIdx.x;
   const int r = find_req(g, cta, [](const ReqDesc &d) { return d.att0; });
   const ReqDesc &R = g.req[r];
-  const int mt_n = (R.lq + BM - 1) / BM;
+  const int mt_n = (R.lq + ROWS - 1) / ROWS;
   const int local = cta - R.att0;
   const int h = local % g.H;
   const int mt = mt_n - 1 - local / g.H;  // longest causal tiles first
   const int kvh = h / (g.H / g.Hkv);
-  const int m0 = mt * BM;
+  const int m0 = mt * ROWS;
+  const bool has_b = m0 + BM < R.lq;
 
   const int kbh = R.kh / g.Bk;
   int nh = n_sel[r];
   nh = nh < 0 ? 0 : (nh > kbh ? kbh : nh);
   const int sub = g.Bk / NK;
   const int n_hist = nh * sub;
-  const int n_cur = min((m0 + BM + NK - 1) / NK, R.lq / NK);
-  const int n_tiles = n_hist + n_cur;
+  // current-chunk tiles up to the last row of each query tile
+  const int n_a = n_hist + (min(m0 + BM, R.lq) - 1) / NK + 1;
+  const int n_b = has_b ? n_hist + (min(m0 + ROWS, R.lq) - 1) / NK + 1 : 0;
+  const int n_tiles = has_b ? n_b : n_a;
   const int32_t *pages = sel_page + (int64_t)r * g.bt_stride;
 
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&bar.k_full[s], 1);
-      mbar_init(&bar.v_full[s], 1);
-      mbar_init(&bar.kv_empty[s], 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.empty[s], 1);
     }
-    mbar_init(&bar.s_full[0], 1);
-    mbar_init(&bar.s_full[1], 1);
-    mbar_init(&bar.p_full, 4);  // one arrival per softmax warp
-    mbar_init(&bar.pv_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar.s_full[x], 1);
+      mbar_init(&bar.p_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&bar.pv_done[x], 1);
+    }
     mbar_init(&bar.drain, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -132,44 +153,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tm.kp);
         tma_prefetch_desc(&tm.vp);
       }
-      uint8_t *sQ = smem + LY::OFF_Q;
-      mbar_expect_tx(&bar.q_full, LY::Q_BYTES);
-      for (int hf = 0; hf < LY::HALVES; ++hf)
-        tma_load_3d(sQ + hf * (BM * 128), &tm.q, &bar.q_full, hf * 64, R.q0 + m0, h);
-      int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % NST;
-        if (t >= NST && !mbar_wait(&bar.kv_empty[s], ((t / NST) - 1) & 1, abort, g.err)) break;
-        uint8_t *sK = smem + LY::OFF_K + s * LY::KV_BYTES;
-        uint8_t *sV = smem + LY::OFF_V + s * LY::KV_BYTES;
-        mbar_expect_tx(&bar.k_full[s], LY::KV_BYTES);
-        mbar_expect_tx(&bar.v_full[s], LY::KV_BYTES);
+      mbar_expect_tx(&bar.q_full, (has_b ? 2 : 1) * LY::Q_BYTES);
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int hf = 0; hf < LY::HALVES; ++hf)
+          tma_load_3d(smem + LY::OFF_Q + x * LY::Q_BYTES + hf * (BM * 128), &tm.q, &bar.q_full,
+                      hf * 64, R.q0 + m0 + x * BM, h);
+      int issued = 0;  // loads: K(t) = 2t, V(t) = 2t+1
+      for (int i = 0; i < 2 * n_tiles; ++i) {
+        const int s = i % NSLOT;
+        if (i >= NSLOT && !mbar_wait(&bar.empty[s], ((i / NSLOT) - 1) & 1, abort, g.err)) break;
+        const int t = i >> 1;
+        const bool is_v = i & 1;
+        uint8_t *dst = smem + LY::OFF_KV + s * LY::KV_BYTES;
+        mbar_expect_tx(&bar.full[s], LY::KV_BYTES);
         if (t < n_hist) {
           int p = __ldg(pages + t / sub);
           if (p < 0 || p >= g.num_pages) p = 0;  // masked by the softmax warps
           const int tok = (t % sub) * NK;
           for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_4d(sK + hf * (NK * 128), &tm.kp, &bar.k_full[s], hf * 64, kvh, tok, p);
-          for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_4d(sV + hf * (NK * 128), &tm.vp, &bar.v_full[s], hf * 64, kvh, tok, p);
+            tma_load_4d(dst + hf * (NK * 128), is_v ? &tm.vp : &tm.kp, &bar.full[s], hf * 64,
+                        kvh, tok, p);
         } else {
           const int j0 = (t - n_hist) * NK;
           for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_3d(sK + hf * (NK * 128), &tm.kc, &bar.k_full[s], hf * 64, R.q0 + j0, kvh);
-          for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_3d(sV + hf * (NK * 128), &tm.vc, &bar.v_full[s], hf * 64, R.q0 + j0, kvh);
+            tma_load_3d(dst + hf * (NK * 128), is_v ? &tm.vc : &tm.kc, &bar.full[s], hf * 64,
+                        R.q0 + j0, kvh);
         }
-        issued = t + 1;
+        issued = i + 1;
       }
-      // drain: every load issued must have landed before the CTA's shared
-      // memory is released (only the last NST can still be in flight)
-      mbar_wait(&bar.q_full, 0, abort, g.err);
-      for (int t = max(0, issued - NST); t < issued; ++t) {
-        const int s = t % NST;
-        const uint32_t par = (t / NST) & 1;
-        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(&bar.k_full[s], par); ++i) {
-        }
-        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(&bar.v_full[s], par); ++i) {
+      // drain: every load issued must land before shared memory is released
+      // (only the last NSLOT can still be in flight)
+      for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.q_full, 0); ++k) {
+      }
+      for (int i = max(0, issued - NSLOT); i < issued; ++i) {
+        const uint32_t par = (i / NSLOT) & 1;
+        for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.full[i % NSLOT], par); ++k) {
         }
       }
     }
@@ -180,146 +198,157 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idPV = idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = smem_addr(smem + LY::OFF_Q);
       const uint32_t sP = smem_addr(smem + LY::OFF_P);
-      bool ok = mbar_wait(&bar.q_full, 0, abort, g.err);
-      auto issue_S = [&](int t) -> bool {
-        const int s = t % NST;
-        if (!mbar_wait(&bar.k_full[s], (t / NST) & 1, abort, g.err)) return false;
-        tc_fence_after();
-        const uint32_t sK = smem_addr(smem + LY::OFF_K + s * LY::KV_BYTES);
-        const uint32_t d = tmem + TM_S + (t & 1) * 128;
+      const uint32_t sKV = smem_addr(smem + LY::OFF_KV);
+      auto slot_wait = [&](int i) {
+        return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
+      };
+      auto issue_S = [&](int x, int t) {
+        const uint32_t q = sQ + x * LY::Q_BYTES;
+        const uint32_t k = sKV + ((2 * t) % NSLOT) * LY::KV_BYTES;
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sQ + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sK + (kk / 4) * (NK * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t a = sdesc_sw128(q + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(k + (kk / 4) * (NK * 128) + (kk % 4) * 32, 16, 1024);
           mma_f16_ss(d, a, b, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar.s_full[t & 1]);
-        return true;
+        mma_commit(&bar.s_full[x]);
       };
-      auto issue_PV = [&](int t) -> bool {
-        const int s = t % NST;
-        if (!mbar_wait(&bar.v_full[s], (t / NST) & 1, abort, g.err)) return false;
-        if (!mbar_wait(&bar.p_full, t & 1, abort, g.err)) return false;
-        tc_fence_after();
-        const uint32_t sV = smem_addr(smem + LY::OFF_V + s * LY::KV_BYTES);
+      auto issue_PV = [&](int x, int t) {
+        const uint32_t pp = sP + x * LY::P_BYTES;
+        const uint32_t v = sKV + ((2 * t + 1) % NSLOT) * LY::KV_BYTES;
+        const uint32_t d = tmem + 256 + x * 128;
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk) {
-          // A = P, K-major over keys; B = V, MN-major (d contiguous): the two
+          // A = P (K-major over keys); B = V, MN-major (d contiguous): the two
           // 64-wide d blocks are NK*128 bytes apart, 8-key groups 1024 apart
-          const uint64_t a = sdesc_sw128(sP + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sV + kk * 2048, NK * 128, 1024);
-          mma_f16_ss(tmem + TM_O, a, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t a = sdesc_sw128(pp + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(v + kk * 2048, NK * 128, 1024);
+          mma_f16_ss(d, a, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar.pv_done);
-        mma_commit(&bar.kv_empty[s]);
-        return true;
+        mma_commit(&bar.pv_done[x]);
       };
-      if (ok && n_tiles > 0) ok = issue_S(0);
+      bool ok = mbar_wait(&bar.q_full, 0, abort, g.err);
+      if (ok && n_tiles > 0) {
+        ok = slot_wait(0);
+        if (ok) {
+          tc_fence_after();
+          issue_S(0, 0);
+          if (has_b) issue_S(1, 0);
+          mma_commit(&bar.empty[0]);
+        }
+      }
       for (int t = 0; ok && t < n_tiles; ++t) {
-        if (t + 1 < n_tiles && !issue_S(t + 1)) break;
-        if (!issue_PV(t)) break;
+        const bool a_now = t < n_a, a_next = t + 1 < n_a;
+        const bool b_now = t < n_b, b_next = t + 1 < n_b;
+        if (!slot_wait(2 * t + 1)) break;  // V(t)
+        if (a_now) {
+          if (!mbar_wait(&bar.p_full[0], t & 1, abort, g.err)) break;
+          tc_fence_after();
+          issue_PV(0, t);
+        }
+        if (t + 1 < n_tiles && !slot_wait(2 * t + 2)) break;  // K(t+1)
+        tc_fence_after();
+        if (a_next) issue_S(0, t + 1);
+        if (b_now) {
+          if (!mbar_wait(&bar.p_full[1], t & 1, abort, g.err)) break;
+          tc_fence_after();
+          issue_PV(1, t);
+        }
+        mma_commit(&bar.empty[(2 * t + 1) % NSLOT]);  // V(t) consumed
+        if (b_next) issue_S(1, t + 1);
+        if (t + 1 < n_tiles) mma_commit(&bar.empty[(2 * t + 2) % NSLOT]);  // K(t+1) consumed
       }
       // every MMA issued has completed before TMEM is freed
       mma_commit(&bar.drain);
-      for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(&bar.drain, 0); ++i) {
+      for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.drain, 0); ++k) {
       }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int row = tid - 128;             // query row within the tile == TMEM lane
-    const int qrow = m0 + row;             // chunk-local query index
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
-    uint8_t *sP = smem + LY::OFF_P;
+    const int x = (warp - 4) >> 2;         // query tile: 0 = A, 1 = B
+    const int n_x = x ? n_b : n_a;
+    const int row = tid - 128 - x * BM;    // row within the tile == TMEM lane
+    const int qrow = m0 + x * BM + row;    // chunk-local query index
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t s_col = x * 128, o_col = 256 + x * 128;
+    uint8_t *sP = smem + LY::OFF_P + x * LY::P_BYTES;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      if (!mbar_wait(&bar.s_full[t & 1], (t >> 1) & 1, abort, g.err)) {
+    int p_next = (n_hist > 0) ? __ldg(pages) : 0;
+    for (int t = 0; t < n_x; ++t) {
+      const int p_cur = p_next;
+      if (t + 1 < n_hist) p_next = __ldg(pages + (t + 1) / sub);
+      if (!mbar_wait(&bar.s_full[x], t & 1, abort, g.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sraw[NK / 32][32];
+      uint32_t sr[NK];
 #pragma unroll
-      for (int c = 0; c < NK / 32; ++c) tmem_ld32(lane_addr + TM_S + (t & 1) * 128 + c * 32, sraw[c]);
+      for (int c = 0; c < NK / 32; ++c)
+        tmem_ld32(lane_addr + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_ld_wait();
 
-      // visibility of this tile's keys
-      bool all_vis = true, none_vis = false;
-      int lim = NK;  // keys [0, lim) visible
       if (t < n_hist) {
-        const int p = __ldg(pages + t / sub);
-        if (p < 0 || p >= g.num_pages) {
-          none_vis = true;
+        if (p_cur < 0 || p_cur >= g.num_pages) {  // invalid page: skip its keys
+#pragma unroll
+          for (int j = 0; j < NK; ++j) sr[j] = __float_as_uint(-INFINITY);
           if (row == 0 && (t % sub) == 0) record_error(g.err, XATTN_EPAGE);
         }
       } else {
-        const int j0 = (t - n_hist) * NK;
-        lim = qrow - j0 + 1;
-        if (lim < NK) all_vis = false;
-        if (lim <= 0) none_vis = true;
-      }
-      float mt = -INFINITY;
+        const int lim = qrow - (t - n_hist) * NK + 1;  // keys [0, lim) are visible
+        if (lim < NK) {
 #pragma unroll
-      for (int c = 0; c < NK / 32; ++c)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float x = __uint_as_float(sraw[c][j]) * scale_log2;
-          if (none_vis || (!all_vis && c * 32 + j >= lim)) x = -INFINITY;
-          sraw[c][j] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
+          for (int j = 0; j < NK; ++j)
+            if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
         }
+      }
+      // softmax_scale > 0, so the row max of the scaled logits is the scaled max
+      const float mt = row_max(sr) * scale_log2;
       const float mnew = fmaxf(m_run, mt);
       const bool need = mnew > m_run + 8.f;
       const float alpha = need ? ex2(m_run - mnew) : 1.f;
       const float m_use = need ? mnew : m_run;
-      const float base = m_use == -INFINITY ? 0.f : m_use;
-      float rs = 0.f;
-      uint32_t pk[NK / 2];
+      const float nb = m_use == -INFINITY ? 0.f : -m_use;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // P row -> 128B-swizzled K-major tile (64-key column blocks); P_x is free:
+      // S_x(t) completing implies PV_x(t-1) completed
 #pragma unroll
-      for (int c = 0; c < NK / 32; ++c)
+      for (int ch = 0; ch < NK / 8; ++ch) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = ex2(__uint_as_float(sraw[c][j]) - base);
-          const float p1 = ex2(__uint_as_float(sraw[c][j + 1]) - base);
-          rs += p0 + p1;
-          pk[(c * 32 + j) / 2] = pack_bf16x2(p0, p1);
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e]), scale_log2, nb));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e + 1]), scale_log2, nb));
+          sum[e] += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
         }
-      l_run = l_run * alpha + rs;
-      m_run = m_use;
-
-      // P buffer and O are free once the previous P V has completed
-      if (t > 0 && !mbar_wait(&bar.pv_done, (t - 1) & 1, abort, g.err)) {
-        ok = false;
-        break;
+        const int blk = ch / 8, cc = ch % 8;
+        *reinterpret_cast<uint4 *>(sP + blk * (BM * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      tc_fence_after();
+      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      m_run = m_use;
       if (t > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(lane_addr + TM_O + c * 32, ov);
+          tmem_ld32(lane_addr + o_col + c * 32, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tmem_st32(lane_addr + TM_O + c * 32, ov);
+          tmem_st32(lane_addr + o_col + c * 32, ov);
         }
         tmem_st_wait();
-      }
-      // P row -> 128B-swizzled K-major tile (64-key column blocks)
-#pragma unroll
-      for (int ch = 0; ch < NK / 8; ++ch) {
-        const int blk = ch / 8, cc = ch % 8;
-        uint8_t *dst = sP + blk * (BM * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(dst) =
-            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.p_full);
+      if (lane == 0) mbar_arrive(&bar.p_full[x]);
     }
     // epilogue: wait for the last P V, normalise, write O and LSE
-    if (ok && n_tiles > 0 && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort, g.err)) {
+    if (ok && n_x > 0 && mbar_wait(&bar.pv_done[x], (n_x - 1) & 1, abort, g.err)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const bool wr = qrow < R.lq;
@@ -327,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(lane_addr + TM_O + c * 32, ov);
+        tmem_ld32(lane_addr + o_col + c * 32, ov);
         tmem_ld_wait();
         if (wr) {
 #pragma unroll

@@ -11,6 +11,7 @@ namespace xattn {
 
 constexpr int kMaxReq = XATTN_MAX_REQUESTS;
 constexpr int kTileCols = 128;  // columns of one softmax-statistics tile (score GEMM N tile)
+constexpr int kAttnRows = 256;  // query rows per attention CTA (two 128-row MMA tiles)
 
 // Per-request geometry of one chunk call (host-computed, passed by value).
 struct ReqDesc {

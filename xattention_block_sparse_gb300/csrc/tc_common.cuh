@@ -12,10 +12,13 @@
 namespace xattn {
 namespace tc {
 
-// Spin budget of every mbarrier wait.  A wait that runs out records
-// XATTN_ETIMEOUT in the device error word and raises the CTA's abort flag, so
-// the kernel unwinds instead of hanging.
-constexpr uint32_t kSpinLimit = 1u << 24;
+// Budget of every mbarrier wait: kSpinLimit polls, each of which may suspend
+// the thread for up to kSuspendNs (it wakes as soon as the phase completes),
+// about 2.6 s in all.  A wait that runs out records XATTN_ETIMEOUT in the
+// device error word and raises the CTA's abort flag, so the kernel unwinds
+// instead of hanging.
+constexpr uint32_t kSpinLimit = 1u << 17;
+constexpr uint32_t kSuspendNs = 20000;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -42,10 +45,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -55,7 +58,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
                                           int32_t *err) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *abort) return false;
+    if (*abort) return false;
   }
   *abort = 1;
   record_error(err, XATTN_ETIMEOUT);
