@@ -68,7 +68,9 @@ def test_workspace_and_block_sum_sizes(lib):
     tstat = H * rq * (ncol // 128) * 8
     rstat = H * rq * 8
     al = lambda x: (x + 255) // 256 * 256
-    expect = al(al(al(scores) + tstat) + rstat) + al(512 * 4)
+    counts = al(al(al(scores) + tstat) + rstat)
+    kcat = al(counts + 512 * 4)          # gathered keys [Hkv, history + chunk, D] bf16
+    expect = al(kcat + 8 * 32768 * 128 * 2)
     assert X.xattn_workspace_size(p) == expect
     assert X.xattn_block_sums_count(p) == H * 32 * 256
     # varlen batch: slabs packed request after request
@@ -84,7 +86,8 @@ def test_workspace_and_block_sum_sizes(lib):
     dict(q_lens=[128], kh_lens=[0], H=6, Hkv=4),     # H % Hkv
     dict(q_lens=[128], kh_lens=[0], D=96),           # head_dim not built
     dict(q_lens=[128], kh_lens=[0], S=3),            # block % stride
-    dict(q_lens=[128], kh_lens=[0], S=64),           # block/stride < 4
+    dict(q_lens=[128], kh_lens=[0], S=64),           # block/stride < 8
+    dict(q_lens=[128], kh_lens=[0], S=32),           # block/stride = 4 < 8
     dict(q_lens=[128], kh_lens=[128 * 600], W=512),  # history beyond the table row
     dict(q_lens=[128] * 65, kh_lens=[0] * 65),       # too many requests
     dict(q_lens=[128], kh_lens=[0], q_head_stride=100),  # head stride too small

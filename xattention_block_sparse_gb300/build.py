@@ -24,6 +24,11 @@ LIB = os.path.join(BUILD, "libxattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+# extra nvcc flags (e.g. -D tuning knobs) and an alternative output directory
+EXTRA = os.environ.get("XATTN_NVCC_FLAGS", "").split()
+if os.environ.get("XATTN_BUILD_DIR"):
+    BUILD = os.path.abspath(os.environ["XATTN_BUILD_DIR"])
+    LIB = os.path.join(BUILD, "libxattn.so")
 
 
 def nvcc() -> str:
@@ -43,7 +48,7 @@ def _digest() -> str:
                              if f.endswith((".cuh", ".h"))] + [os.path.join(INCLUDE, "xattn.h")]:
         with open(path, "rb") as f:
             h.update(path.encode() + f.read())
-    h.update(" ".join(ARCH + CFLAGS).encode())
+    h.update(" ".join(ARCH + CFLAGS + EXTRA).encode())
     h.update(os.uname().machine.encode())
     return h.hexdigest()
 
@@ -61,7 +66,7 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *CFLAGS, *EXTRA, *extra, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stderr}")

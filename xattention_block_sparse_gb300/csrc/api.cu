@@ -19,7 +19,8 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   Geo geo;
-  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0;
+  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0, gat_ctas = 0;
+  int64_t kcat_tokens = 0;
   int max_kb = 0;
   size_t bs_count = 0;
   WsLayout ws{};
@@ -36,7 +37,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   if (D != 64 && D != 128) return XATTN_EUNSUPPORTED;
   if (S < 1 || S > 64 || Bk < 64 || Bk % 64 != 0 || Bk % S != 0) return XATTN_EUNSUPPORTED;
   const int br = Bk / S;
-  if (!pow2(br) || br < 4 || br > 128) return XATTN_EUNSUPPORTED;
+  if (!pow2(br) || br < 8 || br > 128) return XATTN_EUNSUPPORTED;
   if (!p->cu_seqlens_q || !p->cu_seqlens_kh) return XATTN_EINVAL;
   if (p->cu_seqlens_q[0] != 0) return XATTN_EINVAL;
 
@@ -55,7 +56,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   g.lse_hs = p->lse_head_stride;
   g.block_table = p->block_table;
 
-  int64_t gemm = 0, bsum = 0, sel = 0, att = 0;
+  int64_t gemm = 0, bsum = 0, sel = 0, att = 0, gat = 0, kcat = 0;
   size_t scores = 0, tstat = 0, rstat = 0, bs = 0;
   bool any_hist = false;
   for (int r = 0; r < B; ++r) {
@@ -78,6 +79,8 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     d.bsum0 = (int32_t)bsum;
     d.sel0 = (int32_t)sel;
     d.att0 = (int32_t)att;
+    d.gat0 = (int32_t)gat;
+    d.kcat0 = (int32_t)kcat;
     d.score_off = (int64_t)scores;
     d.tstat_off = (int64_t)tstat;
     d.rstat_off = (int64_t)rstat;
@@ -85,7 +88,16 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     const int64_t rq = lq / S, ncol = (kh + lq) / S;
     const int64_t ntile = (ncol + kTileCols - 1) / kTileCols;
     if (lq > 0) {
-      gemm += (int64_t)H * ((rq + 63) / 64) * ntile;
+      // score-GEMM tiles right of the causal diagonal are never visited
+      int64_t per_head = 0;
+      for (int64_t m0 = 0; m0 < rq; m0 += kGemmRows) {
+        const int64_t last = (m0 + kGemmRows < rq ? m0 + kGemmRows : rq) - 1;
+        const int64_t vis = (kh / S + last + 1 < ncol) ? kh / S + last + 1 : ncol;
+        per_head += (vis + kGemmCols - 1) / kGemmCols;
+      }
+      gemm += (int64_t)H * per_head;
+      gat += (int64_t)Hkv * (kbh + qb);
+      kcat += kh + lq;
       bsum += (int64_t)H * qb;
       sel += (int64_t)Hkv * qb;
       att += (int64_t)H * ((lq + kAttnRows - 1) / kAttnRows);
@@ -96,7 +108,9 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     bs += (size_t)H * qb * (kbh + qb);
     if (kbh + qb > pl.max_kb) pl.max_kb = (int)(kbh + qb);
   }
-  if (gemm > INT32_MAX || bsum > INT32_MAX || att > INT32_MAX) return XATTN_EUNSUPPORTED;
+  if (gemm > INT32_MAX || bsum > INT32_MAX || att > INT32_MAX || gat > INT32_MAX ||
+      kcat > INT32_MAX)
+    return XATTN_EUNSUPPORTED;
   if (any_hist && (!p->block_table || p->num_pages < 1)) return XATTN_EINVAL;
   if (p->bt_stride < 0) return XATTN_EINVAL;
   const int64_t tot_q = p->cu_seqlens_q[B];
@@ -109,14 +123,17 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   pl.bsum_ctas = (int)bsum;
   pl.sel_ctas = (int)sel;
   pl.att_ctas = (int)att;
+  pl.gat_ctas = (int)gat;
+  pl.kcat_tokens = kcat;
   pl.bs_count = bs;
   WsLayout &w = pl.ws;
   w.scores = 0;
   w.tstat = align_up(w.scores + scores * sizeof(float));
   w.rstat = align_up(w.tstat + tstat * sizeof(float2));
   w.counts = align_up(w.rstat + rstat * sizeof(float2));
-  w.total = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
-                                    sizeof(int32_t));
+  w.kcat = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
+                                   sizeof(int32_t));
+  w.total = align_up(w.kcat + (size_t)Hkv * (size_t)kcat * D * 2);
   return XATTN_OK;
 }
 
@@ -220,9 +237,12 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
   float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
   float2 *rstat = reinterpret_cast<float2 *>(ws + pl.ws.rstat);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, static_cast<const __nv_bfloat16 *>(q),
+  __nv_bfloat16 *kcat = reinterpret_cast<__nv_bfloat16 *>(ws + pl.ws.kcat);
+  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, pl.gat_ctas, pl.kcat_tokens,
+                           static_cast<const __nv_bfloat16 *>(q),
                            static_cast<const __nv_bfloat16 *>(k_cur),
-                           static_cast<const __nv_bfloat16 *>(k_pool), scale, scores, tstat, st));
+                           static_cast<const __nv_bfloat16 *>(k_pool), kcat, scale, scores, tstat,
+                           st));
   if (s != XATTN_OK) return s;
   return cu(launch_block_sum(pl.geo, pl.bsum_ctas, scores, tstat, rstat, block_sums, st));
 }

@@ -26,8 +26,6 @@
 // ready implies PV_x(t-1) has finished: P_x and O_x are free at that point.
 // Every mbarrier wait is bounded; a timeout records XATTN_ETIMEOUT and the CTA
 // unwinds (draining its TMA loads and MMAs, then freeing TMEM).
-#include <cudaTypedefs.h>
-
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -385,30 +383,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-                 const cuuint64_t *strides, const cuuint32_t *box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int NK>
 cudaError_t launch_tc(const Geo &g, int nctas, const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                       const __nv_bfloat16 *vcur, const __nv_bfloat16 *kpool,

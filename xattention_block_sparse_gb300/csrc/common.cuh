@@ -12,16 +12,20 @@ namespace xattn {
 constexpr int kMaxReq = XATTN_MAX_REQUESTS;
 constexpr int kTileCols = 128;  // columns of one softmax-statistics tile (score GEMM N tile)
 constexpr int kAttnRows = 256;  // query rows per attention CTA (two 128-row MMA tiles)
+constexpr int kGemmRows = 256;  // reshaped rows per score-GEMM CTA (two 128-row MMA tiles)
+constexpr int kGemmCols = 256;  // reshaped columns per score-GEMM CTA
 
 // Per-request geometry of one chunk call (host-computed, passed by value).
 struct ReqDesc {
   int32_t q0;      // first query token of the request in the packed token axis
   int32_t lq;      // query tokens (current chunk)
   int32_t kh;      // history tokens
-  int32_t gemm0;   // first CTA of the request in the score-GEMM grid
-  int32_t bsum0;   // ... in the block-sum grid
+  int32_t gemm0;   // first score-GEMM tile of the request
+  int32_t bsum0;   // first CTA of the request in the block-sum grid
   int32_t sel0;    // ... in the selection grid
   int32_t att0;    // ... in the attention grid
+  int32_t gat0;    // ... in the key-gather grid
+  int32_t kcat0;   // first token of the request in the gathered key buffer
   int32_t pad_;
   int64_t score_off;  // float offset of the request's [H, lq/S, (kh+lq)/S] scores
   int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
@@ -65,11 +69,12 @@ __device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
 // Launch entry points implemented in the kernel translation units.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t scores, tstat, rstat, counts, total;
+  size_t scores, tstat, rstat, counts, kcat, total;
 };
 
-cudaError_t launch_score_gemm(const Geo &g, int nctas, const __nv_bfloat16 *q,
-                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
+cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
+                              const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
+                              const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
                               float *scores, float2 *tstat, cudaStream_t st);
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *scores, const float2 *tstat,
                              float2 *rstat, float *block_sums, cudaStream_t st);

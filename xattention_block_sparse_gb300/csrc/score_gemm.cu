@@ -1,0 +1,350 @@
+// Estimation score GEMM of XAttention BSA ("XAttention BSA Policy 设计文档",
+// select_blocks Step 1 flat_group_gemm_fuse_reshape; "XAttention Offload
+// Stream Synchronization Fix", 技术细节 Stage 1 softmax_compute_partial_stats).
+//
+// For one (request, head) the reshaped scores are a plain GEMM with K = S*D:
+//   s[a, b] = scale * sum_{i<S} q[S a + S-1-i] . k[S b + i]
+// where reshaped column b runs over [history ; current chunk].
+//
+//   gather_k_kernel   copies each request's keys -- the history pages through
+//                     the block table, then the current chunk -- into one
+//                     contiguous [Hkv, tokens, D] buffer (HBM-bound, coalesced),
+//                     so the GEMM reads K with one TMA box per k-step instead
+//                     of one box per page.
+//   score_gemm_kernel persistent CTAs over 256 x 256 output tiles (two 128-row
+//                     MMA tiles; both accumulators fill the 512 TMEM columns).
+//                     The stride reversal costs nothing: 4-D TMA views (d, phase,
+//                     group, head) of q and of the gathered keys pick phase S-1-i
+//                     of q for the k-step that uses phase i of k.
+//     warp 0       TMA producer over an NST-stage ring (runs ahead into the
+//                  next tile while the epilogue drains TMEM)
+//     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
+//     warps 4..11  epilogue, one thread per row: fp32 scores to the workspace
+//                  and per-(row, 128-column tile) (max, sum exp) over the
+//                  visible cells.  Tiles right of the causal diagonal are never
+//                  scheduled; the block-sum merge reads only tiles up to each
+//                  row's diagonal.
+#include "tc_common.cuh"
+
+namespace xattn {
+namespace {
+using namespace tc;
+
+constexpr int TM = 128;           // rows per MMA tile
+constexpr int ROWS = kGemmRows;   // 256 rows per output tile
+constexpr int COLS = kGemmCols;   // 256 columns per output tile
+constexpr int KSTEP = 64;         // bf16 elements of K per stage (one 128-byte swizzle row)
+constexpr int NST = 3;
+constexpr int THREADS = 384;
+constexpr int A_BYTES = ROWS * KSTEP * 2;  // 32 KB
+constexpr int B_BYTES = COLS * KSTEP * 2;  // 32 KB
+constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int OFF_BAR = NST * STAGE;
+constexpr int SMEM_ALLOC = OFF_BAR + 1024 + 1024;
+
+struct Bars {
+  uint64_t full[NST];
+  uint64_t empty[NST];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Maps {
+  CUtensorMap q, k;
+};
+
+struct Tile {
+  int r, h, m0, n0;
+};
+
+// Tile t of the score GEMM: requests in order, then head, then row tile, then
+// column tile; only tiles holding visible cells exist.
+__device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
+  const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0; });
+  const ReqDesc &R = g.req[r];
+  const int S = g.S;
+  const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+  int per_head = 0;
+  for (int m0 = 0; m0 < rq; m0 += ROWS) {
+    const int vis = min(ch + min(m0 + ROWS, rq), ncol);
+    per_head += (vis + COLS - 1) / COLS;
+  }
+  int local = t - R.gemm0;
+  Tile tl;
+  tl.r = r;
+  tl.h = local / per_head;
+  local -= tl.h * per_head;
+  for (int m0 = 0; m0 < rq; m0 += ROWS) {
+    const int vis = min(ch + min(m0 + ROWS, rq), ncol);
+    const int n = (vis + COLS - 1) / COLS;
+    if (local < n) {
+      tl.m0 = m0;
+      tl.n0 = local * COLS;
+      return tl;
+    }
+    local -= n;
+  }
+  tl.m0 = tl.n0 = 0;  // unreachable for valid t
+  return tl;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int ntiles,
+                      float scale, float *__restrict__ scores, float2 *__restrict__ tstat) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars &bar = *reinterpret_cast<Bars *>(smem + OFF_BAR);
+  volatile int *abort = &bar.abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = g.S, D = g.D;
+  const int ksteps = S * D / KSTEP;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.empty[s], 1);
+    }
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.acc_empty, 8);  // one arrival per epilogue warp
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mp.q);
+      tma_prefetch_desc(&mp.k);
+      int it = 0;  // k-steps issued so far (ring position)
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        const Tile tl = decode_tile(g, t);
+        const ReqDesc &R = g.req[tl.r];
+        const int kvh = tl.h / (g.H / g.Hkv);
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const int s = it % NST;
+          if (it >= NST && !mbar_wait(&bar.empty[s], ((it / NST) - 1) & 1, abort, g.err)) {
+            ok = false;
+            break;
+          }
+          const int kk = ks * KSTEP;
+          const int i = kk / D, dc = kk % D;
+          uint8_t *sA = smem + s * STAGE;
+          mbar_expect_tx(&bar.full[s], STAGE);
+          // q rows S*a + S-1-i and key groups S*b + i of this tile
+          tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
+          tma_load_4d(sA + A_BYTES, &mp.k, &bar.full[s], dc, i, R.kcat0 / S + tl.n0, kvh);
+        }
+      }
+      for (int k = max(0, it - NST); k < it; ++k) {
+        const uint32_t par = (k / NST) & 1;
+        for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.full[k % NST], par); ++n) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(TM, COLS, 0, 0);
+      int it = 0, n = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++n) {
+        const Tile tl = decode_tile(g, t);
+        const int rq = g.req[tl.r].lq / S;
+        const bool two_m = tl.m0 + TM < rq;
+        // the epilogue has drained the previous tile's accumulators
+        if (n > 0 && !mbar_wait(&bar.acc_empty, (n - 1) & 1, abort, g.err)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const int s = it % NST;
+          if (!mbar_wait(&bar.full[s], (it / NST) & 1, abort, g.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(smem + s * STAGE);
+          const uint32_t b0 = a0 + A_BYTES;
+          for (int x = 0; x < (two_m ? 2 : 1); ++x) {
+#pragma unroll
+            for (int kq = 0; kq < KSTEP / 16; ++kq) {
+              const uint64_t a = sdesc_sw128(a0 + x * (TM * 128) + kq * 32, 16, 1024);
+              const uint64_t b = sdesc_sw128(b0 + kq * 32, 16, 1024);
+              mma_f16_ss(tmem + x * COLS, a, b, idesc, (ks > 0 || kq > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&bar.empty[s]);
+        }
+        mma_commit(&bar.acc_full);
+      }
+      // every MMA issued has completed before TMEM is freed: the epilogue waited
+      // for each tile's acc_full, and no MMA follows the last commit
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int x = (warp - 4) >> 2;
+    const int row = tid - 128 - x * TM;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + x * COLS;
+    int n = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++n) {
+      const Tile tl = decode_tile(g, t);
+      const ReqDesc &R = g.req[tl.r];
+      const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+      const int ntile = (ncol + kTileCols - 1) / kTileCols;
+      const bool two_m = tl.m0 + TM < rq;
+      const int a = tl.m0 + x * TM + row;
+      if (!mbar_wait(&bar.acc_full, n & 1, abort, g.err)) break;
+      tc_fence_after();
+      if (x == 0 || two_m) {
+        const bool row_ok = a < rq;
+        float *srow = scores + R.score_off + ((int64_t)tl.h * rq + (row_ok ? a : 0)) * ncol;
+#pragma unroll 1
+        for (int j = 0; j < COLS / kTileCols; ++j) {
+          const int c0 = tl.n0 + j * kTileCols;  // first column of this statistics tile
+          uint32_t v[kTileCols];
+#pragma unroll
+          for (int c = 0; c < kTileCols / 32; ++c)
+            tmem_ld32(lane_addr + j * kTileCols + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+          tmem_ld_wait();
+          if (j == COLS / kTileCols - 1) {
+            // all of this tile's accumulators are in registers: release TMEM
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.acc_empty);
+          }
+          if (!row_ok || c0 >= ncol || c0 > ch + a) continue;
+          // visible columns of the row in this tile: [c0, c0 + nv)
+          const int nv = min(min(kTileCols, ncol - c0), ch + a + 1 - c0);
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < kTileCols; c += 4) {
+            const float4 f = make_float4(__uint_as_float(v[c]) * scale,
+                                         __uint_as_float(v[c + 1]) * scale,
+                                         __uint_as_float(v[c + 2]) * scale,
+                                         __uint_as_float(v[c + 3]) * scale);
+            if (c0 + c < ncol) *reinterpret_cast<float4 *>(srow + c0 + c) = f;
+            v[c] = __float_as_uint(c < nv ? f.x : -INFINITY);
+            v[c + 1] = __float_as_uint(c + 1 < nv ? f.y : -INFINITY);
+            v[c + 2] = __float_as_uint(c + 2 < nv ? f.z : -INFINITY);
+            v[c + 3] = __float_as_uint(c + 3 < nv ? f.w : -INFINITY);
+            mx[0] = fmaxf(mx[0], __uint_as_float(v[c]));
+            mx[1] = fmaxf(mx[1], __uint_as_float(v[c + 1]));
+            mx[2] = fmaxf(mx[2], __uint_as_float(v[c + 2]));
+            mx[3] = fmaxf(mx[3], __uint_as_float(v[c + 3]));
+          }
+          const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float ml2 = m * 1.4426950408889634f;
+          float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < kTileCols; ++c)
+            sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), 1.4426950408889634f, -ml2));
+          tstat[R.tstat_off + ((int64_t)tl.h * rq + a) * ntile + c0 / kTileCols] =
+              make_float2(m, (sm[0] + sm[1]) + (sm[2] + sm[3]));
+        }
+      } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.acc_empty);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Key gather: one CTA per (request, kv head, block of Bk tokens).
+// ---------------------------------------------------------------------------
+constexpr int GTHR = 256;
+
+__global__ void __launch_bounds__(GTHR) gather_k_kernel(const __grid_constant__ Geo g,
+                                                        const __nv_bfloat16 *__restrict__ kcur,
+                                                        const __nv_bfloat16 *__restrict__ kpool,
+                                                        __nv_bfloat16 *__restrict__ kcat,
+                                                        int64_t kcat_tokens) {
+  const int cta = blockIdx.x;
+  const int r = find_req(g, cta, [](const ReqDesc &d) { return d.gat0; });
+  const ReqDesc &R = g.req[r];
+  const int kbh = R.kh / g.Bk, kb = kbh + R.lq / g.Bk;
+  const int local = cta - R.gat0;
+  const int j = local % kb, kvh = local / kb;
+  const int D = g.D;
+  const __nv_bfloat16 *src;
+  int64_t src_stride;  // elements between consecutive tokens
+  bool valid = true;
+  if (j < kbh) {
+    const int p = page_of(g, r, j);
+    valid = p >= 0;
+    src = kpool + ((int64_t)(valid ? p : 0) * g.Bk * g.Hkv + kvh) * D;
+    src_stride = (int64_t)g.Hkv * D;
+  } else {
+    src = kcur + (int64_t)kvh * g.kv_hs + (int64_t)(R.q0 + (j - kbh) * g.Bk) * D;
+    src_stride = D;
+  }
+  __nv_bfloat16 *dst = kcat + ((int64_t)kvh * kcat_tokens + R.kcat0 + (int64_t)j * g.Bk) * D;
+  const int per_row = D / 8;  // 16-byte chunks per token row
+  for (int id = threadIdx.x; id < g.Bk * per_row; id += GTHR) {
+    const int t = id / per_row, c = id % per_row;
+    uint4 v = make_uint4(0, 0, 0, 0);  // an invalid page reads as zero keys
+    if (valid) v = __ldg(reinterpret_cast<const uint4 *>(src + t * src_stride) + c);
+    *(reinterpret_cast<uint4 *>(dst + (int64_t)t * D) + c) = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
+                              const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
+                              const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
+                              float *scores, float2 *tstat, cudaStream_t st) {
+  if (gather_ctas > 0) {
+    gather_k_kernel<<<gather_ctas, GTHR, 0, st>>>(g, kcur, kpool, kcat, kcat_tokens);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (ntiles == 0) return cudaSuccess;
+  const int S = g.S, D = g.D;
+  const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
+  Maps mp;
+  {  // q as (d, phase i, group, head)
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(tot_q / S),
+                                (cuuint64_t)g.H};
+    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2, (cuuint64_t)g.q_hs * 2};
+    const cuuint32_t box[4] = {KSTEP, 1, ROWS, 1};
+    if (!encode_bf16(&mp.q, q, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {  // gathered keys as (d, phase i, group, kv head)
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(kcat_tokens / S),
+                                (cuuint64_t)g.Hkv};
+    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2,
+                               (cuuint64_t)kcat_tokens * D * 2};
+    const cuuint32_t box[4] = {KSTEP, 1, COLS, 1};
+    if (!encode_bf16(&mp.k, kcat, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(score_gemm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const int grid = ntiles < sms ? ntiles : sms;
+  score_gemm_kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(g, mp, ntiles, scale, scores, tstat);
+  return cudaGetLastError();
+}
+
+}  // namespace xattn

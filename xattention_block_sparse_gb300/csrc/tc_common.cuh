@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -13,12 +14,15 @@ namespace xattn {
 namespace tc {
 
 // Budget of every mbarrier wait: kSpinLimit polls, each of which may suspend
-// the thread for up to kSuspendNs (it wakes as soon as the phase completes),
-// about 2.6 s in all.  A wait that runs out records XATTN_ETIMEOUT in the
+// the thread for up to the hardware's time limit (or kSuspendNs when set),
+// a few seconds in all.  A wait that runs out records XATTN_ETIMEOUT in the
 // device error word and raises the CTA's abort flag, so the kernel unwinds
 // instead of hanging.
-constexpr uint32_t kSpinLimit = 1u << 17;
-constexpr uint32_t kSuspendNs = 20000;
+#ifndef XATTN_SUSPEND_NS
+#define XATTN_SUSPEND_NS 0
+#endif
+constexpr uint32_t kSuspendNs = XATTN_SUSPEND_NS;  // 0: no hint, the system limit applies
+constexpr uint32_t kSpinLimit = kSuspendNs ? (1u << 17) : (1u << 24);
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -43,13 +47,23 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
-      : "memory");
+  if (kSuspendNs) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Returns false (and sets
@@ -85,6 +99,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_addr(bar))
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -203,6 +226,35 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// Host: tiled tensor maps (bf16, 128-byte swizzle), encoded through the driver
+// entry point so the library does not link libcuda.
+// ---------------------------------------------------------------------------
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// dims/box innermost first; strides in bytes for dims 1..rank-1.
+inline bool encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                        const cuuint64_t *strides, const cuuint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc

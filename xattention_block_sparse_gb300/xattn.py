@@ -14,7 +14,8 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libxattn.so")
+LIB_PATH = os.path.join(os.path.abspath(os.environ["XATTN_BUILD_DIR"]) if os.environ.get(
+    "XATTN_BUILD_DIR") else os.path.join(_PKG, "_build"), "libxattn.so")
 
 XATTN_MAX_REQUESTS = 64
 XATTN_MAX_BLOCKS_PER_ROW = 8192
