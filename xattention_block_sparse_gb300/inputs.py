@@ -253,3 +253,66 @@ def chunk_calls(L: int, chunk: int, block_table: np.ndarray) -> list:
     and history tokens [0, c*chunk) read through the block_table."""
     return [ChunkCall([chunk], [c * chunk], c * chunk, block_table)
             for c in range(L // chunk)]
+
+
+# --------------------------------------------------------------------------
+# Long-context layer stack (the 128K config): drawn on the device
+# --------------------------------------------------------------------------
+
+@dataclass
+class RingLayer:
+    """One synthetic layer of the 128K config.
+
+    q        device bf16 [H, L, D]
+    k_host   pinned host bf16 [P, Bk, Hkv, D]   the layer's KV cache in host
+    v_host   pinned host bf16 [P, Bk, Hkv, D]   memory, pages in logical order
+    """
+    q: object
+    k_host: object
+    v_host: object
+
+
+def make_ring_layer(layer: int, device, L: int | None = None) -> RingLayer:
+    """Seeded inputs of one layer of the 128K config (Qwen3-4B-like: 32 Q / 8 KV
+    heads, head_dim 128).  The tensors (1 GB of q per layer at 128K) are drawn
+    with torch's counter-based generator on the device, seed 1004 + 7919*layer,
+    in the order q, k, v, window bias; values fp32 -> RoPE (NeoX, theta 1e6)
+    -> local-window bias u ~ N(0, 0.5^2) per (1024-token window, KV head) added
+    to q and k -> sink keys 0..3 scaled x3 -> bf16 (round to nearest even).
+    The KV cache goes to pinned host memory in page layout (the history a
+    layer-ring slot is filled from); q stays on the device."""
+    import torch
+
+    cfg = CONFIGS["q4b_128k"]
+    L = L or cfg.L
+    H, Hkv, D, Bk = cfg.H, cfg.Hkv, cfg.D, cfg.block
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1000 + cfg.index + 7919 * layer)
+
+    def rope(x):
+        half = D // 2
+        inv = 1e6 ** (-torch.arange(half, device=device, dtype=torch.float64) * 2.0 / D)
+        ang = torch.arange(L, device=device, dtype=torch.float64)[:, None] * inv[None, :]
+        cos, sin = torch.cos(ang).float(), torch.sin(ang).float()
+        x1, x2 = x[..., :half], x[..., half:]
+        return torch.cat([x1 * cos - x2 * sin, x2 * cos + x1 * sin], dim=-1)
+
+    q = rope(torch.randn((H, L, D), generator=gen, device=device))
+    k = rope(torch.randn((Hkv, L, D), generator=gen, device=device))
+    v = torch.randn((Hkv, L, D), generator=gen, device=device)
+    nwin = (L + 1023) // 1024
+    u = 0.5 * torch.randn((Hkv, nwin, D), generator=gen, device=device)
+    win = torch.arange(L, device=device) // 1024
+    k += u[:, win, :]
+    q += u.repeat_interleave(H // Hkv, dim=0)[:, win, :]
+    k[:, 0:4, :] *= 3.0
+    qb = q.to(torch.bfloat16)
+    del q
+
+    def to_host_pages(x):
+        pages = x.to(torch.bfloat16).reshape(Hkv, L // Bk, Bk, D).permute(1, 2, 0, 3)
+        host = torch.empty(pages.shape, dtype=torch.bfloat16, pin_memory=True)
+        host.copy_(pages)
+        return host
+
+    return RingLayer(qb, to_host_pages(k), to_host_pages(v))

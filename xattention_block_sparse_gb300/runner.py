@@ -87,3 +87,94 @@ class SequencePrefill:
             self.run_chunk(c, Q, K, V, kpool, vpool, tau, O, LSE, stream)
             if on_chunk is not None:
                 on_chunk(c, self.bufs)
+
+
+class LayerRing:
+    """N-slot ring of per-layer KV page pools fed from pinned host memory.
+
+    "Task Plan: Layerwise Offload Refactoring", Phase 1.1 / Phase 4: slot
+    l mod N holds layer l; the first N layers are preloaded, and the slot of
+    layer l is reloaded with layer l+N once layer l's compute has finished.
+    Copies run on one side stream; the compute stream waits on the slot's
+    `ready` event before use and records its `done` event after, the event
+    discipline of "XAttention Offload Stream Synchronization Fix" (修复方案,
+    Event 同步机制) that keeps estimation from reading a slot still in flight."""
+
+    def __init__(self, num_slots, pages, block, Hkv, D, device):
+        self.N = num_slots
+        shape = (num_slots, pages, block, Hkv, D)
+        self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.ready = [None] * num_slots
+        self.done = [torch.cuda.Event() for _ in range(num_slots)]
+        self.owner = [None] * num_slots
+        self.log = []  # (layer, start event, ready event, bytes) per load
+        cur = torch.cuda.current_stream(device)
+        for e in self.done:  # every slot starts free
+            e.record(cur)
+
+    def slot(self, layer):
+        return layer % self.N
+
+    def load(self, layer, host_k, host_v, n_pages):
+        """Queue the copy of the first n_pages pages of `layer` into its slot."""
+        s = self.slot(layer)
+        start = torch.cuda.Event(enable_timing=True)
+        ready = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.done[s])
+            start.record(self.copy_stream)
+            if n_pages > 0:
+                self.k[s, :n_pages].copy_(host_k[:n_pages], non_blocking=True)
+                self.v[s, :n_pages].copy_(host_v[:n_pages], non_blocking=True)
+            ready.record(self.copy_stream)
+        self.ready[s] = ready
+        self.owner[s] = layer
+        self.log.append((layer, start, ready, 2 * n_pages * host_k[0].numel() * 2))
+
+    @property
+    def bytes_copied(self):
+        return sum(x[3] for x in self.log)
+
+    def acquire(self, layer, stream):
+        s = self.slot(layer)
+        assert self.owner[s] == layer, "slot holds another layer"
+        stream.wait_event(self.ready[s])
+        return self.k[s], self.v[s]
+
+    def release(self, layer, stream):
+        self.done[self.slot(layer)].record(stream)
+
+
+def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bufs, problem,
+                       outs, stream, on_layer=None, compute_events=None):
+    """Chunk c of every layer through the ring: history pages [0, c*chunk/block)
+    of each layer are loaded into its slot, the current chunk's K/V are the
+    next chunk/block pages of the same host cache (copied in the same load)."""
+    n_hist = c * chunk // block
+    n_load = n_hist + chunk // block
+    L = len(layers)
+    for l in range(min(ring.N, L)):
+        ring.load(l, layers[l].k_host, layers[l].v_host, n_load)
+    for l in range(L):
+        kp, vp = ring.acquire(l, stream)
+        if compute_events is not None:  # starts after the slot wait
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        with torch.cuda.stream(stream):
+            # current chunk in [Hkv, tokens, D] for the estimation / attention calls
+            kc = kp[n_hist:n_load].reshape(chunk, Hkv, D).permute(1, 0, 2).contiguous()
+            vc = vp[n_hist:n_load].reshape(chunk, Hkv, D).permute(1, 0, 2).contiguous()
+            q = layers[l].q[:, c * chunk:]
+            o, lse = outs[l]
+            prefill_chunk(problem, q, kc, vc, kp, vp, tau, bufs, o[:, c * chunk:],
+                          lse[:, c * chunk:], stream=stream)
+            if compute_events is not None:
+                e1.record(stream)
+                compute_events.append((e0, e1))
+            if on_layer is not None:
+                on_layer(l, bufs)
+        ring.release(l, stream)
+        if l + ring.N < L:
+            ring.load(l + ring.N, layers[l + ring.N].k_host, layers[l + ring.N].v_host, n_load)
