@@ -8,22 +8,25 @@
 // tcgen05 design.  One CTA = two 128-row query tiles (A and B) of one
 // (request, head), sharing every K/V tile:
 //   warp 0        TMA producer: both Q tiles once, then K(t), V(t) for each KV
-//                 tile t (one page of up to 128 keys) through a 3-slot ring of
+//                 tile t (one page of up to 128 keys) through a 5-slot ring of
 //                 128B-swizzled tiles.  History tiles are gathered page by page
 //                 through the selection's page list, then the current chunk up
 //                 to the diagonal.
 //   warp 1        MMA issuer, in the order PV_A(t), S_A(t+1), PV_B(t), S_B(t+1):
 //                 S_x = Q_x K^T into TMEM (128 lanes x NK fp32 columns), then
-//                 O_x += P_x V into a TMEM accumulator.  While one tile's
-//                 softmax runs, the tensor pipe works for the other tile.
+//                 O_x += P_x V into a TMEM accumulator with P_x read from TMEM.
+//                 While one tile's softmax runs, the tensor pipe works for the
+//                 other tile.
 //   warps 4..7    softmax of tile A, warps 8..11 softmax of tile B: thread i
 //                 owns query row i (TMEM lane i).  It loads its S row, masks
 //                 the causal diagonal tile, keeps a running max (rescaling O in
 //                 TMEM only when the max grows by more than 2^8), writes P as
-//                 bf16 into swizzled shared memory for the P V MMA, and at the
-//                 end normalises O and writes O and LSE.
-// Because each thread's tcgen05 ops complete in issue order, S_x(t) being
-// ready implies PV_x(t-1) has finished: P_x and O_x are free at that point.
+//                 bf16 back into the TMEM columns its S row came from (the P V
+//                 MMA reads its A operand there, so P costs no shared-memory
+//                 bandwidth), and at the end normalises O and writes O, LSE.
+// Each thread's tcgen05 ops complete in issue order: S_x(t) being ready
+// implies PV_x(t-1) has finished, so O_x may be rescaled and S_x's columns
+// reused for P_x(t) without further waits.
 // Every mbarrier wait is bounded; a timeout records XATTN_ETIMEOUT and the CTA
 // unwinds (draining its TMA loads and MMAs, then freeing TMEM).
 #include "tc_common.cuh"
@@ -35,7 +38,7 @@ using namespace tc;
 constexpr int BM = 128;       // rows per query tile (MMA M)
 constexpr int ROWS = 2 * BM;  // query rows per CTA
 static_assert(ROWS == kAttnRows, "host grid sizing assumes kAttnRows rows per CTA");
-constexpr int NSLOT = 3;      // K/V ring slots
+constexpr int NSLOT = 5;      // K/V ring slots
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;  // S_A | S_B | O_A | O_B, 128 columns each
 
@@ -44,10 +47,8 @@ struct Layout {
   static constexpr int HALVES = D / 64;  // 64-element (128 B) column blocks
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = NK * D * 2;
-  static constexpr int P_BYTES = BM * NK * 2;
   static constexpr int OFF_Q = 0;                       // Q_A, Q_B
-  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
-  static constexpr int OFF_KV = OFF_P + 2 * P_BYTES;    // ring
+  static constexpr int OFF_KV = OFF_Q + 2 * Q_BYTES;    // ring
   static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
   static constexpr int BYTES = OFF_BAR + 256;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
@@ -69,19 +70,6 @@ struct TMaps {
   CUtensorMap q, kc, vc, kp, vp;
 };
 
-// 8-wide tree reductions keep the dependency chains short.
-template <int N>
-__device__ __forceinline__ float row_max(const uint32_t (&s)[N]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = __uint_as_float(s[i]);
-#pragma unroll
-  for (int j = 8; j < N; ++j) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(s[j]));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
-}
-
 template <int D, int NK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ Geo g, const __grid_constant__ TMaps tm,
@@ -100,9 +88,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const ReqDesc &R = g.req[r];
   const int mt_n = (R.lq + ROWS - 1) / ROWS;
   const int local = cta - R.att0;
+  const int G = g.H / g.Hkv;
+  // longest causal tiles first, all heads of a row tile together
   const int h = local % g.H;
-  const int mt = mt_n - 1 - local / g.H;  // longest causal tiles first
-  const int kvh = h / (g.H / g.Hkv);
+  const int mt = mt_n - 1 - local / g.H;
+  const int kvh = h / G;
   const int m0 = mt * ROWS;
   const bool has_b = m0 + BM < R.lq;
 
@@ -195,7 +185,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idS = idesc_bf16(BM, NK, 0, 0);
       constexpr uint32_t idPV = idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = smem_addr(smem + LY::OFF_Q);
-      const uint32_t sP = smem_addr(smem + LY::OFF_P);
       const uint32_t sKV = smem_addr(smem + LY::OFF_KV);
       auto slot_wait = [&](int i) {
         return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
@@ -213,16 +202,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_commit(&bar.s_full[x]);
       };
       auto issue_PV = [&](int x, int t) {
-        const uint32_t pp = sP + x * LY::P_BYTES;
         const uint32_t v = sKV + ((2 * t + 1) % NSLOT) * LY::KV_BYTES;
         const uint32_t d = tmem + 256 + x * 128;
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk) {
-          // A = P (K-major over keys); B = V, MN-major (d contiguous): the two
-          // 64-wide d blocks are NK*128 bytes apart, 8-key groups 1024 apart
-          const uint64_t a = sdesc_sw128(pp + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
+          // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
+          // (d contiguous): the two 64-wide d blocks are NK*128 bytes apart,
+          // 8-key groups 1024 apart
           const uint64_t b = sdesc_sw128(v + kk * 2048, NK * 128, 1024);
-          mma_f16_ss(d, a, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(d, tmem + x * 128 + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bar.pv_done[x]);
       };
@@ -239,23 +227,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int t = 0; ok && t < n_tiles; ++t) {
         const bool a_now = t < n_a, a_next = t + 1 < n_a;
         const bool b_now = t < n_b, b_next = t + 1 < n_b;
+        const bool next = t + 1 < n_tiles;
         if (!slot_wait(2 * t + 1)) break;  // V(t)
         if (a_now) {
           if (!mbar_wait(&bar.p_full[0], t & 1, abort, g.err)) break;
           tc_fence_after();
           issue_PV(0, t);
         }
-        if (t + 1 < n_tiles && !slot_wait(2 * t + 2)) break;  // K(t+1)
-        tc_fence_after();
-        if (a_next) issue_S(0, t + 1);
+        if (next && !slot_wait(2 * t + 2)) break;  // K(t+1)
+        if (a_next) {  // the softmax has consumed S_A(t): it arrived p_full
+          tc_fence_after();
+          issue_S(0, t + 1);
+        }
         if (b_now) {
           if (!mbar_wait(&bar.p_full[1], t & 1, abort, g.err)) break;
           tc_fence_after();
           issue_PV(1, t);
         }
         mma_commit(&bar.empty[(2 * t + 1) % NSLOT]);  // V(t) consumed
-        if (b_next) issue_S(1, t + 1);
-        if (t + 1 < n_tiles) mma_commit(&bar.empty[(2 * t + 2) % NSLOT]);  // K(t+1) consumed
+        if (b_next) {
+          tc_fence_after();
+          issue_S(1, t + 1);
+        }
+        if (next) mma_commit(&bar.empty[(2 * t + 2) % NSLOT]);  // K(t+1) consumed
       }
       // every MMA issued has completed before TMEM is freed
       mma_commit(&bar.drain);
@@ -270,7 +264,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int qrow = m0 + x * BM + row;    // chunk-local query index
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t s_col = x * 128, o_col = 256 + x * 128;
-    uint8_t *sP = smem + LY::OFF_P + x * LY::P_BYTES;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int p_next = (n_hist > 0) ? __ldg(pages) : 0;
@@ -303,30 +296,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       // softmax_scale > 0, so the row max of the scaled logits is the scaled max
-      const float mt = row_max(sr) * scale_log2;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < NK; j += 8)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          m4[e] = fmax3(m4[e], __uint_as_float(sr[j + 2 * e]), __uint_as_float(sr[j + 2 * e + 1]));
+      const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * scale_log2;
       const float mnew = fmaxf(m_run, mt);
       const bool need = mnew > m_run + 8.f;
       const float alpha = need ? ex2(m_run - mnew) : 1.f;
       const float m_use = need ? mnew : m_run;
       const float nb = m_use == -INFINITY ? 0.f : -m_use;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      // P row -> 128B-swizzled K-major tile (64-key column blocks); P_x is free:
-      // S_x(t) completing implies PV_x(t-1) completed
+      const uint64_t sc2 = f2(scale_log2, scale_log2), nb2 = f2(nb, nb);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+      // P row -> the S row's TMEM columns (two bf16 per column), the A operand
+      // of P V, 64 keys at a time; PV_x(t-1) finished before S_x(t) did
 #pragma unroll
-      for (int ch = 0; ch < NK / 8; ++ch) {
-        uint32_t pk[4];
+      for (int hb = 0; hb < NK / 64; ++hb) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e]), scale_log2, nb));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e + 1]), scale_log2, nb));
-          sum[e] += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+        for (int j = 0; j < 64; j += 2) {
+          float x0, x1;
+          unf2(ffma2(f2(__uint_as_float(sr[hb * 64 + j]), __uint_as_float(sr[hb * 64 + j + 1])),
+                     sc2, nb2),
+               x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[(j >> 1) & 3] = fadd2(sum2[(j >> 1) & 3], f2(p0, p1));
+          pk[j >> 1] = pack_bf16x2(p0, p1);
         }
-        const int blk = ch / 8, cc = ch % 8;
-        *reinterpret_cast<uint4 *>(sP + blk * (BM * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        tmem_st32(lane_addr + s_col + hb * 32, pk);
       }
-      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      float s0, s1, s2, s3;
+      unf2(fadd2(sum2[0], sum2[1]), s0, s1);
+      unf2(fadd2(sum2[2], sum2[3]), s2, s3);
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
       m_run = m_use;
       if (t > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -338,9 +342,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
           tmem_st32(lane_addr + o_col + c * 32, ov);
         }
-        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.p_full[x]);
