@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // The whole warp runs the loop; lane 0 issues.  Page ids are read 32 tiles
+    // ahead (one per lane) so no global load sits on the issue path.
     if (lane == 0) {
       tma_prefetch_desc(&tm.q);
       tma_prefetch_desc(&tm.kc);
@@ -146,17 +148,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int hf = 0; hf < LY::HALVES; ++hf)
           tma_load_3d(smem + LY::OFF_Q + x * LY::Q_BYTES + hf * (BM * 128), &tm.q, &bar.q_full,
                       hf * 64, R.q0 + m0 + x * BM, h);
-      int issued = 0;  // loads: K(t) = 2t, V(t) = 2t+1
-      for (int i = 0; i < 2 * n_tiles; ++i) {
-        const int s = i % NSLOT;
-        if (i >= NSLOT && !mbar_wait(&bar.empty[s], ((i / NSLOT) - 1) & 1, abort, g.err)) break;
-        const int t = i >> 1;
+    }
+    int issued = 0;  // loads: K(t) = 2t, V(t) = 2t+1
+    int pg = 0;      // page id of tile (t & ~31) + lane
+    for (int i = 0; i < 2 * n_tiles; ++i) {
+      const int t = i >> 1;
+      if ((i & 63) == 0) {  // next 32 tiles' page ids, one per lane
+        const int tt = t + lane;
+        pg = tt < n_hist ? __ldg(pages + tt / sub) : 0;
+      }
+      const int p_t = __shfl_sync(0xffffffffu, pg, t & 31);
+      const int s = i % NSLOT;
+      int ok = 1;  // lane 0 waits, the warp follows its verdict
+      if (lane == 0 && i >= NSLOT) ok = mbar_wait(&bar.empty[s], ((i / NSLOT) - 1) & 1, abort, g.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
         const bool is_v = i & 1;
         uint8_t *dst = smem + LY::OFF_KV + s * LY::KV_BYTES;
         mbar_expect_tx(&bar.full[s], LY::KV_BYTES);
         if (t < n_hist) {
-          int p = __ldg(pages + t / sub);
-          if (p < 0 || p >= g.num_pages) p = 0;  // masked by the softmax warps
+          const int p = (p_t < 0 || p_t >= g.num_pages) ? 0 : p_t;  // masked by the softmax
           const int tok = (t % sub) * NK;
           for (int hf = 0; hf < LY::HALVES; ++hf)
             tma_load_4d(dst + hf * (NK * 128), is_v ? &tm.vp : &tm.kp, &bar.full[s], hf * 64,
@@ -167,10 +178,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_3d(dst + hf * (NK * 128), is_v ? &tm.vc : &tm.kc, &bar.full[s], hf * 64,
                         R.q0 + j0, kvh);
         }
-        issued = i + 1;
       }
-      // drain: every load issued must land before shared memory is released
-      // (only the last NSLOT can still be in flight)
+      issued = i + 1;
+    }
+    // drain: every load issued must land before shared memory is released
+    // (only the last NSLOT can still be in flight)
+    if (lane == 0) {
       for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.q_full, 0); ++k) {
       }
       for (int i = max(0, issued - NSLOT); i < issued; ++i) {
@@ -189,29 +202,33 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto slot_wait = [&](int i) {
         return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
       };
+      // Descriptors are built once; a k-step only adds its byte offset / 16 to
+      // the start-address field (all operands lie below 256 KB of shared memory).
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sKV, NK * 128, 1024);
       auto issue_S = [&](int x, int t) {
-        const uint32_t q = sQ + x * LY::Q_BYTES;
-        const uint32_t k = sKV + ((2 * t) % NSLOT) * LY::KV_BYTES;
+        const uint64_t a0 = dQ0 + (uint64_t)((x * LY::Q_BYTES) >> 4);
+        const uint64_t b0 = dK0 + (uint64_t)((((2 * t) % NSLOT) * LY::KV_BYTES) >> 4);
         const uint32_t d = tmem + x * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(q + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(k + (kk / 4) * (NK * 128) + (kk % 4) * 32, 16, 1024);
-          mma_f16_ss(d, a, b, idS, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16_ss(d, a0 + (uint64_t)(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4),
+                     b0 + (uint64_t)(((kk / 4) * (NK * 128) + (kk % 4) * 32) >> 4), idS,
+                     kk > 0 ? 1u : 0u);
         mma_commit(&bar.s_full[x]);
       };
       auto issue_PV = [&](int x, int t) {
-        const uint32_t v = sKV + ((2 * t + 1) % NSLOT) * LY::KV_BYTES;
+        const uint64_t b0 = dV0 + (uint64_t)((((2 * t + 1) % NSLOT) * LY::KV_BYTES) >> 4);
         const uint32_t d = tmem + 256 + x * 128;
+        const uint32_t a = tmem + x * 128;
+        // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
+        // (d contiguous): the two 64-wide d blocks are NK*128 bytes apart,
+        // 8-key groups 1024 apart
 #pragma unroll
-        for (int kk = 0; kk < NK / 16; ++kk) {
-          // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
-          // (d contiguous): the two 64-wide d blocks are NK*128 bytes apart,
-          // 8-key groups 1024 apart
-          const uint64_t b = sdesc_sw128(v + kk * 2048, NK * 128, 1024);
-          mma_f16_ts(d, tmem + x * 128 + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < NK / 16; ++kk)
+          mma_f16_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idPV,
+                     (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar.pv_done[x]);
       };
       bool ok = mbar_wait(&bar.q_full, 0, abort, g.err);
