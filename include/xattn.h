@@ -87,7 +87,7 @@ typedef enum xattn_status {
  * Constraints (XATTN_EINVAL / XATTN_EUNSUPPORTED otherwise):
  *   1 <= num_requests <= XATTN_MAX_REQUESTS; num_heads % num_kv_heads == 0;
  *   head_dim in {64, 128}; block_size % 64 == 0; block_size % stride == 0;
- *   block_size / stride a power of two in [8, 128]; 1 <= stride <= 64;
+ *   block_size / stride a power of two in [8, 32]; 1 <= stride <= 64;
  *   every query and history length a multiple of block_size;
  *   history blocks + query blocks of a request <= XATTN_MAX_BLOCKS_PER_ROW;
  *   history blocks of a request <= bt_stride. */

@@ -21,6 +21,7 @@ struct Plan {
   Geo geo;
   int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0, gat_ctas = 0;
   int64_t kcat_tokens = 0;
+  int64_t stat_rows = 0;
   int max_kb = 0;
   size_t bs_count = 0;
   WsLayout ws{};
@@ -37,7 +38,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   if (D != 64 && D != 128) return XATTN_EUNSUPPORTED;
   if (S < 1 || S > 64 || Bk < 64 || Bk % 64 != 0 || Bk % S != 0) return XATTN_EUNSUPPORTED;
   const int br = Bk / S;
-  if (!pow2(br) || br < 8 || br > 128) return XATTN_EUNSUPPORTED;
+  if (!pow2(br) || br < 8 || br > 32) return XATTN_EUNSUPPORTED;
   if (!p->cu_seqlens_q || !p->cu_seqlens_kh) return XATTN_EINVAL;
   if (p->cu_seqlens_q[0] != 0) return XATTN_EINVAL;
 
@@ -98,7 +99,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
       gemm += (int64_t)H * per_head;
       gat += (int64_t)Hkv * (kbh + qb);
       kcat += kh + lq;
-      bsum += (int64_t)H * qb;
+      bsum += (int64_t)H * qb * ((ncol + kBsumCols - 1) / kBsumCols);
       sel += (int64_t)Hkv * qb;
       att += (int64_t)H * ((lq + kAttnRows - 1) / kAttnRows);
     }
@@ -125,6 +126,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   pl.att_ctas = (int)att;
   pl.gat_ctas = (int)gat;
   pl.kcat_tokens = kcat;
+  pl.stat_rows = (int64_t)rstat;
   pl.bs_count = bs;
   WsLayout &w = pl.ws;
   w.scores = 0;
@@ -244,7 +246,8 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
                            static_cast<const __nv_bfloat16 *>(k_pool), kcat, scale, scores, tstat,
                            st));
   if (s != XATTN_OK) return s;
-  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, scores, tstat, rstat, block_sums, st));
+  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, pl.stat_rows, scores, tstat, rstat,
+                             block_sums, st));
 }
 
 xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,

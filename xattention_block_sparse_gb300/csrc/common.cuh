@@ -14,6 +14,7 @@ constexpr int kTileCols = 128;  // columns of one softmax-statistics tile (score
 constexpr int kAttnRows = 256;  // query rows per attention CTA (two 128-row MMA tiles)
 constexpr int kGemmRows = 256;  // reshaped rows per score-GEMM CTA (two 128-row MMA tiles)
 constexpr int kGemmCols = 256;  // reshaped columns per score-GEMM CTA
+constexpr int kBsumCols = 256;  // columns per block-sum CTA (one per thread)
 
 // Per-request geometry of one chunk call (host-computed, passed by value).
 struct ReqDesc {
@@ -76,8 +77,9 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t
                               const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                               const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
                               float *scores, float2 *tstat, cudaStream_t st);
-cudaError_t launch_block_sum(const Geo &g, int nctas, const float *scores, const float2 *tstat,
-                             float2 *rstat, float *block_sums, cudaStream_t st);
+cudaError_t launch_block_sum(const Geo &g, int nctas, int64_t nrows, const float *scores,
+                             const float2 *tstat, float2 *rstat, float *block_sums,
+                             cudaStream_t st);
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
                           double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st);
 cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx,

@@ -19,11 +19,12 @@
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
 //                  next tile while the epilogue drains TMEM)
 //     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
-//     warps 4..11  epilogue, one thread per row: fp32 scores to the workspace
-//                  and per-(row, 128-column tile) (max, sum exp) over the
-//                  visible cells.  Tiles right of the causal diagonal are never
-//                  scheduled; the block-sum merge reads only tiles up to each
-//                  row's diagonal.
+//     warps 4..11  epilogue, one thread per row: fp32 scores to the workspace,
+//                  laid out [H][Qb][ncol][Br] (a query block's rows contiguous
+//                  per column, so stores coalesce), and per-(row, 128-column
+//                  tile) (max, sum exp) over the visible cells.  Tiles right
+//                  of the causal diagonal are never scheduled; the block-sum
+//                  merge reads only tiles up to each row's diagonal.
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -157,6 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(TM, COLS, 0, 0);
+      // descriptors are built once and advanced by byte offset / 16
+      const uint64_t d0 = sdesc_sw128(smem_addr(smem), 16, 1024);
       int it = 0, n = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++n) {
@@ -173,15 +176,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(smem + s * STAGE);
-          const uint32_t b0 = a0 + A_BYTES;
+          const uint64_t a0 = d0 + (uint64_t)((s * STAGE) >> 4);
+          const uint64_t b0 = a0 + (uint64_t)(A_BYTES >> 4);
           for (int x = 0; x < (two_m ? 2 : 1); ++x) {
 #pragma unroll
-            for (int kq = 0; kq < KSTEP / 16; ++kq) {
-              const uint64_t a = sdesc_sw128(a0 + x * (TM * 128) + kq * 32, 16, 1024);
-              const uint64_t b = sdesc_sw128(b0 + kq * 32, 16, 1024);
-              mma_f16_ss(tmem + x * COLS, a, b, idesc, (ks > 0 || kq > 0) ? 1u : 0u);
-            }
+            for (int kq = 0; kq < KSTEP / 16; ++kq)
+              mma_f16_ss(tmem + x * COLS, a0 + (uint64_t)((x * (TM * 128) + kq * 32) >> 4),
+                         b0 + (uint64_t)((kq * 32) >> 4), idesc, (ks > 0 || kq > 0) ? 1u : 0u);
           }
           mma_commit(&bar.empty[s]);
         }
@@ -207,7 +208,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       if (x == 0 || two_m) {
         const bool row_ok = a < rq;
-        float *srow = scores + R.score_off + ((int64_t)tl.h * rq + (row_ok ? a : 0)) * ncol;
+        // scores are stored [H][Qb][ncol][Br]: the Br rows of a query block are
+        // contiguous per column, so a warp's store of one column is 32 rows in
+        // 32/Br full segments
+        const int br = g.Bk / S;
+        float *sbase = scores + R.score_off +
+                       ((int64_t)(tl.h * (rq / br) + (row_ok ? a : 0) / br) * ncol) * br +
+                       (row_ok ? a : 0) % br;
 #pragma unroll 1
         for (int j = 0; j < COLS / kTileCols; ++j) {
           const int c0 = tl.n0 + j * kTileCols;  // first column of this statistics tile
@@ -226,22 +233,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!row_ok || c0 >= ncol || c0 > ch + a) continue;
           // visible columns of the row in this tile: [c0, c0 + nv)
           const int nv = min(min(kTileCols, ncol - c0), ch + a + 1 - c0);
+          const int nst = min(kTileCols, ncol - c0);  // columns that exist
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < kTileCols; c += 4) {
-            const float4 f = make_float4(__uint_as_float(v[c]) * scale,
-                                         __uint_as_float(v[c + 1]) * scale,
-                                         __uint_as_float(v[c + 2]) * scale,
-                                         __uint_as_float(v[c + 3]) * scale);
-            if (c0 + c < ncol) *reinterpret_cast<float4 *>(srow + c0 + c) = f;
-            v[c] = __float_as_uint(c < nv ? f.x : -INFINITY);
-            v[c + 1] = __float_as_uint(c + 1 < nv ? f.y : -INFINITY);
-            v[c + 2] = __float_as_uint(c + 2 < nv ? f.z : -INFINITY);
-            v[c + 3] = __float_as_uint(c + 3 < nv ? f.w : -INFINITY);
-            mx[0] = fmaxf(mx[0], __uint_as_float(v[c]));
-            mx[1] = fmaxf(mx[1], __uint_as_float(v[c + 1]));
-            mx[2] = fmaxf(mx[2], __uint_as_float(v[c + 2]));
-            mx[3] = fmaxf(mx[3], __uint_as_float(v[c + 3]));
+          for (int c = 0; c < kTileCols; ++c) {
+            const float f = __uint_as_float(v[c]) * scale;
+            if (c < nst) sbase[(int64_t)(c0 + c) * br] = f;
+            v[c] = __float_as_uint(c < nv ? f : -INFINITY);
+            mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
           }
           const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float ml2 = m * 1.4426950408889634f;
@@ -297,11 +296,23 @@ __global__ void __launch_bounds__(GTHR) gather_k_kernel(const __grid_constant__ 
   }
   __nv_bfloat16 *dst = kcat + ((int64_t)kvh * kcat_tokens + R.kcat0 + (int64_t)j * g.Bk) * D;
   const int per_row = D / 8;  // 16-byte chunks per token row
-  for (int id = threadIdx.x; id < g.Bk * per_row; id += GTHR) {
-    const int t = id / per_row, c = id % per_row;
-    uint4 v = make_uint4(0, 0, 0, 0);  // an invalid page reads as zero keys
-    if (valid) v = __ldg(reinterpret_cast<const uint4 *>(src + t * src_stride) + c);
-    *(reinterpret_cast<uint4 *>(dst + (int64_t)t * D) + c) = v;
+  const int n = g.Bk * per_row;
+  // all loads of a thread in flight before the first store
+  for (int id0 = threadIdx.x; id0 < n; id0 += 8 * GTHR) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int id = id0 + u * GTHR;
+      const int t = id / per_row, c = id % per_row;
+      v[u] = make_uint4(0, 0, 0, 0);  // an invalid page reads as zero keys
+      if (valid && id < n) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + t * src_stride) + c);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int id = id0 + u * GTHR;
+      const int t = id / per_row, c = id % per_row;
+      if (id < n) *(reinterpret_cast<uint4 *>(dst + (int64_t)t * D) + c) = v[u];
+    }
   }
 }
 
