@@ -129,15 +129,21 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------
 
-def traffic_for(kernel_file, kernel_name):
+def source_sha(files):
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "xattention_block_sparse_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_files, kernel_name):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel's file; else None."""
+    the current source of the kernel's files; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "xattention_block_sparse_gb300", "csrc", kernel_file)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    sha = source_sha(kernel_files)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -296,7 +302,8 @@ def run_ours(args, ws, rank, local):
                      "frac": att_tflops / peaks["bf16_tflops"],
                      "frac_sustained": att_tflops / peaks["bf16_tflops_sustained"],
                      "peak_source": peak_src,
-                     "traffic": traffic_for("attention.cu", "attn_kernel"),
+                     "traffic": traffic_for(("attention.cu", "tc_common.cuh", "common.cuh"),
+                                            "attn_kernel"),
                      "launch_ms": att_launch_ms},
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "t_meas_ms": ms,
                           "frac": t_roof * 1e3 / ms},
@@ -307,7 +314,8 @@ def run_ours(args, ws, rank, local):
         "n_sel_per_chunk": n_sel,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 5 * nchunk * K_,
+        # per chunk: gather, score GEMM, stat merge, block sum, select, vote, attention
+        "gpu_launches": 7 * nchunk * K_,
         "wall_s_timed": wall,
     }
     if rank == 0:
