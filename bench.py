@@ -202,8 +202,8 @@ def run_ours(args, ws, rank, local):
             if ev is not None:
                 ev[c][2].record(stream)
             X.bsa_chunk_attention(p, Q[:, t0:], K[:, t0:], V[:, t0:], KP, VP, b.sel_page,
-                                  b.n_sel, 1.0 / math.sqrt(cfg.D), O_[:, t0:], LSE[:, t0:],
-                                  stream)
+                                  b.n_sel, 1.0 / math.sqrt(cfg.D), b.workspace, O_[:, t0:],
+                                  LSE[:, t0:], stream)
             if ev is not None:
                 ev[c][3].record(stream)
 

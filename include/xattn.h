@@ -194,13 +194,20 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
  * the history and causal parts are merged online by log-sum-exp, so the result
  * equals flash_attn_with_lse(history) merged with flash_attn_with_lse(causal).
  *   softmax_scale  > 0 (usually 1/sqrt(D)); XATTN_EINVAL otherwise
+ *   workspace      DEVICE scratch of at least xattn_workspace_size(p) bytes,
+ *                  16-byte aligned (XATTN_EWORKSPACE / XATTN_EALIGN otherwise);
+ *                  the same buffer xattn_estimate / xattn_select take.  The
+ *                  work (KV tiles of every 256-row query tile) is split evenly
+ *                  over one persistent CTA per SM; a query tile cut between
+ *                  CTAs leaves normalised partial results (fp32 O, LSE) here,
+ *                  merged by log-sum-exp into o / lse by a second kernel.
  *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
  *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE */
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
                                  const void *v_cur, const void *k_pool, const void *v_pool,
                                  const int32_t *sel_page, const int32_t *n_sel,
-                                 float softmax_scale, void *o, float *lse,
-                                 xattn_stream_t stream);
+                                 float softmax_scale, void *workspace, size_t workspace_bytes,
+                                 void *o, float *lse, xattn_stream_t stream);
 
 /* merge_attention_outputs (BSA policy page, compute_chunked_prefill): for each
  * of `rows` rows, lse = log(exp(lse1) + exp(lse2)) and

@@ -70,7 +70,10 @@ def test_workspace_and_block_sum_sizes(lib):
     al = lambda x: (x + 255) // 256 * 256
     counts = al(al(al(scores) + tstat) + rstat)
     kcat = al(counts + 512 * 4)          # gathered keys [Hkv, history + chunk, D] bf16
-    expect = al(kcat + 8 * 32768 * 128 * 2)
+    part_o = al(kcat + 8 * 32768 * 128 * 2)  # attention partials: 160 CTAs x 2 slots x 256 rows
+    part_lse = al(part_o + 160 * 2 * 256 * 128 * 4)
+    att_cnt = al(part_lse + 160 * 2 * 256 * 4)
+    expect = al(att_cnt + 16 * 16 * 2 * 4)  # two part counters per 256-row attention unit
     assert X.xattn_workspace_size(p) == expect
     assert X.xattn_block_sums_count(p) == H * 32 * 256
     # varlen batch: slabs packed request after request
@@ -100,7 +103,7 @@ def test_invalid_problems_rejected(lib, kw):
     st = lib.xattn_estimate(p.ref(), fake, fake, fake, 0.1, fake, 1 << 40, fake, None)
     assert st in (-1, -5), st
     st = lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,
-                                 fake, None)
+                                 1 << 40, fake, fake, None)
     assert st in (-1, -5), st
 
 
@@ -118,8 +121,12 @@ def test_entry_point_argument_errors(lib):
         assert lib.xattn_select(p.ref(), fake, tau, fake, 1 << 40, None, fake, fake, fake,
                                 None) == -1
     assert lib.xattn_select(p.ref(), fake, 0.9, fake, 16, None, fake, fake, fake, None) == -6
-    assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, odd,
-                                   fake, None) == -2
+    assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,
+                                   1 << 40, odd, fake, None) == -2
+    assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,
+                                   16, fake, fake, None) == -6
+    assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, None,
+                                   1 << 40, fake, fake, None) == -1
     assert lib.lse_merge(fake, fake, fake, fake, 10, 6, fake, 0, fake, None) == -1
     assert lib.lse_merge(fake, fake, fake, fake, -1, 128, fake, 0, fake, None) == -1
     assert lib.lse_merge(odd, fake, fake, fake, 10, 128, fake, 0, fake, None) == -2

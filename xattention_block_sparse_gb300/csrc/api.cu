@@ -135,7 +135,12 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   w.counts = align_up(w.rstat + rstat * sizeof(float2));
   w.kcat = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
                                    sizeof(int32_t));
-  w.total = align_up(w.kcat + (size_t)Hkv * (size_t)kcat * D * 2);
+  // attention partial results: two slots of kAttnRows rows per persistent CTA
+  const size_t part_rows = (size_t)kAttnMaxCtas * 2 * kAttnRows;
+  w.part_o = align_up(w.kcat + (size_t)Hkv * (size_t)kcat * D * 2);
+  w.part_lse = align_up(w.part_o + part_rows * D * sizeof(float));
+  w.att_cnt = align_up(w.part_lse + part_rows * sizeof(float));
+  w.total = align_up(w.att_cnt + (size_t)att * 2 * sizeof(int32_t));  // two per attention unit
   return XATTN_OK;
 }
 
@@ -299,25 +304,32 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
                                  const void *v_cur, const void *k_pool, const void *v_pool,
                                  const int32_t *sel_page, const int32_t *n_sel,
-                                 float softmax_scale, void *o, float *lse, xattn_stream_t stream) {
+                                 float softmax_scale, void *workspace, size_t workspace_bytes,
+                                 void *o, float *lse, xattn_stream_t stream) {
   Plan pl;
   xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse) return XATTN_EINVAL;
+  if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse || !workspace)
+    return XATTN_EINVAL;
   if ((!k_pool || !v_pool) && pl.geo.num_pages > 0) return XATTN_EINVAL;
   if (p->bt_stride < 1) return XATTN_EINVAL;
   if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return XATTN_EINVAL;
   if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(o) ||
-      (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)))
+      (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)) || !aligned16(workspace))
     return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
   if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
   return cu(launch_attention(pl.geo, pl.att_ctas, static_cast<const __nv_bfloat16 *>(q),
                              static_cast<const __nv_bfloat16 *>(k_cur),
                              static_cast<const __nv_bfloat16 *>(v_cur),
                              static_cast<const __nv_bfloat16 *>(k_pool),
                              static_cast<const __nv_bfloat16 *>(v_pool), sel_page, n_sel,
-                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse, st));
+                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse,
+                             reinterpret_cast<float *>(ws + pl.ws.part_o),
+                             reinterpret_cast<float *>(ws + pl.ws.part_lse),
+                             reinterpret_cast<int32_t *>(ws + pl.ws.att_cnt), st));
 }
 
 xattn_status lse_merge(const float *o1, const float *lse1, const float *o2, const float *lse2,

@@ -5,30 +5,39 @@
 // flash_attn_with_lse(history) merged with flash_attn_with_lse(current, causal)
 // by merge_attention_outputs.
 //
-// tcgen05 design.  One CTA = two 128-row query tiles (A and B) of one
-// (request, head), sharing every K/V tile:
-//   warp 0        TMA producer: both Q tiles once, then K(t), V(t) for each KV
-//                 tile t (one page of up to 128 keys) through a 5-slot ring of
-//                 128B-swizzled tiles.  History tiles are gathered page by page
-//                 through the selection's page list, then the current chunk up
-//                 to the diagonal.
+// Work decomposition (stream-K).  A work unit is 256 query rows -- tiles A
+// and B of 128 rows -- of one (request, head); its work items are the KV tiles
+// it attends (selected history pages, then the current chunk up to the unit's
+// last row).  The items of all units, in (request, head, row tile, KV tile)
+// order, are split into one equal contiguous range per persistent CTA (one
+// CTA per SM), so every SM gets the same number of KV tiles.  A CTA walks its
+// range as segments (a unit, or the piece of one that falls in its range).
+// A unit cut between CTAs leaves normalised partial results (fp32 O, LSE);
+// the last CTA to finish a part (a per-unit counter) merges them by
+// log-sum-exp into the final O and LSE.
+//
+// tcgen05 pipeline of one CTA (two query tiles A and B share every K/V tile):
+//   warp 0        TMA producer: Q_A, Q_B of each segment (as soon as the
+//                 previous segment's last S MMA on that tile has completed),
+//                 then K(t), V(t) for each KV tile t (one page of up to 128
+//                 keys) through a 5-slot ring of 128B-swizzled tiles.
 //   warp 1        MMA issuer, in the order PV_A(t), S_A(t+1), PV_B(t), S_B(t+1):
 //                 S_x = Q_x K^T into TMEM (128 lanes x NK fp32 columns), then
 //                 O_x += P_x V into a TMEM accumulator with P_x read from TMEM.
-//                 While one tile's softmax runs, the tensor pipe works for the
-//                 other tile.
 //   warps 4..7    softmax of tile A, warps 8..11 softmax of tile B: thread i
 //                 owns query row i (TMEM lane i).  It loads its S row, masks
 //                 the causal diagonal tile, keeps a running max (rescaling O in
 //                 TMEM only when the max grows by more than 2^8), writes P as
-//                 bf16 back into the TMEM columns its S row came from (the P V
-//                 MMA reads its A operand there, so P costs no shared-memory
-//                 bandwidth), and at the end normalises O and writes O, LSE.
+//                 bf16 back into the TMEM columns its S row came from, and at
+//                 the end of a segment normalises O and writes it (256-bit
+//                 stores, one full 32-byte sector per thread and instruction).
 // Each thread's tcgen05 ops complete in issue order: S_x(t) being ready
 // implies PV_x(t-1) has finished, so O_x may be rescaled and S_x's columns
 // reused for P_x(t) without further waits.
 // Every mbarrier wait is bounded; a timeout records XATTN_ETIMEOUT and the CTA
-// unwinds (draining its TMA loads and MMAs, then freeing TMEM).
+// unwinds (draining its TMA loads and MMAs, then freeing TMEM).  No CTA waits
+// for another: the merge of a split unit is done by whichever CTA finishes its
+// part last.
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -36,8 +45,8 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128;       // rows per query tile (MMA M)
-constexpr int ROWS = 2 * BM;  // query rows per CTA
-static_assert(ROWS == kAttnRows, "host grid sizing assumes kAttnRows rows per CTA");
+constexpr int ROWS = 2 * BM;  // query rows per work unit
+static_assert(ROWS == kAttnRows, "partial-output slots assume kAttnRows rows per unit");
 constexpr int NSLOT = 5;      // K/V ring slots
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;  // S_A | S_B | O_A | O_B, 128 columns each
@@ -50,31 +59,171 @@ struct Layout {
   static constexpr int OFF_Q = 0;                       // Q_A, Q_B
   static constexpr int OFF_KV = OFF_Q + 2 * Q_BYTES;    // ring
   static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
-  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int BYTES = OFF_BAR + 1536;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
 };
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
+  uint64_t grp[2];                 // barrier of one softmax warpgroup (4 warp arrivals)
   uint32_t tmem_base;
   int abort;
+  int last[2];                     // this CTA merges the unit (per query tile)
+  int64_t total;                   // work items (KV tiles over all units)
+  int64_t req_pos0[kMaxReq + 1];   // first work item of each request
+  int32_t req_hist[kMaxReq];       // history KV tiles of the request (selected pages)
+  int32_t req_per_head[kMaxReq];   // work items per head of the request
+  int32_t req_unit0[kMaxReq];      // first unit id of the request
 };
 
 struct TMaps {
   CUtensorMap q, kc, vc, kp, vp;
 };
 
+struct Unit {
+  int n_a, n_b, n_tiles;  // tiles of query tile A, of B, and of the unit
+  bool has_b;
+};
+
+template <int NK>
+__device__ __forceinline__ Unit unit_geom(const ReqDesc &R, int n_hist, int mt) {
+  Unit u;
+  const int m0 = mt * ROWS;
+  u.has_b = m0 + BM < R.lq;
+  u.n_a = n_hist + (min(m0 + BM, R.lq) - 1) / NK + 1;
+  u.n_b = u.has_b ? n_hist + (min(m0 + ROWS, R.lq) - 1) / NK + 1 : 0;
+  u.n_tiles = u.has_b ? u.n_b : u.n_a;
+  return u;
+}
+
+// Work-item tables of the launch, from the selection counts on the device
+// (every CTA computes the same tables: no host round trip).
+template <int NK>
+__device__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
+  int64_t pos = 0;
+  int32_t unit = 0;
+  const int sub = g.Bk / NK;
+  for (int r = 0; r < g.B; ++r) {
+    const ReqDesc &R = g.req[r];
+    const int kbh = R.kh / g.Bk;
+    int nh = n_sel[r];
+    nh = nh < 0 ? 0 : (nh > kbh ? kbh : nh);
+    const int n_hist = nh * sub;
+    int per_head = 0, nmt = 0;
+    for (int mt = 0; mt * ROWS < R.lq; ++mt, ++nmt) per_head += unit_geom<NK>(R, n_hist, mt).n_tiles;
+    bar.req_pos0[r] = pos;
+    bar.req_hist[r] = n_hist;
+    bar.req_per_head[r] = per_head;
+    bar.req_unit0[r] = unit;
+    pos += (int64_t)per_head * g.H;
+    unit += nmt * g.H;
+  }
+  bar.req_pos0[g.B] = pos;
+  bar.total = pos;
+}
+
+// First work item of CTA c when `total` items are split over G CTAs.
+__device__ __forceinline__ int64_t cta_begin(int64_t total, int c, int G) {
+  return total * c / G;
+}
+
+// The CTA whose range holds item `pos`.
+__device__ __forceinline__ int cta_of(int64_t total, int G, int64_t pos) {
+  int c = (int)(pos * G / total);
+  while (c + 1 < G && cta_begin(total, c + 1, G) <= pos) ++c;
+  while (c > 0 && cta_begin(total, c, G) > pos) --c;
+  return c;
+}
+
+// One contiguous piece of a unit handled by this CTA: tiles [t0, t1).
+struct Seg {
+  int r, h, mt, t0, t1, kvh, m0, n_hist, uid;
+  int64_t ustart;  // work item of the unit's tile 0
+  Unit u;
+  bool partial;
+  int slot;  // partial-output slot (0: first segment of the CTA, 1: last)
+};
+
+template <int NK>
+__device__ __forceinline__ Seg make_seg(const Geo &g, const Bars &bar, int64_t pos, int64_t end,
+                                        int k) {
+  Seg s;
+  s.r = 0;
+  while (s.r + 1 < g.B && pos >= bar.req_pos0[s.r + 1]) ++s.r;
+  int64_t rem = pos - bar.req_pos0[s.r];
+  const int ph = bar.req_per_head[s.r];
+  s.h = (int)(rem / ph);
+  rem -= (int64_t)s.h * ph;
+  const ReqDesc &R = g.req[s.r];
+  s.n_hist = bar.req_hist[s.r];
+  s.mt = 0;
+  for (;;) {
+    const int n = unit_geom<NK>(R, s.n_hist, s.mt).n_tiles;
+    if (rem < n) break;
+    rem -= n;
+    ++s.mt;
+  }
+  s.t0 = (int)rem;
+  s.ustart = pos - s.t0;
+  s.u = unit_geom<NK>(R, s.n_hist, s.mt);
+  s.t1 = (int)min((int64_t)s.u.n_tiles, (int64_t)s.t0 + (end - pos));
+  s.kvh = s.h / (g.H / g.Hkv);
+  s.m0 = s.mt * ROWS;
+  s.uid = bar.req_unit0[s.r] + s.h * ((R.lq + ROWS - 1) / ROWS) + s.mt;
+  s.partial = !(s.t0 == 0 && s.t1 == s.u.n_tiles);
+  s.slot = k == 0 ? 0 : 1;
+  return s;
+}
+
+// 32 consecutive values of an output row: fp32 (partials), or bf16 with
+// 256-bit stores when rows are 32-byte aligned, else 128-bit stores.
+__device__ __forceinline__ void store_f32x32(float *dst, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 8)
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + j),
+                 "f"(v[j]), "f"(v[j + 1]), "f"(v[j + 2]), "f"(v[j + 3]), "f"(v[j + 4]),
+                 "f"(v[j + 5]), "f"(v[j + 6]), "f"(v[j + 7])
+                 : "memory");
+}
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&v)[32], bool v8) {
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+  if (v8) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 8)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 2 * j),
+                   "r"(w[j]), "r"(w[j + 1]), "r"(w[j + 2]), "r"(w[j + 3]), "r"(w[j + 4]),
+                   "r"(w[j + 5]), "r"(w[j + 6]), "r"(w[j + 7])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      *reinterpret_cast<uint4 *>(dst + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+  }
+}
+// 8 fp32 of another CTA's partial result, read at L2 (never a stale L1 line).
+__device__ __forceinline__ void load_part8(const float *src, float *v) {
+  asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(src)
+               : "memory");
+}
+
 template <int D, int NK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ Geo g, const __grid_constant__ TMaps tm,
                    const int32_t *__restrict__ sel_page, const int32_t *__restrict__ n_sel,
-                   float scale_log2, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse) {
+                   float scale_log2, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
+                   int o_v8, float *__restrict__ part_o, float *__restrict__ part_lse,
+                   int32_t *__restrict__ unit_cnt) {
   using LY = Layout<D, NK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -83,43 +232,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int *abort = &bar.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cta = blockIdx.x;
-  const int r = find_req(g, cta, [](const ReqDesc &d) { return d.att0; });
-  const ReqDesc &R = g.req[r];
-  const int mt_n = (R.lq + ROWS - 1) / ROWS;
-  const int local = cta - R.att0;
-  const int G = g.H / g.Hkv;
-  // longest causal tiles first, all heads of a row tile together
-  const int h = local % g.H;
-  const int mt = mt_n - 1 - local / g.H;
-  const int kvh = h / G;
-  const int m0 = mt * ROWS;
-  const bool has_b = m0 + BM < R.lq;
-
-  const int kbh = R.kh / g.Bk;
-  int nh = n_sel[r];
-  nh = nh < 0 ? 0 : (nh > kbh ? kbh : nh);
   const int sub = g.Bk / NK;
-  const int n_hist = nh * sub;
-  // current-chunk tiles up to the last row of each query tile
-  const int n_a = n_hist + (min(m0 + BM, R.lq) - 1) / NK + 1;
-  const int n_b = has_b ? n_hist + (min(m0 + ROWS, R.lq) - 1) / NK + 1 : 0;
-  const int n_tiles = has_b ? n_b : n_a;
-  const int32_t *pages = sel_page + (int64_t)r * g.bt_stride;
+  const int G = gridDim.x;
 
   if (tid == 0) {
-    mbar_init(&bar.q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar.q_full[x], 1);
+      mbar_init(&bar.q_empty[x], 1);
+      mbar_init(&bar.s_full[x], 1);
+      mbar_init(&bar.p_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&bar.pv_done[x], 1);
+      mbar_init(&bar.grp[x], 4);
+    }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar.full[s], 1);
       mbar_init(&bar.empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar.s_full[x], 1);
-      mbar_init(&bar.p_full[x], 4);  // one arrival per softmax warp
-      mbar_init(&bar.pv_done[x], 1);
-    }
     mbar_init(&bar.drain, 1);
     bar.abort = 0;
+    build_tables<NK>(g, n_sel, bar);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -130,6 +261,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
+  const int64_t total = bar.total;
+  const int64_t beg = cta_begin(total, blockIdx.x, G);
+  const int64_t end = cta_begin(total, blockIdx.x + 1, G);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -139,56 +273,81 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tm.q);
       tma_prefetch_desc(&tm.kc);
       tma_prefetch_desc(&tm.vc);
-      if (n_hist) {
-        tma_prefetch_desc(&tm.kp);
-        tma_prefetch_desc(&tm.vp);
-      }
-      mbar_expect_tx(&bar.q_full, (has_b ? 2 : 1) * LY::Q_BYTES);
-      for (int x = 0; x < (has_b ? 2 : 1); ++x)
-        for (int hf = 0; hf < LY::HALVES; ++hf)
-          tma_load_3d(smem + LY::OFF_Q + x * LY::Q_BYTES + hf * (BM * 128), &tm.q, &bar.q_full,
-                      hf * 64, R.q0 + m0 + x * BM, h);
+      tma_prefetch_desc(&tm.kp);
+      tma_prefetch_desc(&tm.vp);
     }
-    int issued = 0;  // loads: K(t) = 2t, V(t) = 2t+1
-    int pg = 0;      // page id of tile (t & ~31) + lane
-    for (int i = 0; i < 2 * n_tiles; ++i) {
-      const int t = i >> 1;
-      if ((i & 63) == 0) {  // next 32 tiles' page ids, one per lane
-        const int tt = t + lane;
-        pg = tt < n_hist ? __ldg(pages + tt / sub) : 0;
-      }
-      const int p_t = __shfl_sync(0xffffffffu, pg, t & 31);
-      const int s = i % NSLOT;
-      int ok = 1;  // lane 0 waits, the warp follows its verdict
-      if (lane == 0 && i >= NSLOT) ok = mbar_wait(&bar.empty[s], ((i / NSLOT) - 1) & 1, abort, g.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) {
-        const bool is_v = i & 1;
-        uint8_t *dst = smem + LY::OFF_KV + s * LY::KV_BYTES;
-        mbar_expect_tx(&bar.full[s], LY::KV_BYTES);
-        if (t < n_hist) {
-          const int p = (p_t < 0 || p_t >= g.num_pages) ? 0 : p_t;  // masked by the softmax
-          const int tok = (t % sub) * NK;
-          for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_4d(dst + hf * (NK * 128), is_v ? &tm.vp : &tm.kp, &bar.full[s], hf * 64,
-                        kvh, tok, p);
-        } else {
-          const int j0 = (t - n_hist) * NK;
-          for (int hf = 0; hf < LY::HALVES; ++hf)
-            tma_load_3d(dst + hf * (NK * 128), is_v ? &tm.vc : &tm.kc, &bar.full[s], hf * 64,
-                        R.q0 + j0, kvh);
+    int i = 0;             // K/V loads issued so far (ring position)
+    int qn[2] = {0, 0};    // Q_A / Q_B loads issued so far
+    bool ok = true;
+    int k = 0;
+    for (int64_t pos = beg; ok && pos < end; ++k) {
+      const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+      pos += sg.t1 - sg.t0;
+      const ReqDesc &R = g.req[sg.r];
+      const int32_t *pages = sel_page + (int64_t)sg.r * g.bt_stride;
+      for (int x = 0; x < (sg.u.has_b ? 2 : 1); ++x) {
+        int okq = 1;  // Q_x of the previous segment no longer read by an S MMA
+        if (lane == 0 && qn[x] > 0) okq = mbar_wait(&bar.q_empty[x], (qn[x] - 1) & 1, abort, g.err);
+        if (!__shfl_sync(0xffffffffu, okq, 0)) {
+          ok = false;
+          break;
         }
+        if (lane == 0) {
+          mbar_expect_tx(&bar.q_full[x], LY::Q_BYTES);
+          for (int hf = 0; hf < LY::HALVES; ++hf)
+            tma_load_3d(smem + LY::OFF_Q + x * LY::Q_BYTES + hf * (BM * 128), &tm.q,
+                        &bar.q_full[x], hf * 64, R.q0 + sg.m0 + x * BM, sg.h);
+        }
+        ++qn[x];
       }
-      issued = i + 1;
+      if (!ok) break;
+      int pg = 0;
+      for (int t = sg.t0; t < sg.t1; ++t) {
+        if (((t - sg.t0) & 31) == 0) {  // next 32 tiles' page ids, one per lane
+          const int tt = t + lane;
+          pg = tt < sg.n_hist ? __ldg(pages + tt / sub) : 0;
+        }
+        const int p_t = __shfl_sync(0xffffffffu, pg, (t - sg.t0) & 31);
+        for (int kv = 0; kv < 2; ++kv, ++i) {
+          const int s = i % NSLOT;
+          int oks = 1;  // lane 0 waits, the warp follows its verdict
+          if (lane == 0 && i >= NSLOT)
+            oks = mbar_wait(&bar.empty[s], ((i / NSLOT) - 1) & 1, abort, g.err);
+          if (!__shfl_sync(0xffffffffu, oks, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t *dst = smem + LY::OFF_KV + s * LY::KV_BYTES;
+            mbar_expect_tx(&bar.full[s], LY::KV_BYTES);
+            if (t < sg.n_hist) {
+              const int p = (p_t < 0 || p_t >= g.num_pages) ? 0 : p_t;  // masked by the softmax
+              const int tok = (t % sub) * NK;
+              for (int hf = 0; hf < LY::HALVES; ++hf)
+                tma_load_4d(dst + hf * (NK * 128), kv ? &tm.vp : &tm.kp, &bar.full[s], hf * 64,
+                            sg.kvh, tok, p);
+            } else {
+              const int j0 = (t - sg.n_hist) * NK;
+              for (int hf = 0; hf < LY::HALVES; ++hf)
+                tma_load_3d(dst + hf * (NK * 128), kv ? &tm.vc : &tm.kc, &bar.full[s], hf * 64,
+                            R.q0 + j0, sg.kvh);
+            }
+          }
+        }
+        if (!ok) break;
+      }
     }
     // drain: every load issued must land before shared memory is released
-    // (only the last NSLOT can still be in flight)
+    // (only the last Q of each tile and the last NSLOT K/V can be in flight)
     if (lane == 0) {
-      for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.q_full, 0); ++k) {
-      }
-      for (int i = max(0, issued - NSLOT); i < issued; ++i) {
-        const uint32_t par = (i / NSLOT) & 1;
-        for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.full[i % NSLOT], par); ++k) {
+      for (int x = 0; x < 2; ++x)
+        if (qn[x] > 0)
+          for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.q_full[x], (qn[x] - 1) & 1);
+               ++n) {
+          }
+      for (int j = max(0, i - NSLOT); j < i; ++j) {
+        const uint32_t par = (j / NSLOT) & 1;
+        for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.full[j % NSLOT], par); ++n) {
         }
       }
     }
@@ -199,17 +358,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idPV = idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = smem_addr(smem + LY::OFF_Q);
       const uint32_t sKV = smem_addr(smem + LY::OFF_KV);
-      auto slot_wait = [&](int i) {
-        return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
-      };
       // Descriptors are built once; a k-step only adds its byte offset / 16 to
       // the start-address field (all operands lie below 256 KB of shared memory).
       const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);
       const uint64_t dV0 = sdesc_sw128(sKV, NK * 128, 1024);
-      auto issue_S = [&](int x, int t) {
+      auto slot_wait = [&](int i) {
+        return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
+      };
+      auto issue_S = [&](int x, int i) {  // i: load index of the K tile
         const uint64_t a0 = dQ0 + (uint64_t)((x * LY::Q_BYTES) >> 4);
-        const uint64_t b0 = dK0 + (uint64_t)((((2 * t) % NSLOT) * LY::KV_BYTES) >> 4);
+        const uint64_t b0 = dK0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
         const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -218,8 +377,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                      kk > 0 ? 1u : 0u);
         mma_commit(&bar.s_full[x]);
       };
-      auto issue_PV = [&](int x, int t) {
-        const uint64_t b0 = dV0 + (uint64_t)((((2 * t + 1) % NSLOT) * LY::KV_BYTES) >> 4);
+      auto issue_PV = [&](int x, int i, bool first) {  // i: load index of the V tile
+        const uint64_t b0 = dV0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
         const uint32_t d = tmem + 256 + x * 128;
         const uint32_t a = tmem + x * 128;
         // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
@@ -228,169 +387,288 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk)
           mma_f16_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idPV,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+                     (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bar.pv_done[x]);
       };
-      bool ok = mbar_wait(&bar.q_full, 0, abort, g.err);
-      if (ok && n_tiles > 0) {
-        ok = slot_wait(0);
-        if (ok) {
+      int ib = 0;           // load index of the segment's first K tile
+      int cnt[2] = {0, 0};  // tiles each softmax warpgroup has handed over so far
+      int qm[2] = {0, 0};   // Q_A / Q_B loads consumed
+      int k = 0;
+      bool ok = true;
+      for (int64_t pos = beg; ok && pos < end; ++k) {
+        const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+        pos += sg.t1 - sg.t0;
+        const int nt = sg.t1 - sg.t0;
+        const int na = max(0, min(sg.u.n_a, sg.t1) - sg.t0);
+        const int nb = sg.u.has_b ? max(0, min(sg.u.n_b, sg.t1) - sg.t0) : 0;
+        for (int x = 0; ok && x < (sg.u.has_b ? 2 : 1); ++x)
+          ok = mbar_wait(&bar.q_full[x], qm[x]++ & 1, abort, g.err);
+        if (!ok || !slot_wait(ib)) break;
+        tc_fence_after();
+        // Q_x is released (q_empty) once the segment's last S_x has been issued
+        if (na > 0) issue_S(0, ib);
+        if (na <= 1) mma_commit(&bar.q_empty[0]);
+        if (nb > 0) issue_S(1, ib);
+        if (sg.u.has_b && nb <= 1) mma_commit(&bar.q_empty[1]);
+        mma_commit(&bar.empty[ib % NSLOT]);
+        for (int j = 0; j < nt; ++j) {
+          const int iK = ib + 2 * j, iV = iK + 1;
+          if (!slot_wait(iV)) {
+            ok = false;
+            break;
+          }
+          if (j < na) {
+            if (!mbar_wait(&bar.p_full[0], (cnt[0] + j) & 1, abort, g.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_PV(0, iV, j == 0);
+          }
+          if (j + 1 < nt && !slot_wait(iK + 2)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_S(0, 0);
-          if (has_b) issue_S(1, 0);
-          mma_commit(&bar.empty[0]);
+          if (j + 1 < na) {  // the softmax has consumed S_A(j)
+            issue_S(0, iK + 2);
+            if (j + 2 == na) mma_commit(&bar.q_empty[0]);
+          }
+          if (j < nb) {
+            if (!mbar_wait(&bar.p_full[1], (cnt[1] + j) & 1, abort, g.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_PV(1, iV, j == 0);
+          }
+          mma_commit(&bar.empty[iV % NSLOT]);  // V(j) consumed
+          if (j + 1 < nb) {
+            issue_S(1, iK + 2);
+            if (j + 2 == nb) mma_commit(&bar.q_empty[1]);
+          }
+          if (j + 1 < nt) mma_commit(&bar.empty[(iK + 2) % NSLOT]);  // K(j+1) consumed
         }
-      }
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const bool a_now = t < n_a, a_next = t + 1 < n_a;
-        const bool b_now = t < n_b, b_next = t + 1 < n_b;
-        const bool next = t + 1 < n_tiles;
-        if (!slot_wait(2 * t + 1)) break;  // V(t)
-        if (a_now) {
-          if (!mbar_wait(&bar.p_full[0], t & 1, abort, g.err)) break;
-          tc_fence_after();
-          issue_PV(0, t);
-        }
-        if (next && !slot_wait(2 * t + 2)) break;  // K(t+1)
-        if (a_next) {  // the softmax has consumed S_A(t): it arrived p_full
-          tc_fence_after();
-          issue_S(0, t + 1);
-        }
-        if (b_now) {
-          if (!mbar_wait(&bar.p_full[1], t & 1, abort, g.err)) break;
-          tc_fence_after();
-          issue_PV(1, t);
-        }
-        mma_commit(&bar.empty[(2 * t + 1) % NSLOT]);  // V(t) consumed
-        if (b_next) {
-          tc_fence_after();
-          issue_S(1, t + 1);
-        }
-        if (next) mma_commit(&bar.empty[(2 * t + 2) % NSLOT]);  // K(t+1) consumed
+        ib += 2 * nt;
+        cnt[0] += na;
+        cnt[1] += nb;
       }
       // every MMA issued has completed before TMEM is freed
       mma_commit(&bar.drain);
-      for (uint32_t k = 0; k < kSpinLimit && !mbar_try_wait(&bar.drain, 0); ++k) {
+      for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.drain, 0); ++n) {
       }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int x = (warp - 4) >> 2;         // query tile: 0 = A, 1 = B
-    const int n_x = x ? n_b : n_a;
-    const int row = tid - 128 - x * BM;    // row within the tile == TMEM lane
-    const int qrow = m0 + x * BM + row;    // chunk-local query index
+    const int x = (warp - 4) >> 2;       // query tile: 0 = A, 1 = B
+    const int row = tid - 128 - x * BM;  // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t s_col = x * 128, o_col = 256 + x * 128;
-    float m_run = -INFINITY, l_run = 0.f;
+    int cnt = 0;  // tiles handed over so far
+    int gb = 0;   // uses of this warpgroup's barrier
+    // warpgroup barrier on an mbarrier: bounded, so a peer that gave up on a
+    // timeout cannot leave the others waiting forever
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.grp[x]);
+      return mbar_wait(&bar.grp[x], gb++ & 1, abort, g.err);
+    };
+    int k = 0;
     bool ok = true;
-    int p_next = (n_hist > 0) ? __ldg(pages) : 0;
-    for (int t = 0; t < n_x; ++t) {
-      const int p_cur = p_next;
-      if (t + 1 < n_hist) p_next = __ldg(pages + (t + 1) / sub);
-      if (!mbar_wait(&bar.s_full[x], t & 1, abort, g.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[NK];
-#pragma unroll
-      for (int c = 0; c < NK / 32; ++c)
-        tmem_ld32(lane_addr + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_ld_wait();
-
-      if (t < n_hist) {
-        if (p_cur < 0 || p_cur >= g.num_pages) {  // invalid page: skip its keys
-#pragma unroll
-          for (int j = 0; j < NK; ++j) sr[j] = __float_as_uint(-INFINITY);
-          if (row == 0 && (t % sub) == 0) record_error(g.err, XATTN_EPAGE);
+    for (int64_t pos = beg; ok && pos < end; ++k) {
+      const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+      pos += sg.t1 - sg.t0;
+      const ReqDesc &R = g.req[sg.r];
+      const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
+      const int nx = max(0, min(n_x, sg.t1) - sg.t0);
+      const int qrow = sg.m0 + x * BM + row;  // chunk-local query index
+      const int32_t *pages = sel_page + (int64_t)sg.r * g.bt_stride;
+      float m_run = -INFINITY, l_run = 0.f;
+      int pg = 0;
+      for (int j = 0; j < nx; ++j) {
+        const int t = sg.t0 + j;
+        if ((j & 31) == 0) {  // next 32 tiles' page ids, one per lane
+          const int tt = t + lane;
+          pg = tt < sg.n_hist ? __ldg(pages + tt / sub) : 0;
         }
-      } else {
-        const int lim = qrow - (t - n_hist) * NK + 1;  // keys [0, lim) are visible
-        if (lim < NK) {
-#pragma unroll
-          for (int j = 0; j < NK; ++j)
-            if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
+        const int p_cur = __shfl_sync(0xffffffffu, pg, j & 31);
+        if (!mbar_wait(&bar.s_full[x], (cnt + j) & 1, abort, g.err)) {
+          ok = false;
+          break;
         }
-      }
-      // softmax_scale > 0, so the row max of the scaled logits is the scaled max
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        tc_fence_after();
+        uint32_t sr[NK];
 #pragma unroll
-      for (int j = 0; j < NK; j += 8)
+        for (int c = 0; c < NK / 32; ++c)
+          tmem_ld32(lane_addr + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_ld_wait();
+        if (t < sg.n_hist) {
+          if (p_cur < 0 || p_cur >= g.num_pages) {  // invalid page: skip its keys
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          m4[e] = fmax3(m4[e], __uint_as_float(sr[j + 2 * e]), __uint_as_float(sr[j + 2 * e + 1]));
-      const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * scale_log2;
-      const float mnew = fmaxf(m_run, mt);
-      const bool need = mnew > m_run + 8.f;
-      const float alpha = need ? ex2(m_run - mnew) : 1.f;
-      const float m_use = need ? mnew : m_run;
-      const float nb = m_use == -INFINITY ? 0.f : -m_use;
-      const uint64_t sc2 = f2(scale_log2, scale_log2), nb2 = f2(nb, nb);
-      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-      // P row -> the S row's TMEM columns (two bf16 per column), the A operand
-      // of P V, 64 keys at a time; PV_x(t-1) finished before S_x(t) did
+            for (int jj = 0; jj < NK; ++jj) sr[jj] = __float_as_uint(-INFINITY);
+            if (row == 0 && (t % sub) == 0) record_error(g.err, XATTN_EPAGE);
+          }
+        } else {
+          const int lim = qrow - (t - sg.n_hist) * NK + 1;  // keys [0, lim) are visible
+          if (lim < NK) {
 #pragma unroll
-      for (int hb = 0; hb < NK / 64; ++hb) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          float x0, x1;
-          unf2(ffma2(f2(__uint_as_float(sr[hb * 64 + j]), __uint_as_float(sr[hb * 64 + j + 1])),
-                     sc2, nb2),
-               x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          sum2[(j >> 1) & 3] = fadd2(sum2[(j >> 1) & 3], f2(p0, p1));
-          pk[j >> 1] = pack_bf16x2(p0, p1);
+            for (int jj = 0; jj < NK; ++jj)
+              if (jj >= lim) sr[jj] = __float_as_uint(-INFINITY);
+          }
         }
-        tmem_st32(lane_addr + s_col + hb * 32, pk);
+        // softmax_scale > 0, so the row max of the scaled logits is the scaled max
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int jj = 0; jj < NK; jj += 8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            m4[e] = fmax3(m4[e], __uint_as_float(sr[jj + 2 * e]),
+                          __uint_as_float(sr[jj + 2 * e + 1]));
+        const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * scale_log2;
+        const float mnew = fmaxf(m_run, mt);
+        const bool need = mnew > m_run + 8.f;
+        const float alpha = need ? ex2(m_run - mnew) : 1.f;
+        const float m_use = need ? mnew : m_run;
+        const float nb = m_use == -INFINITY ? 0.f : -m_use;
+        const uint64_t sc2 = f2(scale_log2, scale_log2), nb2 = f2(nb, nb);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+        // P row -> the S row's TMEM columns (two bf16 per column), the A operand
+        // of P V, 64 keys at a time; PV_x of the previous tile finished before
+        // this S did
+#pragma unroll
+        for (int hb = 0; hb < NK / 64; ++hb) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int jj = 0; jj < 64; jj += 2) {
+            const uint64_t xx = ffma2(
+                f2(__uint_as_float(sr[hb * 64 + jj]), __uint_as_float(sr[hb * 64 + jj + 1])), sc2,
+                nb2);
+            float x0, x1;
+            unf2(xx, x0, x1);
+            const uint64_t pp = f2(ex2(x0), ex2(x1));
+            sum2[(jj >> 1) & 3] = fadd2(sum2[(jj >> 1) & 3], pp);
+            float p0, p1;
+            unf2(pp, p0, p1);
+            pk[jj >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(lane_addr + s_col + hb * 32, pk);
+        }
+        float s0, s1, s2, s3;
+        unf2(fadd2(sum2[0], sum2[1]), s0, s1);
+        unf2(fadd2(sum2[2], sum2[3]), s2, s3);
+        l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+        m_run = m_use;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {  // O_x is stable: the previous PV is done
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(lane_addr + o_col + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              ov[jj] = __float_as_uint(__uint_as_float(ov[jj]) * alpha);
+            tmem_st32(lane_addr + o_col + c * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.p_full[x]);
       }
-      float s0, s1, s2, s3;
-      unf2(fadd2(sum2[0], sum2[1]), s0, s1);
-      unf2(fadd2(sum2[2], sum2[3]), s2, s3);
-      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
-      m_run = m_use;
-      if (t > 0 && __any_sync(0xffffffffu, need)) {
+      if (!ok) break;
+      cnt += nx;
+      // segment epilogue: O normalised and written -- final (bf16) when the
+      // segment is the whole unit, else a partial result (fp32 O, LSE) in this
+      // CTA's slot.  Tile x exists (rows below lq) iff x == 0 or has_b.
+      if (x == 1 && !sg.u.has_b) continue;
+      const bool wr = qrow < R.lq;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      const int64_t prow = ((int64_t)blockIdx.x * 2 + sg.slot) * ROWS + x * BM + row;
+      __nv_bfloat16 *orow = o + (int64_t)sg.h * g.q_hs + (int64_t)(R.q0 + qrow) * D;
+      float *lrow = lse + (int64_t)sg.h * g.lse_hs + R.q0 + qrow;
+      if (nx > 0) {
+        if (!mbar_wait(&bar.pv_done[x], (cnt - 1) & 1, abort, g.err)) break;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(lane_addr + o_col + c * 32, ov);
           tmem_ld_wait();
+          if (!wr) continue;
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tmem_st32(lane_addr + o_col + c * 32, ov);
+          for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(ov[jj]) * inv;
+          if (sg.partial)
+            store_f32x32(part_o + prow * D + c * 32, v);
+          else
+            store_bf16x32(orow + c * 32, v, o_v8 != 0);
         }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.p_full[x]);
-    }
-    // epilogue: wait for the last P V, normalise, write O and LSE
-    if (ok && n_x > 0 && mbar_wait(&bar.pv_done[x], (n_x - 1) & 1, abort, g.err)) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const bool wr = qrow < R.lq;
-      __nv_bfloat16 *orow = o + (int64_t)h * g.q_hs + (int64_t)(R.q0 + qrow) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(lane_addr + o_col + c * 32, ov);
-        tmem_ld_wait();
-        if (wr) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + j) = v;
-          }
-        }
+      if (wr) {
+        if (sg.partial)
+          part_lse[prow] = lse_v;  // -inf marks an empty part (no tile of this query tile)
+        else
+          *lrow = lse_v;
       }
-      if (wr)
-        lse[(int64_t)h * g.lse_hs + R.q0 + qrow] =
-            l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      if (!sg.partial) continue;
+      // ---- split unit: count this part in; the last part merges them all.
+      // Parts: the CTAs c0..c1 whose ranges meet the unit's items; the unit is
+      // c0's last segment (slot 1) unless it starts c0's range, and the first
+      // segment (slot 0) of every later CTA.
+      const int64_t uend = sg.ustart + sg.u.n_tiles;
+      const int c0 = cta_of(total, G, sg.ustart), c1 = cta_of(total, G, uend - 1);
+      __threadfence();  // this thread's part is visible GPU-wide
+      if (!group_sync()) break;
+      if (row == 0) {
+        int nparts = 0;
+        for (int c = c0; c <= c1; ++c) nparts += cta_begin(total, c, G) < cta_begin(total, c + 1, G);
+        __threadfence();
+        const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, 1);
+        __threadfence();
+        bar.last[x] = before == nparts - 1;
+      }
+      if (!group_sync()) break;
+      if (!*reinterpret_cast<volatile int *>(&bar.last[x]) || !wr) continue;
+      __threadfence();
+      auto part_row = [&](int c) -> int64_t {  // -1: CTA without items
+        const int64_t bc = cta_begin(total, c, G);
+        if (bc == cta_begin(total, c + 1, G)) return -1;
+        const int slot = (c == c0 && bc < sg.ustart) ? 1 : 0;
+        return ((int64_t)c * 2 + slot) * ROWS + x * BM + row;
+      };
+      float M = -INFINITY;
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t pr = part_row(c);
+        if (pr >= 0) M = fmaxf(M, __ldcg(part_lse + pr));
+      }
+      float den = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t pr = part_row(c);
+        if (pr < 0) continue;
+        const float lp = __ldcg(part_lse + pr);
+        if (lp != -INFINITY) den += __expf(lp - M);
+      }
+      const float rden = den > 0.f ? 1.f / den : 0.f;
+      for (int cb = 0; cb < D / 32; ++cb) {
+        float acc[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
+        for (int c = c0; c <= c1; ++c) {
+          const int64_t pr = part_row(c);
+          if (pr < 0) continue;
+          const float lp = __ldcg(part_lse + pr);
+          if (lp == -INFINITY) continue;  // no key of this row in the part (O not written)
+          const float w = __expf(lp - M) * rden;
+          float v[32];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) load_part8(part_o + pr * D + cb * 32 + q8 * 8, v + q8 * 8);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) acc[jj] = fmaf(w, v[jj], acc[jj]);
+        }
+        store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
+      }
+      *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
     }
   }
 
@@ -400,14 +678,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// ---------------------------------------------------------------------------
-// Host side: tensor maps and launch
-// ---------------------------------------------------------------------------
 template <int D, int NK>
-cudaError_t launch_tc(const Geo &g, int nctas, const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
+cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                       const __nv_bfloat16 *vcur, const __nv_bfloat16 *kpool,
                       const __nv_bfloat16 *vpool, const int32_t *sel_page, const int32_t *n_sel,
-                      float scale, __nv_bfloat16 *o, float *lse, cudaStream_t st) {
+                      float scale, __nv_bfloat16 *o, float *lse, float *part_o, float *part_lse,
+                      int32_t *unit_cnt, int nunits, cudaStream_t st) {
   TMaps tm;
   const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
   {
@@ -436,11 +712,17 @@ cudaError_t launch_tc(const Geo &g, int nctas, const __nv_bfloat16 *q, const __n
     tm.vp = tm.vc;
   }
   using LY = Layout<D, NK>;
+  static_assert(sizeof(Bars) <= 1536, "barrier block");
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, NK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<D, NK><<<nctas, THREADS, LY::SMEM_ALLOC, st>>>(
-      g, tm, sel_page, n_sel, scale * 1.4426950408889634f, o, lse);
+  // per-unit part counters start at zero
+  e = cudaMemsetAsync(unit_cnt, 0, (size_t)nunits * 2 * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  const int o_v8 = (reinterpret_cast<uintptr_t>(o) % 32 == 0) && ((g.q_hs * 2) % 32 == 0);
+  attn_tc_kernel<D, NK><<<grid, THREADS, LY::SMEM_ALLOC, st>>>(
+      g, tm, sel_page, n_sel, scale * 1.4426950408889634f, o, lse, o_v8, part_o, part_lse,
+      unit_cnt);
   return cudaGetLastError();
 }
 
@@ -450,19 +732,25 @@ cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
                              const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,
                              const int32_t *sel_page, const int32_t *n_sel, float scale,
-                             __nv_bfloat16 *o, float *lse, cudaStream_t st) {
-  if (nctas == 0) return cudaSuccess;
+                             __nv_bfloat16 *o, float *lse, float *part_o, float *part_lse,
+                             int32_t *unit_cnt, cudaStream_t st) {
+  if (nctas == 0) return cudaSuccess;  // no query rows
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int grid = sms < kAttnMaxCtas ? sms : kAttnMaxCtas;
   const bool wide = g.Bk % 128 == 0;  // KV tile: 128 keys, else 64
   if (g.D == 128)
-    return wide ? launch_tc<128, 128>(g, nctas, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
-                                      scale, o, lse, st)
-                : launch_tc<128, 64>(g, nctas, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
-                                     scale, o, lse, st);
+    return wide ? launch_tc<128, 128>(g, grid, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
+                                      scale, o, lse, part_o, part_lse, unit_cnt, nctas, st)
+                : launch_tc<128, 64>(g, grid, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
+                                     scale, o, lse, part_o, part_lse, unit_cnt, nctas, st);
   if (g.D == 64)
-    return wide ? launch_tc<64, 128>(g, nctas, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
-                                     scale, o, lse, st)
-                : launch_tc<64, 64>(g, nctas, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
-                                    scale, o, lse, st);
+    return wide ? launch_tc<64, 128>(g, grid, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
+                                     scale, o, lse, part_o, part_lse, unit_cnt, nctas, st)
+                : launch_tc<64, 64>(g, grid, q, kcur, vcur, kpool, vpool, sel_page, n_sel,
+                                    scale, o, lse, part_o, part_lse, unit_cnt, nctas, st);
   return cudaErrorInvalidValue;
 }
 

@@ -11,7 +11,8 @@ namespace xattn {
 
 constexpr int kMaxReq = XATTN_MAX_REQUESTS;
 constexpr int kTileCols = 128;  // columns of one softmax-statistics tile (score GEMM N tile)
-constexpr int kAttnRows = 256;  // query rows per attention CTA (two 128-row MMA tiles)
+constexpr int kAttnRows = 256;  // query rows per attention work unit (two 128-row MMA tiles)
+constexpr int kAttnMaxCtas = 160;  // persistent attention CTAs at most (one per SM)
 constexpr int kGemmRows = 256;  // reshaped rows per score-GEMM CTA (two 128-row MMA tiles)
 constexpr int kGemmCols = 256;  // reshaped columns per score-GEMM CTA
 constexpr int kBsumCols = 256;  // columns per block-sum CTA (one per thread)
@@ -70,7 +71,7 @@ __device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
 // Launch entry points implemented in the kernel translation units.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t scores, tstat, rstat, counts, kcat, total;
+  size_t scores, tstat, rstat, counts, kcat, part_o, part_lse, att_cnt, total;
 };
 
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
@@ -88,7 +89,8 @@ cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
                              const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,
                              const int32_t *sel_page, const int32_t *n_sel, float scale,
-                             __nv_bfloat16 *o, float *lse, cudaStream_t st);
+                             __nv_bfloat16 *o, float *lse, float *part_o, float *part_lse,
+                             int32_t *unit_cnt, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *o1, const float *l1, const float *o2, const float *l2,
                              int64_t rows, int D, void *o_out, int bf16_out, float *l_out,
                              cudaStream_t st);

@@ -57,7 +57,7 @@ def prefill_chunk(problem, q, k_cur, v_cur, k_pool, v_pool, tau, bufs: ChunkBuff
     X.xattn_select(problem, bufs.block_sums, tau, bufs.workspace, bufs.mask, bufs.sel_idx,
                    bufs.sel_page, bufs.n_sel, stream)
     X.bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, bufs.sel_page, bufs.n_sel,
-                          softmax_scale, o, lse, stream)
+                          softmax_scale, bufs.workspace, o, lse, stream)
 
 
 class SequencePrefill:

@@ -79,7 +79,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
         "xattn_select": (ctypes.c_int, [P, vp, f64, vp, sz, vp, vp, vp, vp, vp]),
         "xattn_select_noalloc": (ctypes.c_int, [P, vp, f64, vp, vp, vp, vp, vp]),
-        "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp]),
+        "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, sz, vp, vp,
+                                                vp]),
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
         "xattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -205,10 +206,12 @@ def xattn_select_noalloc(problem, block_sums, threshold, mask, sel_idx, sel_page
 
 
 def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
-                        o, lse, stream=None):
+                        workspace, o, lse, stream=None):
     st = load_library().bsa_chunk_attention(problem.ref(), _ptr(q), _ptr(k_cur), _ptr(v_cur),
                                             _ptr(k_pool), _ptr(v_pool), _ptr(sel_page),
-                                            _ptr(n_sel), float(softmax_scale), _ptr(o), _ptr(lse),
+                                            _ptr(n_sel), float(softmax_scale), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _ptr(o), _ptr(lse),
                                             _stream(stream))
     _check(st, "bsa_chunk_attention")
 
