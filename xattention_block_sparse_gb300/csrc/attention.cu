@@ -21,9 +21,12 @@
 //                 previous segment's last S MMA on that tile has completed),
 //                 then K(t), V(t) for each KV tile t (one page of up to 128
 //                 keys) through a 5-slot ring of 128B-swizzled tiles.
-//   warp 1        MMA issuer, in the order PV_A(t), S_A(t+1), PV_B(t), S_B(t+1):
-//                 S_x = Q_x K^T into TMEM (128 lanes x NK fp32 columns), then
+//   warps 1, 2    MMA issuers of tiles A and B, taking turns so the pipe
+//                 sees S_A(0), S_B(0), PV_A(t), S_A(t+1), PV_B(t), S_B(t+1), ...:
+//                 S_x = Q_x K^T into TMEM (128 lanes x NK fp32 columns),
 //                 O_x += P_x V into a TMEM accumulator with P_x read from TMEM.
+//                 While the softmax of one tile runs, the pipe works for the
+//                 other; each issuer waits on its barriers during the other's turn.
 //   warps 4..7    softmax of tile A, warps 8..11 softmax of tile B: thread i
 //                 owns query row i (TMEM lane i).  It loads its S row, masks
 //                 the causal diagonal tile, keeps a running max (rescaling O in
@@ -72,6 +75,7 @@ struct Bars {
   uint64_t pv_done[2];
   uint64_t drain;
   uint64_t grp[2];                 // barrier of one softmax warpgroup (4 warp arrivals)
+  uint64_t tok[2];                 // MMA issuer turn tokens (tile A's, tile B's)
   uint32_t tmem_base;
   int abort;
   int last[2];                     // this CTA merges the unit (per query tile)
@@ -243,12 +247,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&bar.p_full[x], 4);  // one arrival per softmax warp
       mbar_init(&bar.pv_done[x], 1);
       mbar_init(&bar.grp[x], 4);
+      mbar_init(&bar.tok[x], 1);
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar.full[s], 1);
-      mbar_init(&bar.empty[s], 1);
+      mbar_init(&bar.empty[s], 2);  // released by both MMA issuers
     }
-    mbar_init(&bar.drain, 1);
+    mbar_init(&bar.drain, 2);
     bar.abort = 0;
     build_tables<NK>(g, n_sel, bar);
     fence_mbar_init();
@@ -351,109 +356,119 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues every MMA of query tile A, warp 2 those of tile B, taking
+    // turns (two token mbarriers) so the tensor pipe still sees the single
+    // ping-pong order S_A(0), S_B(0), [PV_A(t), S_A(t+1)], [PV_B(t), S_B(t+1)],
+    // ...: the softmax of one tile runs while the pipe works for the other.
+    // The pipe queues very few MMAs; each issuer does its barrier waits and
+    // bookkeeping while the other one's turn keeps the pipe fed.  A K/V slot
+    // is released when both issuers have let it go (two arrivals): a commit
+    // after the MMAs that read it, or, for a tile its query tile does not
+    // attend, a plain arrival once the tile has landed.
     if (lane == 0) {
+      const int x = warp - 1;
       constexpr uint32_t idS = idesc_bf16(BM, NK, 0, 0);
       constexpr uint32_t idPV = idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = smem_addr(smem + LY::OFF_Q);
       const uint32_t sKV = smem_addr(smem + LY::OFF_KV);
       // Descriptors are built once; a k-step only adds its byte offset / 16 to
       // the start-address field (all operands lie below 256 KB of shared memory).
-      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024) + (uint64_t)((x * LY::Q_BYTES) >> 4);
       const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);
       const uint64_t dV0 = sdesc_sw128(sKV, NK * 128, 1024);
+      const uint32_t tS = tmem + x * 128, tO = tmem + 256 + x * 128;
       auto slot_wait = [&](int i) {
         return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
       };
-      auto issue_S = [&](int x, int i) {  // i: load index of the K tile
-        const uint64_t a0 = dQ0 + (uint64_t)((x * LY::Q_BYTES) >> 4);
+      auto issue_S = [&](int i) {  // i: load index of the K tile
         const uint64_t b0 = dK0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
-        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16_ss(d, a0 + (uint64_t)(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4),
+          mma_f16_ss(tS, dQ + (uint64_t)(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4),
                      b0 + (uint64_t)(((kk / 4) * (NK * 128) + (kk % 4) * 32) >> 4), idS,
                      kk > 0 ? 1u : 0u);
         mma_commit(&bar.s_full[x]);
       };
-      auto issue_PV = [&](int x, int i, bool first) {  // i: load index of the V tile
+      auto issue_PV = [&](int i, bool first) {  // i: load index of the V tile
         const uint64_t b0 = dV0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
-        const uint32_t d = tmem + 256 + x * 128;
-        const uint32_t a = tmem + x * 128;
         // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
         // (d contiguous): the two 64-wide d blocks are NK*128 bytes apart,
         // 8-key groups 1024 apart
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk)
-          mma_f16_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idPV,
+          mma_f16_ts(tO, tS + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idPV,
                      (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bar.pv_done[x]);
       };
-      int ib = 0;           // load index of the segment's first K tile
-      int cnt[2] = {0, 0};  // tiles each softmax warpgroup has handed over so far
-      int qm[2] = {0, 0};   // Q_A / Q_B loads consumed
+      int turn = 0;  // turns taken: A's turn n follows B's turn n-1, B's turn n follows A's turn n
+      auto take_turn = [&]() {
+        const bool got = (x == 0 && turn == 0) ||
+                         mbar_wait(&bar.tok[x], (x == 0 ? turn - 1 : turn) & 1, abort, g.err);
+        ++turn;
+        return got;
+      };
+      auto pass_turn = [&]() { mbar_arrive(&bar.tok[1 - x]); };
+      int ib = 0;   // load index of the segment's first K tile
+      int cnt = 0;  // tiles the softmax of this query tile has handed over so far
+      int qm = 0;   // Q loads of this tile consumed
       int k = 0;
       bool ok = true;
       for (int64_t pos = beg; ok && pos < end; ++k) {
         const Seg sg = make_seg<NK>(g, bar, pos, end, k);
         pos += sg.t1 - sg.t0;
         const int nt = sg.t1 - sg.t0;
-        const int na = max(0, min(sg.u.n_a, sg.t1) - sg.t0);
-        const int nb = sg.u.has_b ? max(0, min(sg.u.n_b, sg.t1) - sg.t0) : 0;
-        for (int x = 0; ok && x < (sg.u.has_b ? 2 : 1); ++x)
-          ok = mbar_wait(&bar.q_full[x], qm[x]++ & 1, abort, g.err);
-        if (!ok || !slot_wait(ib)) break;
+        const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
+        const int nx = max(0, min(n_x, sg.t1) - sg.t0);
+        const bool has_q = x == 0 || sg.u.has_b;  // Q_x loaded for this segment
+        // turn 0 of the segment: S_x(0)
+        if (has_q && !mbar_wait(&bar.q_full[x], qm++ & 1, abort, g.err)) break;
+        if (nx > 0 && !slot_wait(ib)) break;
+        if (!take_turn()) break;
         tc_fence_after();
-        // Q_x is released (q_empty) once the segment's last S_x has been issued
-        if (na > 0) issue_S(0, ib);
-        if (na <= 1) mma_commit(&bar.q_empty[0]);
-        if (nb > 0) issue_S(1, ib);
-        if (sg.u.has_b && nb <= 1) mma_commit(&bar.q_empty[1]);
-        mma_commit(&bar.empty[ib % NSLOT]);
+        if (nx > 0) issue_S(ib);
+        if (has_q && nx <= 1) mma_commit(&bar.q_empty[x]);  // Q_x released after its last S
+        if (nx > 0) mma_commit(&bar.empty[ib % NSLOT]);
+        pass_turn();
         for (int j = 0; j < nt; ++j) {
           const int iK = ib + 2 * j, iV = iK + 1;
-          if (!slot_wait(iV)) {
-            ok = false;
-            break;
-          }
-          if (j < na) {
-            if (!mbar_wait(&bar.p_full[0], (cnt[0] + j) & 1, abort, g.err)) {
+          if (j < nx) {
+            // waits first, then the turn: PV_x(j) and S_x(j+1) back to back
+            if (!slot_wait(iV) || !mbar_wait(&bar.p_full[x], (cnt + j) & 1, abort, g.err) ||
+                (j + 1 < nx && !slot_wait(iK + 2)) || !take_turn()) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_PV(0, iV, j == 0);
-          }
-          if (j + 1 < nt && !slot_wait(iK + 2)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (j + 1 < na) {  // the softmax has consumed S_A(j)
-            issue_S(0, iK + 2);
-            if (j + 2 == na) mma_commit(&bar.q_empty[0]);
-          }
-          if (j < nb) {
-            if (!mbar_wait(&bar.p_full[1], (cnt[1] + j) & 1, abort, g.err)) {
+            issue_PV(iV, j == 0);  // the softmax has turned S_x(j) into P_x(j)
+            mma_commit(&bar.empty[iV % NSLOT]);
+            if (j + 1 < nx) {
+              issue_S(iK + 2);  // after PV_x(j): S_x(j+1) overwrites P_x(j)'s columns
+              if (j + 2 == nx) mma_commit(&bar.q_empty[x]);
+              mma_commit(&bar.empty[(iK + 2) % NSLOT]);
+            }
+            pass_turn();
+          } else {
+            // a tile beyond this query tile's last one: an empty turn, and K, V
+            // released once landed (their slots' previous phases are then complete)
+            if (!take_turn()) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            issue_PV(1, iV, j == 0);
+            pass_turn();
+            if (!slot_wait(iK) || !slot_wait(iV)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive(&bar.empty[iK % NSLOT]);
+            mbar_arrive(&bar.empty[iV % NSLOT]);
           }
-          mma_commit(&bar.empty[iV % NSLOT]);  // V(j) consumed
-          if (j + 1 < nb) {
-            issue_S(1, iK + 2);
-            if (j + 2 == nb) mma_commit(&bar.q_empty[1]);
-          }
-          if (j + 1 < nt) mma_commit(&bar.empty[(iK + 2) % NSLOT]);  // K(j+1) consumed
         }
         ib += 2 * nt;
-        cnt[0] += na;
-        cnt[1] += nb;
+        cnt += nx;
       }
-      // every MMA issued has completed before TMEM is freed
+      // every MMA issued (by both issuers) has completed before TMEM is freed
       mma_commit(&bar.drain);
       for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.drain, 0); ++n) {
       }
@@ -516,15 +531,20 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (jj >= lim) sr[jj] = __float_as_uint(-INFINITY);
           }
         }
-        // softmax_scale > 0, so the row max of the scaled logits is the scaled max
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // softmax_scale > 0, so the row max of the scaled logits is the scaled
+        // max; eight independent max chains keep the reduction short
+        float m8[8];
 #pragma unroll
-        for (int jj = 0; jj < NK; jj += 8)
+        for (int e = 0; e < 8; ++e)
+          m8[e] = fmax3(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), -INFINITY);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            m4[e] = fmax3(m4[e], __uint_as_float(sr[jj + 2 * e]),
-                          __uint_as_float(sr[jj + 2 * e + 1]));
-        const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * scale_log2;
+        for (int jj = 16; jj < NK; jj += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            m8[e] = fmax3(m8[e], __uint_as_float(sr[jj + 2 * e]), __uint_as_float(sr[jj + 2 * e + 1]));
+        const float mt =
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+            scale_log2;
         const float mnew = fmaxf(m_run, mt);
         const bool need = mnew > m_run + 8.f;
         const float alpha = need ? ex2(m_run - mnew) : 1.f;
