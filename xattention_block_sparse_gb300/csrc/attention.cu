@@ -62,7 +62,7 @@ struct Layout {
   static constexpr int OFF_Q = 0;                       // Q_A, Q_B
   static constexpr int OFF_KV = OFF_Q + 2 * Q_BYTES;    // ring
   static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
-  static constexpr int BYTES = OFF_BAR + 1536;
+  static constexpr int BYTES = OFF_BAR + 2048;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
 };
 
@@ -84,6 +84,10 @@ struct Bars {
   int32_t req_hist[kMaxReq];       // history KV tiles of the request (selected pages)
   int32_t req_per_head[kMaxReq];   // work items per head of the request
   int32_t req_unit0[kMaxReq];      // first unit id of the request
+  int32_t max_unit;                // largest unit (KV tiles)
+  int32_t whole_units;             // schedule: 1 = one whole unit per CTA, 0 = stream-K
+  int64_t beg, end;                // this CTA's work items
+  int32_t csk;                     // stream-K CTA index, -1 if this CTA has no range
 };
 
 struct TMaps {
@@ -113,6 +117,7 @@ __device__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
   int64_t pos = 0;
   int32_t unit = 0;
   const int sub = g.Bk / NK;
+  bar.max_unit = 0;
   for (int r = 0; r < g.B; ++r) {
     const ReqDesc &R = g.req[r];
     const int kbh = R.kh / g.Bk;
@@ -120,7 +125,11 @@ __device__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
     nh = nh < 0 ? 0 : (nh > kbh ? kbh : nh);
     const int n_hist = nh * sub;
     int per_head = 0, nmt = 0;
-    for (int mt = 0; mt * ROWS < R.lq; ++mt, ++nmt) per_head += unit_geom<NK>(R, n_hist, mt).n_tiles;
+    for (int mt = 0; mt * ROWS < R.lq; ++mt, ++nmt) {
+      const int n = unit_geom<NK>(R, n_hist, mt).n_tiles;
+      per_head += n;
+      bar.max_unit = max(bar.max_unit, n);
+    }
     bar.req_pos0[r] = pos;
     bar.req_hist[r] = n_hist;
     bar.req_per_head[r] = per_head;
@@ -143,6 +152,43 @@ __device__ __forceinline__ int cta_of(int64_t total, int G, int64_t pos) {
   while (c + 1 < G && cta_begin(total, c + 1, G) <= pos) ++c;
   while (c > 0 && cta_begin(total, c, G) > pos) --c;
   return c;
+}
+
+// The work of CTA blockIdx.x.  Two schedules, chosen from the tables alone
+// (every CTA takes the same decision):
+//  * whole units: CTA c takes unit c of the units ordered by decreasing row
+//    tile (the larger units first within a request), the hardware handing
+//    out CTAs as SMs free up -- no unit is split, no merge; used when the
+//    launch is small (under kWholeUnitsTiles items per SM) and no unit
+//    dwarfs a fair share, where stream-K's segment changes and merges cost
+//    more than the imbalance they remove;
+//  * stream-K: the last Gsk CTAs of the grid split the items evenly.
+constexpr int kWholeUnitsTiles = 160;
+template <int NK>
+__device__ void schedule(const Geo &g, Bars &bar, int Gsk) {
+  const int64_t total = bar.total;
+  const int grid = gridDim.x, c = blockIdx.x;
+  const int64_t share = (total + Gsk - 1) / Gsk;
+  bar.whole_units = share < kWholeUnitsTiles && 4 * (int64_t)bar.max_unit <= 5 * share;
+  bar.beg = bar.end = 0;
+  bar.csk = -1;
+  if (bar.whole_units) {
+    int r = 0;
+    while (r + 1 < g.B && c >= bar.req_unit0[r + 1]) ++r;
+    const ReqDesc &R = g.req[r];
+    const int nmt = (R.lq + ROWS - 1) / ROWS;
+    const int l = c - bar.req_unit0[r];
+    if (R.lq == 0 || l >= nmt * g.H) return;  // past the last unit
+    const int mt = nmt - 1 - l / g.H, h = l % g.H;
+    int64_t pos = bar.req_pos0[r] + (int64_t)h * bar.req_per_head[r];
+    for (int m = 0; m < mt; ++m) pos += unit_geom<NK>(R, bar.req_hist[r], m).n_tiles;
+    bar.beg = pos;
+    bar.end = pos + unit_geom<NK>(R, bar.req_hist[r], mt).n_tiles;
+  } else if (c >= grid - Gsk) {
+    bar.csk = c - (grid - Gsk);
+    bar.beg = cta_begin(total, bar.csk, Gsk);
+    bar.end = cta_begin(total, bar.csk + 1, Gsk);
+  }
 }
 
 // One contiguous piece of a unit handled by this CTA: tiles [t0, t1).
@@ -227,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const int32_t *__restrict__ sel_page, const int32_t *__restrict__ n_sel,
                    float scale_log2, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
                    int o_v8, float *__restrict__ part_o, float *__restrict__ part_lse,
-                   int32_t *__restrict__ unit_cnt) {
+                   int32_t *__restrict__ unit_cnt, int Gsk) {
   using LY = Layout<D, NK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -237,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = g.Bk / NK;
-  const int G = gridDim.x;
+  const int G = Gsk;  // stream-K CTAs
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -256,8 +302,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar.drain, 2);
     bar.abort = 0;
     build_tables<NK>(g, n_sel, bar);
+    schedule<NK>(g, bar, Gsk);
     fence_mbar_init();
   }
+  __syncthreads();
+  const int64_t total = bar.total;
+  const int64_t beg = bar.beg, end = bar.end;
+  const int csk = bar.csk;  // partial results only arise under stream-K
+  if (beg >= end) return;   // a CTA without work (uniform: before any TMEM use)
   if (warp == 1) {
     tmem_alloc(&bar.tmem_base, TMEM_COLS);
     tmem_relinquish();
@@ -266,9 +318,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
-  const int64_t total = bar.total;
-  const int64_t beg = cta_begin(total, blockIdx.x, G);
-  const int64_t end = cta_begin(total, blockIdx.x + 1, G);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -604,7 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool wr = qrow < R.lq;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-      const int64_t prow = ((int64_t)blockIdx.x * 2 + sg.slot) * ROWS + x * BM + row;
+      const int64_t prow = ((int64_t)csk * 2 + sg.slot) * ROWS + x * BM + row;
       __nv_bfloat16 *orow = o + (int64_t)sg.h * g.q_hs + (int64_t)(R.q0 + qrow) * D;
       float *lrow = lse + (int64_t)sg.h * g.lse_hs + R.q0 + qrow;
       if (nx > 0) {
@@ -665,7 +714,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float lps[MAXP];
         int np = 0;
         for (int c = c0; c <= c1; ++c) {
-          if (c == (int)blockIdx.x) continue;
+          if (c == csk) continue;
           const int64_t pr = part_row(c);
           const float lp = (pr >= 0 && wr) ? __ldcg(part_lse + pr) : -INFINITY;
           if (lp == -INFINITY) continue;  // no key of this row in the part (O not written)
@@ -799,7 +848,8 @@ cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv
     tm.vp = tm.vc;
   }
   using LY = Layout<D, NK>;
-  static_assert(sizeof(Bars) <= 1536, "barrier block");
+  static_assert(sizeof(Bars) <= 2048, "barrier block");
+  static_assert(LY::SMEM_ALLOC <= 232448, "dynamic shared memory of one CTA");
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, NK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
@@ -807,9 +857,13 @@ cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv
   e = cudaMemsetAsync(unit_cnt, 0, (size_t)nunits * 2 * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
   const int o_v8 = (reinterpret_cast<uintptr_t>(o) % 32 == 0) && ((g.q_hs * 2) % 32 == 0);
-  attn_tc_kernel<D, NK><<<grid, THREADS, LY::SMEM_ALLOC, st>>>(
+  // one CTA per unit (the whole-units schedule), at least Gsk (stream-K): the
+  // kernel decides on the device which of the two it runs
+  const int Gsk = grid;
+  const int ctas = nunits > Gsk ? nunits : Gsk;
+  attn_tc_kernel<D, NK><<<ctas, THREADS, LY::SMEM_ALLOC, st>>>(
       g, tm, sel_page, n_sel, scale * 1.4426950408889634f, o, lse, o_v8, part_o, part_lse,
-      unit_cnt);
+      unit_cnt, Gsk);
   return cudaGetLastError();
 }
 
