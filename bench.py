@@ -297,13 +297,13 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": workload_desc(args.workload, tau), "tokens_per_step": L,
                    "chunks": nchunk, "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "tensor", "kernel": "attn_kernel (bsa_chunk_attention)",
+        "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel (bsa_chunk_attention)",
                      "achieved": att_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": att_tflops / peaks["bf16_tflops"],
                      "frac_sustained": att_tflops / peaks["bf16_tflops_sustained"],
                      "peak_source": peak_src,
                      "traffic": traffic_for(("attention.cu", "tc_common.cuh", "common.cuh"),
-                                            "attn_kernel"),
+                                            "attn_tc_kernel"),
                      "launch_ms": att_launch_ms},
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "t_meas_ms": ms,
                           "frac": t_roof * 1e3 / ms},
