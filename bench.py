@@ -67,9 +67,11 @@ def chunk_work(cfg, c, chunk, n_sel):
     rq, ch = Lc // S, Lh // S
     cells = H * (rq * ch + rq * (rq + 1) // 2)
     f_est = 2 * S * D * cells
-    b_est_gemm = 2 * Hkv * D * (Lh + Lc) * 2 + 2 * H * Lc * D + 4 * cells
+    # estimation inputs read once (keys of every KV head, the chunk's queries);
+    # the reshaped scores are an intermediate the kernels never store
+    b_est_gemm = 2 * Hkv * D * (Lh + Lc) + 2 * H * Lc * D
     qb, kb = Lc // Bk, (Lh + Lc) // Bk
-    b_bsum = 4 * cells + 4 * H * qb * kb
+    b_bsum = 4 * H * qb * kb  # the block sums written
     f_att = 4 * H * D * Lc * (n_sel * Bk) + 4 * H * D * Lc * (Lc + 1) // 2
     b_att = 2 * 2 * Hkv * D * (n_sel * Bk + Lc) + 2 * 2 * H * Lc * D + 4 * H * Lc
     return dict(f_est=f_est, b_est=b_est_gemm, b_bsum=b_bsum, f_att=f_att, b_att=b_att,

@@ -108,10 +108,11 @@ typedef struct xattn_problem {
   int64_t lse_head_stride;        /* elements between heads of lse */
 } xattn_problem;
 
-/* Bytes of scratch the caller must provide to xattn_estimate / xattn_select
- * for this problem (0 on invalid problems).  The workspace holds the fp32
- * reshaped score matrix, per-tile and merged softmax statistics and the vote
- * counters; its contents between calls are unspecified. */
+/* Bytes of scratch the caller must provide to xattn_estimate, xattn_select and
+ * bsa_chunk_attention for this problem (0 on invalid problems).  The workspace
+ * holds the estimation's per-(reshaped row, KV block) partial sums and
+ * per-tile softmax statistics, the gathered keys, the vote counters and the
+ * attention's partial results; its contents between calls are unspecified. */
 size_t xattn_workspace_size(const xattn_problem *p);
 
 /* Number of fp32 elements of block_sums (and bytes of the optional mask):

@@ -64,11 +64,10 @@ def test_workspace_and_block_sum_sizes(lib):
     # one 4096-token chunk with 28672 history tokens (last chunk of the 32K case)
     p = _prob([4096], [28672])
     H, rq, ncol = 16, 4096 // 8, 32768 // 8
-    scores = H * rq * ncol * 4
+    bpart = H * rq * (ncol // 16) * 4    # one float per (reshaped row, KV block of Br = 16)
     tstat = H * rq * (ncol // 128) * 8
-    rstat = H * rq * 8
     al = lambda x: (x + 255) // 256 * 256
-    counts = al(al(al(scores) + tstat) + rstat)
+    counts = al(al(bpart) + tstat)
     kcat = al(counts + 512 * 4)          # gathered keys [Hkv, history + chunk, D] bf16
     part_o = al(kcat + 8 * 32768 * 128 * 2)  # attention partials: 160 CTAs x 2 slots x 256 rows
     part_lse = al(part_o + 160 * 2 * 256 * 128 * 4)

@@ -21,7 +21,6 @@ struct Plan {
   Geo geo;
   int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0, gat_ctas = 0;
   int64_t kcat_tokens = 0;
-  int64_t stat_rows = 0;
   int max_kb = 0;
   size_t bs_count = 0;
   WsLayout ws{};
@@ -58,7 +57,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   g.block_table = p->block_table;
 
   int64_t gemm = 0, bsum = 0, sel = 0, att = 0, gat = 0, kcat = 0;
-  size_t scores = 0, tstat = 0, rstat = 0, bs = 0;
+  size_t bpart = 0, tstat = 0, bs = 0;
   bool any_hist = false;
   for (int r = 0; r < B; ++r) {
     const int64_t q0 = p->cu_seqlens_q[r], q1 = p->cu_seqlens_q[r + 1];
@@ -82,9 +81,8 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     d.att0 = (int32_t)att;
     d.gat0 = (int32_t)gat;
     d.kcat0 = (int32_t)kcat;
-    d.score_off = (int64_t)scores;
+    d.bpart_off = (int64_t)bpart;
     d.tstat_off = (int64_t)tstat;
-    d.rstat_off = (int64_t)rstat;
     d.bs_off = (int64_t)bs;
     const int64_t rq = lq / S, ncol = (kh + lq) / S;
     const int64_t ntile = (ncol + kTileCols - 1) / kTileCols;
@@ -99,13 +97,12 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
       gemm += (int64_t)H * per_head;
       gat += (int64_t)Hkv * (kbh + qb);
       kcat += kh + lq;
-      bsum += (int64_t)H * qb * ((ncol + kBsumCols - 1) / kBsumCols);
+      bsum += (int64_t)H * qb;
       sel += (int64_t)Hkv * qb;
       att += (int64_t)H * ((lq + kAttnRows - 1) / kAttnRows);
     }
-    scores += (size_t)H * rq * ncol;
+    bpart += (size_t)H * rq * (ncol / (Bk / S));  // one float per (reshaped row, KV block)
     tstat += (size_t)H * rq * ntile;
-    rstat += (size_t)H * rq;
     bs += (size_t)H * qb * (kbh + qb);
     if (kbh + qb > pl.max_kb) pl.max_kb = (int)(kbh + qb);
   }
@@ -126,13 +123,11 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   pl.att_ctas = (int)att;
   pl.gat_ctas = (int)gat;
   pl.kcat_tokens = kcat;
-  pl.stat_rows = (int64_t)rstat;
   pl.bs_count = bs;
   WsLayout &w = pl.ws;
-  w.scores = 0;
-  w.tstat = align_up(w.scores + scores * sizeof(float));
-  w.rstat = align_up(w.tstat + tstat * sizeof(float2));
-  w.counts = align_up(w.rstat + rstat * sizeof(float2));
+  w.bpart = 0;
+  w.tstat = align_up(w.bpart + bpart * sizeof(float));
+  w.counts = align_up(w.tstat + tstat * sizeof(float2));
   w.kcat = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
                                    sizeof(int32_t));
   // attention partial results: two slots of kAttnRows rows per persistent CTA
@@ -240,18 +235,17 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
   if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
   if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   char *ws = static_cast<char *>(workspace);
-  float *scores = reinterpret_cast<float *>(ws + pl.ws.scores);
+  float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
   float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
-  float2 *rstat = reinterpret_cast<float2 *>(ws + pl.ws.rstat);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16 *kcat = reinterpret_cast<__nv_bfloat16 *>(ws + pl.ws.kcat);
   s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, pl.gat_ctas, pl.kcat_tokens,
                            static_cast<const __nv_bfloat16 *>(q),
                            static_cast<const __nv_bfloat16 *>(k_cur),
-                           static_cast<const __nv_bfloat16 *>(k_pool), kcat, scale, scores, tstat,
+                           static_cast<const __nv_bfloat16 *>(k_pool), kcat, scale, bpart, tstat,
                            st));
   if (s != XATTN_OK) return s;
-  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, pl.stat_rows, scores, tstat, rstat,
+  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, bpart, tstat,
                              block_sums, st));
 }
 

@@ -15,7 +15,6 @@ constexpr int kAttnRows = 256;  // query rows per attention work unit (two 128-r
 constexpr int kAttnMaxCtas = 160;  // persistent attention CTAs at most (one per SM)
 constexpr int kGemmRows = 256;  // reshaped rows per score-GEMM CTA (two 128-row MMA tiles)
 constexpr int kGemmCols = 256;  // reshaped columns per score-GEMM CTA
-constexpr int kBsumCols = 256;  // columns per block-sum CTA (one per thread)
 
 // Per-request geometry of one chunk call (host-computed, passed by value).
 struct ReqDesc {
@@ -29,9 +28,8 @@ struct ReqDesc {
   int32_t gat0;    // ... in the key-gather grid
   int32_t kcat0;   // first token of the request in the gathered key buffer
   int32_t pad_;
-  int64_t score_off;  // float offset of the request's [H, lq/S, (kh+lq)/S] scores
+  int64_t bpart_off;  // float offset of the request's [H, Qb, Kb, Br] block partial sums
   int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
-  int64_t rstat_off;  // float2 offset of its [H, lq/S] merged statistics
   int64_t bs_off;     // offset of its [H, Qb, Kb] block sums / mask
 };
 
@@ -71,16 +69,15 @@ __device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
 // Launch entry points implemented in the kernel translation units.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t scores, tstat, rstat, counts, kcat, part_o, part_lse, att_cnt, total;
+  size_t bpart, tstat, counts, kcat, part_o, part_lse, att_cnt, total;
 };
 
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
                               const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                               const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
-                              float *scores, float2 *tstat, cudaStream_t st);
-cudaError_t launch_block_sum(const Geo &g, int nctas, int64_t nrows, const float *scores,
-                             const float2 *tstat, float2 *rstat, float *block_sums,
-                             cudaStream_t st);
+                              float *bpart, float2 *tstat, cudaStream_t st);
+cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
+                             float *block_sums, cudaStream_t st);
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
                           double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st);
 cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx,

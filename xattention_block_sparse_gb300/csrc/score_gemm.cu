@@ -19,12 +19,20 @@
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
 //                  next tile while the epilogue drains TMEM)
 //     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
-//     warps 4..11  epilogue, one thread per row: fp32 scores to the workspace,
-//                  laid out [H][Qb][ncol][Br] (a query block's rows contiguous
-//                  per column, so stores coalesce), and per-(row, 128-column
-//                  tile) (max, sum exp) over the visible cells.  Tiles right
-//                  of the causal diagonal are never scheduled; the block-sum
-//                  merge reads only tiles up to each row's diagonal.
+//     warps 4..11  epilogue, one thread per row, per 128-column statistics
+//                  tile: the tile max m_t over the visible cells, and for each
+//                  Br-column KV block of the tile the partial sum
+//                  sum exp(s - m_t) over its visible cells; their total is the
+//                  tile's sum l_t.  The block partials ([H][Qb][Kb][Br]: a
+//                  query block's rows contiguous per KV block, so a warp's
+//                  store of one block is two or four full segments) and
+//                  (m_t, l_t) go to the workspace; the fp32 score matrix itself
+//                  is never written.  block_sum_kernel (estimate.cu) merges
+//                  the tile statistics per row and rescales the partials:
+//                  sum over the block of exp(s - m)/l = sum_t-part * e^(m_t - m)/l,
+//                  exactly the two-pass normalise-then-sum of the pages, with
+//                  pass 2 folded into pass 1 per tile.  Tiles right of the
+//                  causal diagonal are never scheduled.
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -91,9 +99,11 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
   return tl;
 }
 
+template <int BR>
 __global__ void __launch_bounds__(THREADS, 1)
     score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int ntiles,
-                      float scale, float *__restrict__ scores, float2 *__restrict__ tstat) {
+                      float scale, float *__restrict__ bpart, float2 *__restrict__ tstat) {
+  constexpr int NB = kTileCols / BR;  // KV blocks per statistics tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -208,13 +218,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       if (x == 0 || two_m) {
         const bool row_ok = a < rq;
-        // scores are stored [H][Qb][ncol][Br]: the Br rows of a query block are
-        // contiguous per column, so a warp's store of one column is 32 rows in
-        // 32/Br full segments
-        const int br = g.Bk / S;
-        float *sbase = scores + R.score_off +
-                       ((int64_t)(tl.h * (rq / br) + (row_ok ? a : 0) / br) * ncol) * br +
-                       (row_ok ? a : 0) % br;
+        const int Qb = rq / BR, Kb = ncol / BR;
+        // block partials are stored [H][Qb][Kb][Br]
+        float *pbase = bpart + R.bpart_off +
+                       ((int64_t)(tl.h * Qb + (row_ok ? a : 0) / BR) * Kb) * BR +
+                       (row_ok ? a : 0) % BR;
 #pragma unroll 1
         for (int j = 0; j < COLS / kTileCols; ++j) {
           const int c0 = tl.n0 + j * kTileCols;  // first column of this statistics tile
@@ -233,23 +241,30 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!row_ok || c0 >= ncol || c0 > ch + a) continue;
           // visible columns of the row in this tile: [c0, c0 + nv)
           const int nv = min(min(kTileCols, ncol - c0), ch + a + 1 - c0);
-          const int nst = min(kTileCols, ncol - c0);  // columns that exist
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int c = 0; c < kTileCols; ++c) {
             const float f = __uint_as_float(v[c]) * scale;
-            if (c < nst) sbase[(int64_t)(c0 + c) * br] = f;
             v[c] = __float_as_uint(c < nv ? f : -INFINITY);
             mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
           }
           const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float ml2 = m * 1.4426950408889634f;
-          float sm[4] = {0.f, 0.f, 0.f, 0.f};
+          float pb[NB];
+#pragma unroll
+          for (int q = 0; q < NB; ++q) pb[q] = 0.f;
 #pragma unroll
           for (int c = 0; c < kTileCols; ++c)
-            sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), 1.4426950408889634f, -ml2));
+            pb[c / BR] += ex2(fmaf(__uint_as_float(v[c]), 1.4426950408889634f, -ml2));
+          float l = 0.f;
+#pragma unroll
+          for (int q = 0; q < NB; ++q) {
+            l += pb[q];
+            const int kb = c0 / BR + q;
+            if (kb < Kb) pbase[(int64_t)kb * BR] = pb[q];
+          }
           tstat[R.tstat_off + ((int64_t)tl.h * rq + a) * ntile + c0 / kTileCols] =
-              make_float2(m, (sm[0] + sm[1]) + (sm[2] + sm[3]));
+              make_float2(m, l);
         }
       } else {
         tc_fence_before();
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(GTHR) gather_k_kernel(const __grid_constant__ 
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
                               const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                               const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
-                              float *scores, float2 *tstat, cudaStream_t st) {
+                              float *bpart, float2 *tstat, cudaStream_t st) {
   if (gather_ctas > 0) {
     gather_k_kernel<<<gather_ctas, GTHR, 0, st>>>(g, kcur, kpool, kcat, kcat_tokens);
     cudaError_t e = cudaGetLastError();
@@ -350,12 +365,20 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(score_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-  if (e != cudaSuccess) return e;
   const int grid = ntiles < sms ? ntiles : sms;
-  score_gemm_kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(g, mp, ntiles, scale, scores, tstat);
-  return cudaGetLastError();
+  auto run = [&](auto kernel) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(g, mp, ntiles, scale, bpart, tstat);
+    return cudaGetLastError();
+  };
+  switch (g.Bk / S) {  // Br: reshaped columns per KV block
+    case 8: return run(score_gemm_kernel<8>);
+    case 16: return run(score_gemm_kernel<16>);
+    case 32: return run(score_gemm_kernel<32>);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace xattn
