@@ -149,15 +149,20 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
  * blocks are visited by (q_j descending, j ascending) and block j is kept iff
  * the integer mass visited before it is < R (threshold >= 1 keeps every q_j > 0).
  * Then, over history blocks only: a KV-head group keeps a block if any of its
- * query heads does; a block is selected when 2*votes > Hkv * Qb_r (votes over
- * KV heads x query blocks); history block 0 and block Kb_h-1 are always added.
+ * query heads does; a block is selected when
+ *   votes * vote_den > vote_num * (Hkv * Qb_r)     (votes over KV heads x query blocks)
+ * -- (1, 2) is the pages' strict majority -- and, if force_sink_last != 0,
+ * history block 0 and block Kb_h-1 are always added.
  *   threshold   > 0 (0.9 and 0.95 are the pages' settings)
+ *   vote_num, vote_den   0 <= vote_num <= vote_den, vote_den > 0 (XATTN_EINVAL otherwise)
+ *   force_sink_last      0 or 1
  *   mask        DEVICE u8 [xattn_block_sums_count(p)] or NULL: per-head keep flags
  *   sel_idx     DEVICE int32 [B, bt_stride]: ascending logical history block ids
  *   sel_page    DEVICE int32 [B, bt_stride]: block_table[r][sel_idx]
  *   n_sel       DEVICE int32 [B]: number of valid entries per request
  * Entries past n_sel[r] are left untouched. */
 xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,
+                          int32_t vote_num, int32_t vote_den, int32_t force_sink_last,
                           void *workspace, size_t workspace_bytes, uint8_t *mask,
                           int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
                           xattn_stream_t stream);
@@ -185,7 +190,8 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
  *    threads) race on it and must be ordered by the caller.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
-                                  double threshold, uint8_t *mask, int32_t *sel_idx,
+                                  double threshold, int32_t vote_num, int32_t vote_den,
+                                  int32_t force_sink_last, uint8_t *mask, int32_t *sel_idx,
                                   int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream);
 
 /* Sparse chunk attention (BSA policy page, compute_chunked_prefill).  For each
@@ -225,6 +231,11 @@ xattn_status lse_merge(const float *o1, const float *lse1, const float *o2,
  * device after synchronising `stream`.  *code is XATTN_OK or the first fault
  * status recorded by a kernel.  Diagnostic call: it blocks the host. */
 xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t clear);
+
+/* xattn_device_error(stream, code, 1) under the name of the boundary table:
+ * the first fault status recorded since the last read, then reset.  Blocks
+ * the host (diagnostics and tests). */
+xattn_status xattn_last_device_error(xattn_stream_t stream, int32_t *host_code);
 
 /* Static description of a status code. */
 const char *xattn_status_string(xattn_status s);

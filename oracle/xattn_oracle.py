@@ -255,14 +255,16 @@ def threshold_select(v32: np.ndarray, tau: float) -> np.ndarray:
     return out
 
 
-def gqa_vote(mask: np.ndarray, num_kv_heads: int, kb_hist: int, force: bool = True):
+def gqa_vote(mask: np.ndarray, num_kv_heads: int, kb_hist: int, force: bool = True,
+             vote=(1, 2)):
     """[BSA] Step 4 GQA-aware aggregation + majority voting on a [H, Qb, Kb]
     mask.  Any query head of a KV-head group selects for the group (with one
     head per group the mask is used as it is); a history block survives when
-    it is voted for by more than half of the (KV head, query block) pairs;
-    then the first (sink) and last history block are always added.  Only the
-    history columns j < kb_hist take part: the current chunk is always
-    attended causally.  Returns ascending logical block ids."""
+    it is voted for by more than vote = num/den of the (KV head, query block)
+    pairs -- the pages' vote_ratio > 0.5 is (1, 2); then, with `force`, the
+    first (sink) and last history block are always added.  Only the history
+    columns j < kb_hist take part: the current chunk is always attended
+    causally.  Returns ascending logical block ids."""
     H, qb, _ = mask.shape
     G = H // num_kv_heads
     if kb_hist == 0:
@@ -270,7 +272,8 @@ def gqa_vote(mask: np.ndarray, num_kv_heads: int, kb_hist: int, force: bool = Tr
     m = mask[:, :, :kb_hist].reshape(num_kv_heads, G, qb, kb_hist)
     per_kv = m.any(axis=1)
     count = per_kv.sum(axis=(0, 1))
-    keep = 2 * count > num_kv_heads * qb          # vote_ratio > 0.5, in integers
+    num, den = vote
+    keep = count * den > num * num_kv_heads * qb   # count / total > num / den, in integers
     if force:
         keep[0] = True
         keep[kb_hist - 1] = True
@@ -362,10 +365,10 @@ def estimate_request(q, k_cur, pool_k, bt_row, kh_len, H, Hkv, stride, block, sc
     return np.stack(out)
 
 
-def select_request(bs32, tau, Hkv, kb_hist, bt_row):
+def select_request(bs32, tau, Hkv, kb_hist, bt_row, vote=(1, 2), force=True):
     """Threshold selection + vote of one request: (mask, sel_idx, sel_page)."""
     mask = threshold_select(bs32, tau)
-    sel = gqa_vote(mask, Hkv, kb_hist)
+    sel = gqa_vote(mask, Hkv, kb_hist, force=force, vote=vote)
     pages = np.asarray([int(bt_row[j]) for j in sel], dtype=np.int64)
     return mask, sel, pages
 

@@ -41,10 +41,11 @@ def check_block_sums(gpu, ref, br, what=""):
     return float((err / np.maximum(np.abs(ref), 1e-30)).max())
 
 
-def check_selection(bs32, gpu_mask, gpu_sel, gpu_pages, n_sel, tau, Hkv, kbh, bt_row, what=""):
+def check_selection(bs32, gpu_mask, gpu_sel, gpu_pages, n_sel, tau, Hkv, kbh, bt_row, what="",
+                    vote=(1, 2), force=True):
     """The oracle's selection applied to the GPU's own block sums must equal the
     GPU's mask, selected block ids and pages bit for bit."""
-    mask, sel, pages = O.select_request(bs32, tau, Hkv, kbh, bt_row)
+    mask, sel, pages = O.select_request(bs32, tau, Hkv, kbh, bt_row, vote=vote, force=force)
     if gpu_mask is not None:
         diff = mask != gpu_mask.astype(bool)
         assert not diff.any(), f"{what}: mask differs in {diff.sum()} entries"

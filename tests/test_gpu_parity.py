@@ -184,8 +184,9 @@ def test_unallocated_page_is_reported_not_trapped():
     X.xattn_device_error(clear=True)  # clear anything an earlier test left
     RN.prefill_chunk(prob, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], case.KP, case.VP, 0.9,
                      bufs, O_[:, t0:], LSE[:, t0:])
-    code = X.xattn_device_error(clear=True)
+    code = X.xattn_device_error(clear=False)
     assert code == -3
+    assert X.xattn_last_device_error() == -3  # read and reset
     assert X.xattn_device_error() == 0
     assert torch.isfinite(LSE[:, t0:]).all()
 
@@ -231,3 +232,29 @@ def test_stream_ordering_side_stream_copy():
     assert np.array_equal(ref["resident"][0], ref["side"][0])
     assert np.array_equal(ref["resident"][1], ref["side"][1])
     assert np.array_equal(ref["resident"][2], ref["side"][2])
+
+
+@pytest.mark.parametrize("vote,force", [((0, 1), False), ((1, 4), True), ((3, 4), False),
+                                        ((1, 1), True)])
+def test_selection_vote_parameters(vote, force):
+    """Vote ratio num/den and sink/last forcing of xattn_select, bit-exact against
+    the oracle's selection on the GPU's own block sums (a partial threshold, so
+    the votes differ between blocks)."""
+    case = SequenceCase("q06b_4k")
+    cfg = case.cfg
+    c, tau = 3, 0.6
+    p, b = case.seq.problems[c], case.seq.bufs
+    t0 = c * case.chunk
+    X.xattn_estimate(p, case.Q[:, t0:], case.K[:, t0:], case.KP,
+                     RN.estimation_scale(cfg.D, cfg.stride), b.workspace, b.block_sums)
+    X.xattn_select(p, b.block_sums, tau, b.workspace, b.mask, b.sel_idx, b.sel_page, b.n_sel,
+                   vote=vote, force_sink_last=force)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    n = X.xattn_block_sums_count(p)
+    kbh, qb_n = t0 // cfg.block, case.chunk // cfg.block
+    bs32 = b.block_sums[:n].cpu().numpy().reshape(cfg.H, qb_n, kbh + qb_n)
+    mk = b.mask[:n].cpu().numpy().reshape(bs32.shape)
+    check_selection(bs32, mk, b.sel_idx[0].cpu().numpy(), b.sel_page[0].cpu().numpy(),
+                    int(b.n_sel[0].item()), tau, cfg.Hkv, kbh, case.wl.block_table[0],
+                    f"vote {vote} force {force}", vote=vote, force=force)

@@ -117,9 +117,15 @@ def test_entry_point_argument_errors(lib):
                               None) == -1
     assert lib.xattn_estimate(p.ref(), fake, fake, fake, 0.1, fake, 16, fake, None) == -6
     for tau in (0.0, -1.0, float("nan"), float("inf")):
-        assert lib.xattn_select(p.ref(), fake, tau, fake, 1 << 40, None, fake, fake, fake,
+        assert lib.xattn_select(p.ref(), fake, tau, 1, 2, 1, fake, 1 << 40, None, fake, fake, fake,
                                 None) == -1
-    assert lib.xattn_select(p.ref(), fake, 0.9, fake, 16, None, fake, fake, fake, None) == -6
+    assert lib.xattn_select(p.ref(), fake, 0.9, 1, 2, 1, fake, 16, None, fake, fake, fake,
+                            None) == -6
+    for num, den, force in ((1, 0, 1), (-1, 2, 1), (3, 2, 1), (1, 2, 2)):  # bad vote / force
+        assert lib.xattn_select(p.ref(), fake, 0.9, num, den, force, fake, 1 << 40, None, fake,
+                                fake, fake, None) == -1
+        assert lib.xattn_select_noalloc(p.ref(), fake, 0.9, num, den, force, None, fake, fake,
+                                        fake, None) == -1
     assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,
                                    1 << 40, odd, fake, None) == -2
     assert lib.bsa_chunk_attention(p.ref(), fake, fake, fake, fake, fake, fake, fake, 0.1, fake,

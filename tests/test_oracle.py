@@ -318,6 +318,12 @@ def test_vote_hand_cases():
     sel = O.gqa_vote(m, 2, 4)
     assert sel.tolist() == [0, 1, 3]          # 0 and 3 forced (sink, last)
     assert O.gqa_vote(m, 2, 4, force=False).tolist() == [1]
+    # other vote ratios num/den over the same counts (block 1: 3 of 4, block 2: 2 of 4)
+    assert O.gqa_vote(m, 2, 4, force=False, vote=(0, 1)).tolist() == [1, 2]  # any vote
+    assert O.gqa_vote(m, 2, 4, force=False, vote=(1, 4)).tolist() == [1, 2]  # > 1 of 4
+    assert O.gqa_vote(m, 2, 4, force=False, vote=(3, 4)).tolist() == []      # > 3 of 4
+    assert O.gqa_vote(m, 2, 4, force=False, vote=(1, 1)).tolist() == []
+    assert O.gqa_vote(m, 2, 4, vote=(1, 1)).tolist() == [0, 3]                # forced only
     # G = 1: the mask votes as it is
     m1 = np.zeros((2, 3, 6), dtype=bool)
     m1[:, :2, 2] = True                        # 4 of 6 votes

@@ -41,7 +41,7 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     W = X.XATTN_NOALLOC_MAX_COUNTERS // 2 + 1
     p = _fake_problem([128, 128], [128, 128], W)
     fake = ctypes.c_void_p(0x10000)
-    st = lib.xattn_select_noalloc(p.ref(), fake, 0.9, None, fake, fake, fake, None)
+    st = lib.xattn_select_noalloc(p.ref(), fake, 0.9, 1, 2, 1, None, fake, fake, fake, None)
     assert st == -6  # XATTN_EWORKSPACE
 
 
@@ -85,8 +85,8 @@ def test_noalloc_select_matches_workspace_select_on_consecutive_calls():
         idx2 = torch.full_like(bufs.sel_idx, -9)
         page2 = torch.full_like(bufs.sel_page, -9)
         nsel2 = torch.full_like(bufs.n_sel, -9)
-        st = lib.xattn_select_noalloc(p.ref(), ptr(bufs.block_sums), ctypes.c_double(tau),
-                                      ptr(mask2), ptr(idx2), ptr(page2), ptr(nsel2), stream)
+        st = lib.xattn_select_noalloc(p.ref(), ptr(bufs.block_sums), ctypes.c_double(tau), 1, 2,
+                                      1, ptr(mask2), ptr(idx2), ptr(page2), ptr(nsel2), stream)
         assert st == 0, X.STATUS.get(st, st)
         torch.cuda.synchronize()
         k = int(nsel2[0].item())

@@ -141,6 +141,11 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
+// Vote ratio num/den in [0, 1]; force flag 0 or 1.
+inline bool vote_ok(int32_t num, int32_t den, int32_t force) {
+  return den > 0 && num >= 0 && num <= den && (force == 0 || force == 1);
+}
+
 // Device address of the error word for the current device (cached per device).
 std::atomic<int32_t *> g_err_addr[64];
 
@@ -250,6 +255,7 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
 }
 
 xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,
+                          int32_t vote_num, int32_t vote_den, int32_t force_sink_last,
                           void *workspace, size_t workspace_bytes, uint8_t *mask,
                           int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
                           xattn_stream_t stream) {
@@ -258,6 +264,7 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
   if (s != XATTN_OK) return s;
   if (!block_sums || !workspace || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
   if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
+  if (!vote_ok(vote_num, vote_den, force_sink_last)) return XATTN_EINVAL;
   if (p->bt_stride < 1) return XATTN_EINVAL;
   if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_sums) & 3)) return XATTN_EALIGN;
   if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
@@ -268,17 +275,20 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
   if (s != XATTN_OK) return s;
   s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
   if (s != XATTN_OK) return s;
-  return cu(launch_vote(pl.geo, counts, sel_idx, sel_page, n_sel, st));
+  return cu(launch_vote(pl.geo, counts, vote_num, vote_den, force_sink_last, sel_idx, sel_page,
+                        n_sel, st));
 }
 
 xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
-                                  double threshold, uint8_t *mask, int32_t *sel_idx,
+                                  double threshold, int32_t vote_num, int32_t vote_den,
+                                  int32_t force_sink_last, uint8_t *mask, int32_t *sel_idx,
                                   int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream) {
   Plan pl;
   xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
   if (!block_sums || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
   if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
+  if (!vote_ok(vote_num, vote_den, force_sink_last)) return XATTN_EINVAL;
   if (p->bt_stride < 1) return XATTN_EINVAL;
   if (reinterpret_cast<uintptr_t>(block_sums) & 3) return XATTN_EALIGN;
   const size_t n_counters = (size_t)pl.geo.B * (size_t)p->bt_stride;
@@ -292,7 +302,8 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
   if (s != XATTN_OK) return s;
   s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
   if (s != XATTN_OK) return s;
-  return cu(launch_vote(pl.geo, counts, sel_idx, sel_page, n_sel, st));
+  return cu(launch_vote(pl.geo, counts, vote_num, vote_den, force_sink_last, sel_idx, sel_page,
+                        n_sel, st));
 }
 
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
@@ -350,6 +361,10 @@ xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t cl
   }
   *code = v;
   return XATTN_OK;
+}
+
+xattn_status xattn_last_device_error(xattn_stream_t stream, int32_t *host_code) {
+  return xattn_device_error(stream, host_code, 1);
 }
 
 const char *xattn_status_string(xattn_status s) {

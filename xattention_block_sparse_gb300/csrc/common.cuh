@@ -80,8 +80,9 @@ cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const 
                              float *block_sums, cudaStream_t st);
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
                           double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st);
-cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx,
-                        int32_t *sel_page, int32_t *n_sel, cudaStream_t st);
+cudaError_t launch_vote(const Geo &g, const int32_t *counts, int vote_num, int vote_den,
+                        int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
+                        int32_t *n_sel, cudaStream_t st);
 cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
                              const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,

@@ -7,8 +7,9 @@
 //                  bitonic sort of (q_j desc, j asc), exclusive prefix of the
 //                  sorted masses, keep iff prefix < fl64(tau * T).  The group's
 //                  "any" over its heads then votes once per history block.
-//   vote_kernel    one CTA per request: majority test 2*votes > Hkv*Qb, sink and
-//                  last history block forced, ascending compaction, page lookup.
+//   vote_kernel    one CTA per request: vote test votes*den > num*Hkv*Qb ((1, 2):
+//                  strict majority), sink and last history block forced (when
+//                  asked), ascending compaction, page lookup.
 //
 // Every step is integer or exactly rounded, so the result does not depend on
 // the order in which threads add or compare.
@@ -135,6 +136,7 @@ constexpr int VTHR = 512;
 
 __global__ void __launch_bounds__(VTHR) vote_kernel(const __grid_constant__ Geo g,
                                                     const int32_t *__restrict__ counts,
+                                                    int vote_num, int vote_den, int force,
                                                     int32_t *__restrict__ sel_idx,
                                                     int32_t *__restrict__ sel_page,
                                                     int32_t *__restrict__ n_sel) {
@@ -142,12 +144,15 @@ __global__ void __launch_bounds__(VTHR) vote_kernel(const __grid_constant__ Geo 
   const int r = blockIdx.x;
   const ReqDesc &R = g.req[r];
   const int kbh = R.kh / g.Bk, Qb = R.lq / g.Bk;
-  const int votes_total = g.Hkv * Qb;
+  const int64_t votes_total = (int64_t)g.Hkv * Qb;
   const int tid = threadIdx.x;
   const int per = (kbh + VTHR - 1) / VTHR;
   const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
   const int32_t *cnt = counts + (int64_t)r * g.bt_stride;
-  auto keep = [&](int j) { return 2 * cnt[j] > votes_total || j == 0 || j == kbh - 1; };
+  auto keep = [&](int j) {
+    return (int64_t)cnt[j] * vote_den > (int64_t)vote_num * votes_total ||
+           (force && (j == 0 || j == kbh - 1));
+  };
   unsigned long long mine = 0;
   for (int j = beg; j < end; ++j) mine += keep(j) ? 1 : 0;
   unsigned long long total;
@@ -185,9 +190,11 @@ cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *bloc
   return cudaGetLastError();
 }
 
-cudaError_t launch_vote(const Geo &g, const int32_t *counts, int32_t *sel_idx, int32_t *sel_page,
-                        int32_t *n_sel, cudaStream_t st) {
-  vote_kernel<<<g.B, VTHR, 0, st>>>(g, counts, sel_idx, sel_page, n_sel);
+cudaError_t launch_vote(const Geo &g, const int32_t *counts, int vote_num, int vote_den,
+                        int force_sink_last, int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
+                        cudaStream_t st) {
+  vote_kernel<<<g.B, VTHR, 0, st>>>(g, counts, vote_num, vote_den, force_sink_last, sel_idx,
+                                    sel_page, n_sel);
   return cudaGetLastError();
 }
 

@@ -28,7 +28,7 @@ STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAG
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
             "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
             "lse_merge",
-            "xattn_device_error", "xattn_status_string"]
+            "xattn_device_error", "xattn_last_device_error", "xattn_status_string"]
 
 
 class XattnError(RuntimeError):
@@ -77,12 +77,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "xattn_block_sums_count": (sz, [P]),
         "xattn_block_sums_offset": (sz, [P, i32]),
         "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
-        "xattn_select": (ctypes.c_int, [P, vp, f64, vp, sz, vp, vp, vp, vp, vp]),
-        "xattn_select_noalloc": (ctypes.c_int, [P, vp, f64, vp, vp, vp, vp, vp]),
+        "xattn_select": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp]),
+        "xattn_select_noalloc": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, vp, vp, vp, vp]),
         "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, sz, vp, vp,
                                                 vp]),
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
+        "xattn_last_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "xattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -186,8 +187,11 @@ def xattn_estimate(problem, q, k_cur, k_pool, scale, workspace, block_sums, stre
 
 
 def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_page, n_sel,
-                 stream=None):
+                 stream=None, vote=(1, 2), force_sink_last=True):
+    """vote = (num, den): a history block is selected when its votes exceed
+    num/den of the (KV head, query block) pairs; (1, 2) is the strict majority."""
     st = load_library().xattn_select(problem.ref(), _ptr(block_sums), float(threshold),
+                                     int(vote[0]), int(vote[1]), int(bool(force_sink_last)),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _ptr(mask), _ptr(sel_idx), _ptr(sel_page), _ptr(n_sel),
                                      _stream(stream))
@@ -195,11 +199,13 @@ def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_p
 
 
 def xattn_select_noalloc(problem, block_sums, threshold, mask, sel_idx, sel_page, n_sel,
-                         stream=None):
+                         stream=None, vote=(1, 2), force_sink_last=True):
     """xattn_select without a workspace, for callers that cannot allocate device
     memory on the prefill path; its vote counters live in a fixed array inside
     the library (one per GPU), so calls that overlap on the GPU race."""
     st = load_library().xattn_select_noalloc(problem.ref(), _ptr(block_sums), float(threshold),
+                                             int(vote[0]), int(vote[1]),
+                                             int(bool(force_sink_last)),
                                              _ptr(mask), _ptr(sel_idx), _ptr(sel_page),
                                              _ptr(n_sel), _stream(stream))
     _check(st, "xattn_select_noalloc")
@@ -228,6 +234,13 @@ def xattn_device_error(stream=None, clear: bool = True) -> int:
     code = ctypes.c_int32(0)
     st = load_library().xattn_device_error(_stream(stream), ctypes.byref(code), 1 if clear else 0)
     _check(st, "xattn_device_error")
+    return int(code.value)
+
+
+def xattn_last_device_error(stream=None) -> int:
+    code = ctypes.c_int32(0)
+    st = load_library().xattn_last_device_error(_stream(stream), ctypes.byref(code))
+    _check(st, "xattn_last_device_error")
     return int(code.value)
 
 
