@@ -4,8 +4,12 @@
 //
 //   select_kernel  one CTA per (request, KV head, query block).  For each query
 //                  head of the group: integer masses q_j = rne(bs_j * 2^32),
-//                  bitonic sort of (q_j desc, j asc), exclusive prefix of the
-//                  sorted masses, keep iff prefix < fl64(tau * T).  The group's
+//                  visited in (q_j desc, j asc) order; block j is kept iff the
+//                  mass visited before it, prefix_j, is < fl64(tau * T).  Rows
+//                  of up to kRankMax blocks get prefix_j directly as the sum of
+//                  the masses whose key (q, -index) exceeds j's -- all the
+//                  group's rows at once, no barrier in the loop; longer rows
+//                  go through a bitonic sort and a prefix scan.  The group's
 //                  "any" over its heads then votes once per history block.
 //   vote_kernel    one CTA per request: vote test votes*den > num*Hkv*Qb ((1, 2):
 //                  strict majority), sink and last history block forced (when
@@ -20,6 +24,9 @@ namespace {
 
 constexpr int STHR = 512;
 constexpr int SWARPS = STHR / 32;
+constexpr int kRankMax = 512;    // longest row ranked directly (Kb^2 compare-adds per row)
+constexpr int kRankKeys = 4096;  // keys of all G rows held at once
+constexpr int kRankMaxG = 64;    // largest GQA group taking the direct path
 
 __device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long v, int lane) {
 #pragma unroll
@@ -53,8 +60,8 @@ __device__ unsigned long long block_excl_scan(unsigned long long v, unsigned lon
 __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Geo g,
                                                       const float *__restrict__ bs, double tau,
                                                       uint8_t *__restrict__ mask,
-                                                      int32_t *__restrict__ counts) {
-  extern __shared__ unsigned long long keys[];  // [npad] then any-flags
+                                                      int32_t *__restrict__ counts, int nkeys) {
+  extern __shared__ __align__(16) uint8_t sel_smem[];  // any-flags [npad], then keys
   __shared__ unsigned long long wbuf[SWARPS + 1];
   const int cta = blockIdx.x;
   const int r = find_req(g, cta, [](const ReqDesc &d) { return d.sel0; });
@@ -65,11 +72,62 @@ __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Ge
   const int G = g.H / g.Hkv;
   int npad = 1;
   while (npad < Kb) npad <<= 1;
-  uint8_t *anyf = reinterpret_cast<uint8_t *>(keys + npad);
+  uint8_t *anyf = sel_smem;
+  unsigned long long *keys = reinterpret_cast<unsigned long long *>(sel_smem + ((npad + 15) & ~15));
   const int tid = threadIdx.x;
 
   for (int j = tid; j < kbh; j += STHR) anyf[j] = 0;
 
+  // (the keys of G rows must fit the shared memory the launch sized: nkeys)
+  if (Kb <= kRankMax && G * Kb <= kRankKeys && G <= kRankMaxG && G * Kb <= nkeys) {
+    // direct ranks: keys of every head of the group in shared memory
+    unsigned long long *gk = keys;  // [G][Kb]
+    __shared__ unsigned long long tot[kRankMaxG];
+    for (int idx = tid; idx < G * Kb; idx += STHR) {
+      const int gi = idx / Kb, j = idx - gi * Kb;
+      const float v = bs[R.bs_off + ((int64_t)(kvh * G + gi) * Qb + qb) * Kb + j];
+      // v * 2^32 is exact in fp32; the conversion rounds half to even
+      const unsigned long long qv = v > 0.f ? __float2ull_rn(v * 4294967296.0f) : 0ull;
+      gk[idx] = (qv << 16) | (unsigned long long)(0xFFFF - j);
+    }
+    __syncthreads();
+    // row totals T, one warp per row
+    for (int gi = tid >> 5; gi < G; gi += SWARPS) {
+      unsigned long long t = 0ull;
+      for (int j = tid & 31; j < Kb; j += 32) t += gk[gi * Kb + j] >> 16;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if ((tid & 31) == 0) tot[gi] = t;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * Kb; idx += STHR) {
+      const int gi = idx / Kb, j = idx - gi * Kb;
+      const unsigned long long *row = gk + gi * Kb;
+      const unsigned long long kj = row[j];
+      // four independent partial sums over the row (shared-memory broadcasts)
+      unsigned long long p4[4] = {0ull, 0ull, 0ull, 0ull};
+      int i = 0;
+      for (; i + 4 <= Kb; i += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const unsigned long long ki = row[i + u];
+          p4[u] += ki > kj ? (ki >> 16) : 0ull;
+        }
+      }
+      for (; i < Kb; ++i) {
+        const unsigned long long ki = row[i];
+        p4[0] += ki > kj ? (ki >> 16) : 0ull;
+      }
+      const unsigned long long pre = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+      const unsigned long long qv = kj >> 16;
+      const bool keep =
+          tau >= 1.0 ? (qv > 0ull) : ((double)pre < __dmul_rn(tau, (double)tot[gi]));
+      const int64_t row_off = R.bs_off + ((int64_t)(kvh * G + gi) * Qb + qb) * Kb;
+      if (mask) mask[row_off + j] = keep ? 1 : 0;
+      if (keep && j < kbh) anyf[j] = 1;
+    }
+    __syncthreads();
+  } else
   for (int gi = 0; gi < G; ++gi) {
     const int h = kvh * G + gi;
     const int64_t row_off = R.bs_off + ((int64_t)h * Qb + qb) * Kb;
@@ -180,13 +238,18 @@ cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *bloc
   if (nctas == 0) return cudaSuccess;
   int npad = 1;
   while (npad < max_kb) npad <<= 1;
-  const size_t smem = (size_t)npad * sizeof(unsigned long long) + (size_t)npad;
+  const int G = g.H / g.Hkv;
+  // keys: the sort's npad, or the direct ranks' G rows (see select_kernel)
+  size_t nkeys = (size_t)npad;
+  if (max_kb <= kRankMax && G * max_kb <= kRankKeys && G <= kRankMaxG && (size_t)G * max_kb > nkeys)
+    nkeys = (size_t)G * max_kb;
+  const size_t smem = (((size_t)npad + 15) & ~(size_t)15) + nkeys * sizeof(unsigned long long);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts);
+  select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts, (int)nkeys);
   return cudaGetLastError();
 }
 
