@@ -19,8 +19,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   Geo geo;
-  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0, gat_ctas = 0;
-  int64_t kcat_tokens = 0;
+  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0;
   int max_kb = 0;
   size_t bs_count = 0;
   WsLayout ws{};
@@ -56,7 +55,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   g.lse_hs = p->lse_head_stride;
   g.block_table = p->block_table;
 
-  int64_t gemm = 0, bsum = 0, sel = 0, att = 0, gat = 0, kcat = 0;
+  int64_t gemm = 0, bsum = 0, sel = 0, att = 0;
   size_t bpart = 0, tstat = 0, bs = 0;
   bool any_hist = false;
   for (int r = 0; r < B; ++r) {
@@ -79,8 +78,6 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     d.bsum0 = (int32_t)bsum;
     d.sel0 = (int32_t)sel;
     d.att0 = (int32_t)att;
-    d.gat0 = (int32_t)gat;
-    d.kcat0 = (int32_t)kcat;
     d.bpart_off = (int64_t)bpart;
     d.tstat_off = (int64_t)tstat;
     d.bs_off = (int64_t)bs;
@@ -95,8 +92,6 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
         per_head += (vis + kGemmCols - 1) / kGemmCols;
       }
       gemm += (int64_t)H * per_head;
-      gat += (int64_t)Hkv * (kbh + qb);
-      kcat += kh + lq;
       bsum += (int64_t)H * qb;
       sel += (int64_t)Hkv * qb;
       att += (int64_t)H * ((lq + kAttnRows - 1) / kAttnRows);
@@ -106,8 +101,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     bs += (size_t)H * qb * (kbh + qb);
     if (kbh + qb > pl.max_kb) pl.max_kb = (int)(kbh + qb);
   }
-  if (gemm > INT32_MAX || bsum > INT32_MAX || att > INT32_MAX || gat > INT32_MAX ||
-      kcat > INT32_MAX)
+  if (gemm > INT32_MAX || bsum > INT32_MAX || att > INT32_MAX)
     return XATTN_EUNSUPPORTED;
   if (any_hist && (!p->block_table || p->num_pages < 1)) return XATTN_EINVAL;
   if (p->bt_stride < 0) return XATTN_EINVAL;
@@ -121,18 +115,15 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   pl.bsum_ctas = (int)bsum;
   pl.sel_ctas = (int)sel;
   pl.att_ctas = (int)att;
-  pl.gat_ctas = (int)gat;
-  pl.kcat_tokens = kcat;
   pl.bs_count = bs;
   WsLayout &w = pl.ws;
   w.bpart = 0;
   w.tstat = align_up(w.bpart + bpart * sizeof(float));
   w.counts = align_up(w.tstat + tstat * sizeof(float2));
-  w.kcat = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
-                                   sizeof(int32_t));
   // attention partial results: two slots of kAttnRows rows per persistent CTA
   const size_t part_rows = (size_t)kAttnMaxCtas * 2 * kAttnRows;
-  w.part_o = align_up(w.kcat + (size_t)Hkv * (size_t)kcat * D * 2);
+  w.part_o = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
+                                     sizeof(int32_t));
   w.part_lse = align_up(w.part_o + part_rows * D * sizeof(float));
   w.att_cnt = align_up(w.part_lse + part_rows * sizeof(float));
   w.total = align_up(w.att_cnt + (size_t)att * 2 * sizeof(int32_t));  // two per attention unit
@@ -243,12 +234,9 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
   float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
   float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  __nv_bfloat16 *kcat = reinterpret_cast<__nv_bfloat16 *>(ws + pl.ws.kcat);
-  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, pl.gat_ctas, pl.kcat_tokens,
-                           static_cast<const __nv_bfloat16 *>(q),
+  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, static_cast<const __nv_bfloat16 *>(q),
                            static_cast<const __nv_bfloat16 *>(k_cur),
-                           static_cast<const __nv_bfloat16 *>(k_pool), kcat, scale, bpart, tstat,
-                           st));
+                           static_cast<const __nv_bfloat16 *>(k_pool), scale, bpart, tstat, st));
   if (s != XATTN_OK) return s;
   return cu(launch_block_sum(pl.geo, pl.bsum_ctas, bpart, tstat,
                              block_sums, st));

@@ -25,8 +25,6 @@ struct ReqDesc {
   int32_t bsum0;   // first CTA of the request in the block-sum grid
   int32_t sel0;    // ... in the selection grid
   int32_t att0;    // ... in the attention grid
-  int32_t gat0;    // ... in the key-gather grid
-  int32_t kcat0;   // first token of the request in the gathered key buffer
   int32_t pad_;
   int64_t bpart_off;  // float offset of the request's [H, Qb, Kb, Br] block partial sums
   int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
@@ -69,12 +67,11 @@ __device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
 // Launch entry points implemented in the kernel translation units.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t bpart, tstat, counts, kcat, part_o, part_lse, att_cnt, total;
+  size_t bpart, tstat, counts, part_o, part_lse, att_cnt, total;
 };
 
-cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
-                              const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
-                              const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
+cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
+                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
                               float *bpart, float2 *tstat, cudaStream_t st);
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
                              float *block_sums, cudaStream_t st);

@@ -6,18 +6,20 @@
 //   s[a, b] = scale * sum_{i<S} q[S a + S-1-i] . k[S b + i]
 // where reshaped column b runs over [history ; current chunk].
 //
-//   gather_k_kernel   copies each request's keys -- the history pages through
-//                     the block table, then the current chunk -- into one
-//                     contiguous [Hkv, tokens, D] buffer (HBM-bound, coalesced),
-//                     so the GEMM reads K with one TMA box per k-step instead
-//                     of one box per page.
 //   score_gemm_kernel persistent CTAs over 256 x 256 output tiles (two 128-row
 //                     MMA tiles; both accumulators fill the 512 TMEM columns).
-//                     The stride reversal costs nothing: 4-D TMA views (d, phase,
-//                     group, head) of q and of the gathered keys pick phase S-1-i
-//                     of q for the k-step that uses phase i of k.
+//                     The stride reversal costs nothing: TMA views (d, phase,
+//                     group, ...) of q and of the keys pick phase S-1-i of q for
+//                     the k-step that uses phase i of k.  The keys are read where
+//                     they live: a tile's 256 reshaped columns are 256/Br boxes of
+//                     Br rows, each one history page -- a 5-D view
+//                     (d, KV head, phase, group, page) of the pool, addressed
+//                     through the block table -- or Br columns of the current
+//                     chunk; the boxes land back to back, which is the layout of
+//                     one 256-row box.
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
-//                  next tile while the epilogue drains TMEM)
+//                  next tile while the epilogue drains TMEM); lane q issues
+//                  box q of each k-step
 //     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
 //     warps 4..11  epilogue, one thread per row, per 128-column statistics
 //                  tile: the tile max m_t over the visible cells, and for each
@@ -61,7 +63,7 @@ struct Bars {
 };
 
 struct Maps {
-  CUtensorMap q, k;
+  CUtensorMap q, kp, kc;  // queries, pool keys (5-D), current-chunk keys (4-D)
 };
 
 struct Tile {
@@ -134,30 +136,63 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    constexpr int NSUB = COLS / BR;             // key boxes per k-step
+    constexpr int SUB_BYTES = BR * KSTEP * 2;   // Br rows of 128 B (a multiple of 1024)
+    static_assert(NSUB <= 32 && SUB_BYTES % 1024 == 0, "key boxes");
     if (lane == 0) {
       tma_prefetch_desc(&mp.q);
-      tma_prefetch_desc(&mp.k);
-      int it = 0;  // k-steps issued so far (ring position)
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        const Tile tl = decode_tile(g, t);
-        const ReqDesc &R = g.req[tl.r];
-        const int kvh = tl.h / (g.H / g.Hkv);
-        for (int ks = 0; ks < ksteps; ++ks, ++it) {
-          const int s = it % NST;
-          if (it >= NST && !mbar_wait(&bar.empty[s], ((it / NST) - 1) & 1, abort, g.err)) {
-            ok = false;
-            break;
-          }
-          const int kk = ks * KSTEP;
-          const int i = kk / D, dc = kk % D;
-          uint8_t *sA = smem + s * STAGE;
-          mbar_expect_tx(&bar.full[s], STAGE);
-          // q rows S*a + S-1-i and key groups S*b + i of this tile
-          tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
-          tma_load_4d(sA + A_BYTES, &mp.k, &bar.full[s], dc, i, R.kcat0 / S + tl.n0, kvh);
+      tma_prefetch_desc(&mp.kp);
+      tma_prefetch_desc(&mp.kc);
+    }
+    int it = 0;  // k-steps issued so far (ring position)
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Tile tl = decode_tile(g, t);
+      const ReqDesc &R = g.req[tl.r];
+      const int kvh = tl.h / (g.H / g.Hkv);
+      const int ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+      // this lane's key box: reshaped columns [b, b + Br) are one history page
+      // (its block-table entry) or Br groups of the current chunk
+      bool hist = false;
+      int src = R.q0 / S;  // columns past the last one: any in-bounds box (masked)
+      if (lane < NSUB) {
+        const int b = tl.n0 + lane * BR;
+        if (b < ch) {
+          hist = true;
+          src = page_of(g, tl.r, b / BR);  // -1 (and a recorded error) if out of the pool
+          if (src < 0) src = 0;
+        } else if (b < ncol) {
+          src = R.q0 / S + (b - ch);
         }
       }
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const int s = it % NST;
+        int oks = 1;  // lane 0 waits, the warp follows its verdict
+        if (lane == 0 && it >= NST)
+          oks = mbar_wait(&bar.empty[s], ((it / NST) - 1) & 1, abort, g.err);
+        if (!__shfl_sync(0xffffffffu, oks, 0)) {
+          ok = false;
+          break;
+        }
+        const int kk = ks * KSTEP;
+        const int i = kk / D, dc = kk % D;
+        uint8_t *sA = smem + s * STAGE;
+        if (lane == 0) {
+          mbar_expect_tx(&bar.full[s], STAGE);
+          // q rows S*a + S-1-i of this tile
+          tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
+        }
+        __syncwarp();
+        if (lane < NSUB) {  // key rows S*b + i
+          uint8_t *dst = sA + A_BYTES + lane * SUB_BYTES;
+          if (hist)
+            tma_load_5d(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src);
+          else
+            tma_load_4d(dst, &mp.kc, &bar.full[s], dc, i, src, kvh);
+        }
+      }
+    }
+    if (lane == 0) {
       for (int k = max(0, it - NST); k < it; ++k) {
         const uint32_t par = (k / NST) & 1;
         for (uint32_t n = 0; n < kSpinLimit && !mbar_try_wait(&bar.full[k % NST], par); ++n) {
@@ -280,70 +315,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// ---------------------------------------------------------------------------
-// Key gather: one CTA per (request, kv head, block of Bk tokens).
-// ---------------------------------------------------------------------------
-constexpr int GTHR = 256;
-
-__global__ void __launch_bounds__(GTHR) gather_k_kernel(const __grid_constant__ Geo g,
-                                                        const __nv_bfloat16 *__restrict__ kcur,
-                                                        const __nv_bfloat16 *__restrict__ kpool,
-                                                        __nv_bfloat16 *__restrict__ kcat,
-                                                        int64_t kcat_tokens) {
-  const int cta = blockIdx.x;
-  const int r = find_req(g, cta, [](const ReqDesc &d) { return d.gat0; });
-  const ReqDesc &R = g.req[r];
-  const int kbh = R.kh / g.Bk, kb = kbh + R.lq / g.Bk;
-  const int local = cta - R.gat0;
-  const int j = local % kb, kvh = local / kb;
-  const int D = g.D;
-  const __nv_bfloat16 *src;
-  int64_t src_stride;  // elements between consecutive tokens
-  bool valid = true;
-  if (j < kbh) {
-    const int p = page_of(g, r, j);
-    valid = p >= 0;
-    src = kpool + ((int64_t)(valid ? p : 0) * g.Bk * g.Hkv + kvh) * D;
-    src_stride = (int64_t)g.Hkv * D;
-  } else {
-    src = kcur + (int64_t)kvh * g.kv_hs + (int64_t)(R.q0 + (j - kbh) * g.Bk) * D;
-    src_stride = D;
-  }
-  __nv_bfloat16 *dst = kcat + ((int64_t)kvh * kcat_tokens + R.kcat0 + (int64_t)j * g.Bk) * D;
-  const int per_row = D / 8;  // 16-byte chunks per token row
-  const int n = g.Bk * per_row;
-  // all loads of a thread in flight before the first store
-  for (int id0 = threadIdx.x; id0 < n; id0 += 8 * GTHR) {
-    uint4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int id = id0 + u * GTHR;
-      const int t = id / per_row, c = id % per_row;
-      v[u] = make_uint4(0, 0, 0, 0);  // an invalid page reads as zero keys
-      if (valid && id < n) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + t * src_stride) + c);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int id = id0 + u * GTHR;
-      const int t = id / per_row, c = id % per_row;
-      if (id < n) *(reinterpret_cast<uint4 *>(dst + (int64_t)t * D) + c) = v[u];
-    }
-  }
-}
-
 }  // namespace
 
-cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t kcat_tokens,
-                              const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
-                              const __nv_bfloat16 *kpool, __nv_bfloat16 *kcat, float scale,
+cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
+                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
                               float *bpart, float2 *tstat, cudaStream_t st) {
-  if (gather_ctas > 0) {
-    gather_k_kernel<<<gather_ctas, GTHR, 0, st>>>(g, kcur, kpool, kcat, kcat_tokens);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   if (ntiles == 0) return cudaSuccess;
-  const int S = g.S, D = g.D;
+  const int S = g.S, D = g.D, BRc = g.Bk / S;
   const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
   Maps mp;
   {  // q as (d, phase i, group, head)
@@ -353,13 +331,22 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, int gather_ctas, int64_t
     const cuuint32_t box[4] = {KSTEP, 1, ROWS, 1};
     if (!encode_bf16(&mp.q, q, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
-  {  // gathered keys as (d, phase i, group, kv head)
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(kcat_tokens / S),
+  {  // current-chunk keys as (d, phase i, group, kv head), Br groups per box
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(tot_q / S),
                                 (cuuint64_t)g.Hkv};
-    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2,
-                               (cuuint64_t)kcat_tokens * D * 2};
-    const cuuint32_t box[4] = {KSTEP, 1, COLS, 1};
-    if (!encode_bf16(&mp.k, kcat, 4, dims, str, box)) return cudaErrorInvalidValue;
+    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2, (cuuint64_t)g.kv_hs * 2};
+    const cuuint32_t box[4] = {KSTEP, 1, (cuuint32_t)BRc, 1};
+    if (!encode_bf16(&mp.kc, kcur, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  if (g.num_pages > 0 && kpool) {  // pool keys as (d, kv head, phase i, group, page)
+    const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)g.Hkv, (cuuint64_t)S, (cuuint64_t)BRc,
+                                (cuuint64_t)g.num_pages};
+    const cuuint64_t str[4] = {(cuuint64_t)D * 2, (cuuint64_t)g.Hkv * D * 2,
+                               (cuuint64_t)S * g.Hkv * D * 2, (cuuint64_t)g.Bk * g.Hkv * D * 2};
+    const cuuint32_t box[5] = {KSTEP, 1, 1, (cuuint32_t)BRc, 1};
+    if (!encode_bf16(&mp.kp, kpool, 5, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    mp.kp = mp.kc;  // no history anywhere: never used
   }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
