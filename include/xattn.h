@@ -227,6 +227,16 @@ xattn_status lse_merge(const float *o1, const float *lse1, const float *o2,
                        const float *lse2, int64_t rows, int32_t head_dim, void *o_out,
                        int32_t o_out_bf16, float *lse_out, xattn_stream_t stream);
 
+/* Host utility for streaming chunks (no method step): copies `rows` rows of
+ * `width_bytes` bytes, src rows `src_pitch` bytes apart, dst rows `dst_pitch`
+ * bytes apart -- e.g. the [H, chunk, D] window of a [H, L, D] tensor, one row
+ * per head -- enqueued on `stream` (one 2-D copy).  to_device != 0: src is
+ * HOST (pinned for an asynchronous copy), dst DEVICE; else the reverse.
+ * XATTN_EINVAL on null pointers, negative sizes or a pitch below width_bytes. */
+xattn_status xattn_copy_rows_async(void *dst, int64_t dst_pitch, const void *src, int64_t src_pitch,
+                                   int64_t width_bytes, int64_t rows, int32_t to_device,
+                                   xattn_stream_t stream);
+
 /* Reads (and, if clear != 0, resets) the device error word of the current
  * device after synchronising `stream`.  *code is XATTN_OK or the first fault
  * status recorded by a kernel.  Diagnostic call: it blocks the host. */

@@ -136,6 +136,11 @@ def test_entry_point_argument_errors(lib):
     assert lib.lse_merge(odd, fake, fake, fake, 10, 128, fake, 0, fake, None) == -2
     assert lib.lse_merge(None, None, None, None, 0, 128, None, 0, None, None) == 0
     assert lib.xattn_status_string(-3) == b"page id outside the pool"
+    # the 2-D window copy checks its geometry before touching CUDA
+    assert lib.xattn_copy_rows_async(fake, 100, fake, 100, 200, 4, 1, None) == -1  # pitch < width
+    assert lib.xattn_copy_rows_async(fake, 256, fake, 256, 128, -1, 1, None) == -1
+    assert lib.xattn_copy_rows_async(None, 256, fake, 256, 128, 4, 0, None) == -1
+    assert lib.xattn_copy_rows_async(None, 256, None, 256, 0, 4, 0, None) == 0    # nothing to copy
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -351,6 +351,19 @@ xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t cl
   return XATTN_OK;
 }
 
+xattn_status xattn_copy_rows_async(void *dst, int64_t dst_pitch, const void *src, int64_t src_pitch,
+                                   int64_t width_bytes, int64_t rows, int32_t to_device,
+                                   xattn_stream_t stream) {
+  if (width_bytes < 0 || rows < 0 || dst_pitch < width_bytes || src_pitch < width_bytes)
+    return XATTN_EINVAL;
+  if (width_bytes == 0 || rows == 0) return XATTN_OK;
+  if (!dst || !src) return XATTN_EINVAL;
+  return cu(cudaMemcpy2DAsync(dst, (size_t)dst_pitch, src, (size_t)src_pitch, (size_t)width_bytes,
+                              (size_t)rows,
+                              to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost,
+                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 xattn_status xattn_last_device_error(xattn_stream_t stream, int32_t *host_code) {
   return xattn_device_error(stream, host_code, 1);
 }

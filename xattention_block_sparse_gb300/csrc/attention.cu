@@ -706,70 +706,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int slot = (c == c0 && bc < sg.ustart) ? 1 : 0;
         return ((int64_t)c * 2 + slot) * ROWS + x * BM + row;
       };
-      constexpr int MAXP = 4;
-      if (c1 - c0 <= MAXP) {
-        // this CTA's part is still in TMEM (O_x, l_run); up to MAXP other
-        // parts, whose weights are known before any O load is issued
-        int64_t prs[MAXP];
-        float lps[MAXP];
-        int np = 0;
-        for (int c = c0; c <= c1; ++c) {
-          if (c == csk) continue;
-          const int64_t pr = part_row(c);
-          const float lp = (pr >= 0 && wr) ? __ldcg(part_lse + pr) : -INFINITY;
-          if (lp == -INFINITY) continue;  // no key of this row in the part (O not written)
-          prs[np] = pr;
-          lps[np] = lp;
-          ++np;
-        }
-        float M = lse_v;
+      // every part, this CTA's included, from global memory in CTA order: the
+      // same arithmetic whichever CTA merges, so results are reproducible
+      // (rows past the request, wr == false, are whole warps: lq is a multiple of 64)
+      constexpr int MP = 6;  // parts merged with all their loads in flight
+      if (wr && c1 - c0 < MP) {
+        // weights first (in CTA order), then per 8 columns the loads of every part
+        int64_t pr[MP];
+        float lp[MP];
 #pragma unroll
-        for (int q = 0; q < MAXP; ++q)
-          if (q < np) M = fmaxf(M, lps[q]);
-        float w_own = (M == -INFINITY || lse_v == -INFINITY) ? 0.f : __expf(lse_v - M);
-        float ws[MAXP], den = w_own;
-#pragma unroll
-        for (int q = 0; q < MAXP; ++q) {
-          ws[q] = q < np ? __expf(lps[q] - M) : 0.f;
-          den += ws[q];
+        for (int q = 0; q < MP; ++q) {
+          pr[q] = c0 + q <= c1 ? part_row(c0 + q) : -1;
+          lp[q] = pr[q] >= 0 ? __ldcg(part_lse + pr[q]) : -INFINITY;
         }
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < MP; ++q) M = fmaxf(M, lp[q]);
+        float den = 0.f, w[MP];
+#pragma unroll
+        for (int q = 0; q < MP; ++q) den += lp[q] != -INFINITY ? __expf(lp[q] - M) : 0.f;
         const float rden = den > 0.f ? 1.f / den : 0.f;
-        w_own *= rden * inv;  // applied to the unnormalised O in TMEM
 #pragma unroll
-        for (int q = 0; q < MAXP; ++q) ws[q] *= rden;
+        for (int q = 0; q < MP; ++q) w[q] = lp[q] != -INFINITY ? __expf(lp[q] - M) * rden : 0.f;
         for (int cb = 0; cb < D / 32; ++cb) {
           float acc[32];
-          __syncwarp();
-          if (nx > 0) {
-            uint32_t ov[32];
-            tmem_ld32(lane_addr + o_col + cb * 32, ov);
-            tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc[jj] = __uint_as_float(ov[jj]) * w_own;
-          } else {
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float v[MP][8];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
-          }
-          for (int q = 0; q < np; q += 2) {  // two parts' loads in flight at a time
-            const bool two = q + 1 < np;
-            const float w0 = ws[q], w1 = two ? ws[q + 1] : 0.f;
-            const float *src0 = part_o + prs[q] * D + cb * 32;
-            const float *src1 = part_o + prs[two ? q + 1 : q] * D + cb * 32;
+            for (int q = 0; q < MP; ++q) {
+              if (lp[q] != -INFINITY) {  // a part without keys of this row wrote no O
+                load_part8(part_o + pr[q] * D + cb * 32 + q8 * 8, v[q]);
+              } else {
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              float v0[8], v1[8];
-              load_part8(src0 + q8 * 8, v0);
-              load_part8(src1 + q8 * 8, v1);
+                for (int e = 0; e < 8; ++e) v[q][e] = 0.f;
+              }
+            }
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                acc[q8 * 8 + e] = fmaf(w1, v1[e], fmaf(w0, v0[e], acc[q8 * 8 + e]));
+            for (int e = 0; e < 8; ++e) {
+              float a8 = 0.f;
+#pragma unroll
+              for (int q = 0; q < MP; ++q) a8 = fmaf(w[q], v[q][e], a8);
+              acc[q8 * 8 + e] = a8;
             }
           }
-          if (wr) store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
+          store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
         }
-        if (wr) *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
+        *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
       } else if (wr) {
-        // many parts: every part, this CTA's included, from global memory
+        // more parts: the same arithmetic, one part at a time
         float M = -INFINITY;
         for (int c = c0; c <= c1; ++c) {
           const int64_t pr = part_row(c);
@@ -778,9 +763,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         float den = 0.f;
         for (int c = c0; c <= c1; ++c) {
           const int64_t pr = part_row(c);
-          if (pr < 0) continue;
-          const float lp = __ldcg(part_lse + pr);
-          if (lp != -INFINITY) den += __expf(lp - M);
+          const float lp = pr >= 0 ? __ldcg(part_lse + pr) : -INFINITY;
+          den += lp != -INFINITY ? __expf(lp - M) : 0.f;
         }
         const float rden = den > 0.f ? 1.f / den : 0.f;
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -793,13 +777,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float lp = __ldcg(part_lse + pr);
             if (lp == -INFINITY) continue;
             const float w = __expf(lp - M) * rden;
+            float v[32];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              float v[8];
-              load_part8(part_o + pr * D + cb * 32 + q8 * 8, v);
+            for (int q8 = 0; q8 < 4; ++q8) load_part8(part_o + pr * D + cb * 32 + q8 * 8, v + q8 * 8);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[q8 * 8 + e] = fmaf(w, v[e], acc[q8 * 8 + e]);
-            }
+            for (int jj = 0; jj < 32; ++jj) acc[jj] = fmaf(w, v[jj], acc[jj]);
           }
           store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
         }

@@ -88,6 +88,58 @@ class SequencePrefill:
             if on_chunk is not None:
                 on_chunk(c, self.bufs)
 
+    def run_from_host(self, host, dev, tau, stream, h2d_stream, d2h_stream):
+        """The whole prefill from pinned host memory, copies overlapped with
+        compute.  On `h2d_stream`: chunk 0's Q, K, V, then the two page pools
+        (one copy each: a chunk's history pages are scattered through the pool
+        by the block table), then the Q, K, V of chunks 1, 2, ...; chunk c
+        computes on `stream` once the copies it reads have landed (an event), so
+        chunk 0 runs while the pools are still coming in and later chunks'
+        inputs arrive under earlier chunks' compute.  Chunk c's O and LSE go
+        device -> host on `d2h_stream` once it is done ([SYNC] 修复方案: every
+        consumer waits on the event of the copy it reads).
+
+        host, dev: dicts of tensors 'q', 'k', 'v', 'kpool', 'vpool', 'o', 'lse'
+        (host pinned, same shapes).  Work is enqueued after whatever `stream`
+        already holds; the side streams start from that point too.  Returns the
+        event recorded on `stream` after the last read-back."""
+        import torch
+        start = torch.cuda.Event()
+        start.record(stream)
+        h2d_stream.wait_event(start)
+        d2h_stream.wait_event(start)
+        n = len(self.problems)
+        ready = []
+
+        def chunk_inputs(c):
+            t0, t1 = c * self.chunk, (c + 1) * self.chunk
+            for name in ("q", "k", "v"):  # one 2-D copy each: a row per head
+                X.copy_window_async(dev[name], host[name], t0, t1, h2d_stream)
+            ev = torch.cuda.Event()
+            ev.record(h2d_stream)
+            ready.append(ev)
+
+        with torch.cuda.stream(h2d_stream):
+            chunk_inputs(0)
+            dev["kpool"].copy_(host["kpool"], non_blocking=True)
+            dev["vpool"].copy_(host["vpool"], non_blocking=True)
+            for c in range(1, n):
+                chunk_inputs(c)
+        for c in range(n):
+            t0, t1 = c * self.chunk, (c + 1) * self.chunk
+            stream.wait_event(ready[c])
+            self.run_chunk(c, dev["q"], dev["k"], dev["v"], dev["kpool"], dev["vpool"], tau,
+                           dev["o"], dev["lse"], stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h_stream.wait_event(done)
+            X.copy_window_async(host["o"], dev["o"], t0, t1, d2h_stream)
+            X.copy_window_async(host["lse"], dev["lse"], t0, t1, d2h_stream)
+        back = torch.cuda.Event()
+        back.record(d2h_stream)
+        stream.wait_event(back)
+        return back
+
 
 class LayerRing:
     """N-slot ring of per-layer KV page pools fed from pinned host memory.

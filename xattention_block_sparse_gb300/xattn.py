@@ -28,7 +28,8 @@ STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAG
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
             "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
             "lse_merge",
-            "xattn_device_error", "xattn_last_device_error", "xattn_status_string"]
+            "xattn_device_error", "xattn_last_device_error", "xattn_copy_rows_async",
+            "xattn_status_string"]
 
 
 class XattnError(RuntimeError):
@@ -84,6 +85,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
         "xattn_last_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
+        "xattn_copy_rows_async": (ctypes.c_int, [vp, i64, vp, i64, i64, i64, i32, vp]),
         "xattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -242,6 +244,23 @@ def xattn_last_device_error(stream=None) -> int:
     st = load_library().xattn_last_device_error(_stream(stream), ctypes.byref(code))
     _check(st, "xattn_last_device_error")
     return int(code.value)
+
+
+def copy_window_async(dst, src, t0, t1, stream=None):
+    """dst[:, t0:t1] = src[:, t0:t1] for [rows, L, ...] tensors on opposite sides
+    (one side pinned host, the other device), as one 2-D copy on `stream`."""
+    to_device = 1 if dst.is_cuda else 0
+    if dst.is_cuda == src.is_cuda:
+        raise ValueError("copy_window_async copies between host and device")
+    if dst.shape != src.shape or not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("copy_window_async wants two contiguous tensors of one shape")
+    row = dst[0].numel() * dst.element_size()          # bytes of one leading row
+    per_t = dst[0, 0].numel() * dst.element_size()     # bytes of one token
+    off = t0 * per_t
+    st = load_library().xattn_copy_rows_async(
+        ctypes.c_void_p(dst.data_ptr() + off), row, ctypes.c_void_p(src.data_ptr() + off), row,
+        (t1 - t0) * per_t, dst.shape[0], to_device, _stream(stream))
+    _check(st, "xattn_copy_rows_async")
 
 
 def xattn_status_string(status: int) -> str:
