@@ -204,10 +204,14 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
  *   workspace      DEVICE scratch of at least xattn_workspace_size(p) bytes,
  *                  16-byte aligned (XATTN_EWORKSPACE / XATTN_EALIGN otherwise);
  *                  the same buffer xattn_estimate / xattn_select take.  The
- *                  work (KV tiles of every 256-row query tile) is split evenly
- *                  over one persistent CTA per SM; a query tile cut between
- *                  CTAs leaves normalised partial results (fp32 O, LSE) here,
- *                  merged by log-sum-exp into o / lse by a second kernel.
+ *                  kernel picks its schedule on the device from n_sel: one CTA
+ *                  per 256-row query unit for small launches, else the KV
+ *                  tiles of all units split evenly over one persistent CTA per
+ *                  SM; a unit cut between CTAs leaves normalised partial results
+ *                  (fp32 O, LSE) here, merged by log-sum-exp into o / lse by the
+ *                  CTA that finishes its part last.  The result does not depend
+ *                  on which CTA that is (the parts are merged in a fixed order):
+ *                  repeated calls give identical bits.
  *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
  *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE */
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
