@@ -17,9 +17,14 @@
 //                     through the block table -- or Br columns of the current
 //                     chunk; the boxes land back to back, which is the layout of
 //                     one 256-row box.
+//                     When the query heads per KV head are even, two CTAs
+//                     of a cluster take the same tile of two heads of one KV
+//                     group: their key tiles are identical, so each CTA loads
+//                     half of the key boxes and multicasts them to both, which
+//                     halves the TMA box count that limits this kernel.
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
 //                  next tile while the epilogue drains TMEM); lane q issues
-//                  box q of each k-step
+//                  key box q of each k-step (of this CTA's half in a pair)
 //     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
 //     warps 4..11  epilogue, one thread per row, per 128-column statistics
 //                  tile: the tile max m_t over the visible cells, and for each
@@ -71,9 +76,13 @@ struct Tile {
 };
 
 // Tile t of the score GEMM: requests in order, then head, then row tile, then
-// column tile; only tiles holding visible cells exist.
-__device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
-  const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0; });
+// column tile; only tiles holding visible cells exist.  With PAIR the index runs
+// over head pairs (2p, 2p + 1) -- two query heads of one KV group, which read the
+// same key tile -- and the CTA of cluster rank `rank` takes head 2p + rank.
+template <bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const Geo &g, int t, int rank) {
+  constexpr int div = PAIR ? 2 : 1;
+  const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0 / div; });
   const ReqDesc &R = g.req[r];
   const int S = g.S;
   const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
@@ -82,11 +91,12 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
     const int vis = min(ch + min(m0 + ROWS, rq), ncol);
     per_head += (vis + COLS - 1) / COLS;
   }
-  int local = t - R.gemm0;
+  int local = t - R.gemm0 / div;
   Tile tl;
   tl.r = r;
   tl.h = local / per_head;
   local -= tl.h * per_head;
+  if (PAIR) tl.h = 2 * tl.h + rank;
   for (int m0 = 0; m0 < rq; m0 += ROWS) {
     const int vis = min(ch + min(m0 + ROWS, rq), ncol);
     const int n = (vis + COLS - 1) / COLS;
@@ -101,7 +111,7 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
   return tl;
 }
 
-template <int BR>
+template <int BR, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int ntiles,
                       float scale, float *__restrict__ bpart, float2 *__restrict__ tstat) {
@@ -114,11 +124,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = g.S, D = g.D;
   const int ksteps = S * D / KSTEP;
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  // a pair's tiles: cluster c of the grid walks pair tiles c, c + nclusters, ...
+  const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar.full[s], 1);
-      mbar_init(&bar.empty[s], 1);
+      // with PAIR a slot is refilled (in both CTAs) once both CTAs' MMAs read it
+      mbar_init(&bar.empty[s], PAIR ? 2 : 1);
     }
     mbar_init(&bar.acc_full, 1);
     mbar_init(&bar.acc_empty, 8);  // one arrival per epilogue warp
@@ -132,13 +147,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peer's multicast loads and commits target barriers this CTA has initialised
+  if (PAIR) cluster_sync();
   const uint32_t tmem = bar.tmem_base;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     constexpr int NSUB = COLS / BR;             // key boxes per k-step
+    constexpr int NOWN = PAIR ? NSUB / 2 : NSUB;  // boxes this CTA issues (PAIR: to both CTAs)
     constexpr int SUB_BYTES = BR * KSTEP * 2;   // Br rows of 128 B (a multiple of 1024)
     static_assert(NSUB <= 32 && SUB_BYTES % 1024 == 0, "key boxes");
+    const int box = rank * NOWN + lane;         // the key box this lane issues
     if (lane == 0) {
       tma_prefetch_desc(&mp.q);
       tma_prefetch_desc(&mp.kp);
@@ -146,8 +165,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int it = 0;  // k-steps issued so far (ring position)
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-      const Tile tl = decode_tile(g, t);
+    for (int t = tile0; ok && t < ntiles; t += tstep) {
+      const Tile tl = decode_tile<PAIR>(g, t, rank);
       const ReqDesc &R = g.req[tl.r];
       const int kvh = tl.h / (g.H / g.Hkv);
       const int ch = R.kh / S, ncol = (R.kh + R.lq) / S;
@@ -155,8 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // (its block-table entry) or Br groups of the current chunk
       bool hist = false;
       int src = R.q0 / S;  // columns past the last one: any in-bounds box (masked)
-      if (lane < NSUB) {
-        const int b = tl.n0 + lane * BR;
+      if (lane < NOWN) {
+        const int b = tl.n0 + box * BR;
         if (b < ch) {
           hist = true;
           src = page_of(g, tl.r, b / BR);  // -1 (and a recorded error) if out of the pool
@@ -183,12 +202,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
         }
         __syncwarp();
-        if (lane < NSUB) {  // key rows S*b + i
-          uint8_t *dst = sA + A_BYTES + lane * SUB_BYTES;
-          if (hist)
-            tma_load_5d(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src);
-          else
-            tma_load_4d(dst, &mp.kc, &bar.full[s], dc, i, src, kvh);
+        if (lane < NOWN) {  // key rows S*b + i
+          uint8_t *dst = sA + A_BYTES + box * SUB_BYTES;
+          if (PAIR) {
+            if (hist)
+              tma_load_5d_mc(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src, 3);
+            else
+              tma_load_4d_mc(dst, &mp.kc, &bar.full[s], dc, i, src, kvh, 3);
+          } else {
+            if (hist)
+              tma_load_5d(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src);
+            else
+              tma_load_4d(dst, &mp.kc, &bar.full[s], dc, i, src, kvh);
+          }
         }
       }
     }
@@ -207,8 +233,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t d0 = sdesc_sw128(smem_addr(smem), 16, 1024);
       int it = 0, n = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++n) {
-        const Tile tl = decode_tile(g, t);
+      for (int t = tile0; ok && t < ntiles; t += tstep, ++n) {
+        const Tile tl = decode_tile<PAIR>(g, t, rank);
         const int rq = g.req[tl.r].lq / S;
         const bool two_m = tl.m0 + TM < rq;
         // the epilogue has drained the previous tile's accumulators
@@ -229,12 +255,23 @@ __global__ void __launch_bounds__(THREADS, 1)
               mma_f16_ss(tmem + x * COLS, a0 + (uint64_t)((x * (TM * 128) + kq * 32) >> 4),
                          b0 + (uint64_t)((kq * 32) >> 4), idesc, (ks > 0 || kq > 0) ? 1u : 0u);
           }
-          mma_commit(&bar.empty[s]);
+          if (PAIR)
+            mma_commit_mc(&bar.empty[s], 3);  // both CTAs' slot s may be refilled
+          else
+            mma_commit(&bar.empty[s]);
         }
         mma_commit(&bar.acc_full);
       }
       // every MMA issued has completed before TMEM is freed: the epilogue waited
-      // for each tile's acc_full, and no MMA follows the last commit
+      // for each tile's acc_full, and no MMA follows the last commit.  With PAIR
+      // the peer's arrivals on this CTA's slots have landed too before it exits.
+      if (PAIR) {
+        for (int k = max(0, it - NST); k < it; ++k) {
+          const uint32_t par = (k / NST) & 1;
+          for (uint32_t q = 0; q < kSpinLimit && !mbar_try_wait(&bar.empty[k % NST], par); ++q) {
+          }
+        }
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
@@ -242,8 +279,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row = tid - 128 - x * TM;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + x * COLS;
     int n = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++n) {
-      const Tile tl = decode_tile(g, t);
+    for (int t = tile0; t < ntiles; t += tstep, ++n) {
+      const Tile tl = decode_tile<PAIR>(g, t, rank);
       const ReqDesc &R = g.req[tl.r];
       const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
       const int ntile = (ncol + kTileCols - 1) / kTileCols;
@@ -312,6 +349,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no CTA of a pair leaves while the other may still write its shared memory
+  if (PAIR) cluster_sync();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -352,18 +391,44 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidValue;
-  const int grid = ntiles < sms ? ntiles : sms;
+  // Pairs of query heads of one KV group run as 2-CTA clusters that share each
+  // key tile: every CTA issues half of the key boxes, multicast to both.
+  const bool pair = (g.H / g.Hkv) % 2 == 0;
   auto run = [&](auto kernel) {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(g, mp, ntiles, scale, bpart, tstat);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = st;
+    int units = ntiles, slots = sms;
+    if (pair) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3(2);
+      int ncl = 0;
+      e = cudaOccupancyMaxActiveClusters(&ncl, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (ncl < 1) return cudaErrorInvalidConfiguration;
+      units = ntiles / 2;  // head pairs
+      slots = ncl;
+    }
+    const int n = units < slots ? units : slots;
+    cfg.gridDim = dim3(pair ? 2 * n : n);
+    e = cudaLaunchKernelEx(&cfg, kernel, g, mp, units, scale, bpart, tstat);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
   switch (g.Bk / S) {  // Br: reshaped columns per KV block
-    case 8: return run(score_gemm_kernel<8>);
-    case 16: return run(score_gemm_kernel<16>);
-    case 32: return run(score_gemm_kernel<32>);
+    case 8: return pair ? run(score_gemm_kernel<8, true>) : run(score_gemm_kernel<8, false>);
+    case 16: return pair ? run(score_gemm_kernel<16, true>) : run(score_gemm_kernel<16, false>);
+    case 32: return pair ? run(score_gemm_kernel<32, true>) : run(score_gemm_kernel<32, false>);
     default: return cudaErrorInvalidValue;
   }
 }
