@@ -231,6 +231,25 @@ xattn_status lse_merge(const float *o1, const float *lse1, const float *o2,
                        const float *lse2, int64_t rows, int32_t head_dim, void *o_out,
                        int32_t o_out_bf16, float *lse_out, xattn_stream_t stream);
 
+/* KV store of a prefill chunk ("Task Plan: Layerwise Offload Refactoring",
+ * Phase 1.2, offload_layer_kv_async: a prefill's keys and values go block by
+ * block into the cache blocks named by its block ids).  Chunk token t of
+ * request r sits at position kh_r + t of the request, so for every KV head
+ *   k_pool[page][row][kvh][:] = k_cur[kvh][q0_r + t][:]   (v likewise),
+ *   page = block_table[r][(kh_r + t) / block_size], row = (kh_r + t) % block_size,
+ * which makes the chunk's blocks history for the request's next chunk.
+ *   k_cur, v_cur    DEVICE bf16 [Hkv, tokens, D] (kv_head_stride), as for
+ *                   bsa_chunk_attention
+ *   k_pool, v_pool  DEVICE bf16 [num_pages, block_size, Hkv, D], written
+ * The block table row must reach the chunk's last block: (kh_r + lq_r) /
+ * block_size <= bt_stride for every request, else XATTN_EINVAL (as are null
+ * pointers and num_pages < 1); pointers must be 16-byte aligned (XATTN_EALIGN).
+ * A table entry outside [0, num_pages) (-1: unallocated) records XATTN_EPAGE
+ * in the device error word and that block is not written.  Enqueued on
+ * `stream`; nothing else in the pools changes. */
+xattn_status xattn_store_kv(const xattn_problem *p, const void *k_cur, const void *v_cur,
+                            void *k_pool, void *v_pool, xattn_stream_t stream);
+
 /* Host utility for streaming chunks (no method step): copies `rows` rows of
  * `width_bytes` bytes, src rows `src_pitch` bytes apart, dst rows `dst_pitch`
  * bytes apart -- e.g. the [H, chunk, D] window of a [H, L, D] tensor, one row

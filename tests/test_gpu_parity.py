@@ -282,3 +282,74 @@ def test_prefill_from_host_matches_device_resident_run():
     assert X.xattn_device_error() == 0
     assert np.array_equal(host["o"].float().numpy(), O_dev)
     assert np.array_equal(host["lse"].numpy(), L_dev)
+
+
+@pytest.mark.parametrize("Hkv,D,Bk", [(8, 128, 128), (1, 64, 64)])
+def test_store_kv_writes_each_chunk_block_to_its_page(Hkv, D, Bk):
+    """xattn_store_kv on a two-request varlen chunk: every chunk block lands,
+    bit for bit, on the page its position names in the block table; history
+    pages and pages no block names keep their contents; a -1 entry records
+    XATTN_EPAGE and leaves that block unwritten."""
+    d = dev()
+    rng = np.random.default_rng(7 + D)
+    q_lens, kh_lens = [2 * Bk, 3 * Bk], [Bk, 0]
+    tot = sum(q_lens)
+    P = 12
+    kc = rng.integers(0, 1 << 16, size=(Hkv, tot, D), dtype=np.uint16)
+    vc = rng.integers(0, 1 << 16, size=(Hkv, tot, D), dtype=np.uint16)
+    perm = rng.permutation(P).astype(np.int32)
+    bt = np.full((2, 4), -1, dtype=np.int32)
+    bt[0, :3] = perm[:3]           # block 0 is history: not written
+    bt[1, :3] = perm[3:6]
+    bt[1, 1] = -1                  # unallocated: recorded, skipped
+    sentinel = np.uint16(0x7E7E)
+    kp = np.full((P, Bk, Hkv, D), sentinel, dtype=np.uint16)
+    vp = kp.copy()
+    as_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(d).view(torch.bfloat16)
+    KC, VC, KP, VP = as_dev(kc), as_dev(vc), as_dev(kp), as_dev(vp)
+    prob = X.Problem(8 * Hkv, Hkv, D, 8, Bk, q_lens, kh_lens, torch.from_numpy(bt).to(d), P)
+    X.xattn_store_kv(prob, KC, VC, KP, VP)
+    torch.cuda.synchronize()
+    assert X.xattn_last_device_error() == -3  # XATTN_EPAGE
+    want_k, want_v = kp.copy(), vp.copy()
+    q0 = 0
+    for r in range(2):
+        for j in range(q_lens[r] // Bk):
+            page = bt[r, kh_lens[r] // Bk + j]
+            if page < 0:
+                continue
+            toks = slice(q0 + j * Bk, q0 + (j + 1) * Bk)
+            want_k[page] = kc[:, toks].transpose(1, 0, 2)
+            want_v[page] = vc[:, toks].transpose(1, 0, 2)
+        q0 += q_lens[r]
+    got_k = KP.view(torch.int16).cpu().numpy().view(np.uint16)
+    got_v = VP.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got_k, want_k)
+    assert np.array_equal(got_v, want_v)
+
+
+def test_prefill_from_host_with_kv_store_matches_prefilled_pool():
+    """run_from_host(store_kv=True) copies only Q, K, V and builds the pools on
+    the device, chunk by chunk, from the sequence's own keys and values: its O
+    and LSE equal those of the run on the prefilled pools, and the pools end
+    equal to them.  The device pools start as NaN, so a history page read
+    before it was stored would show."""
+    case = SequenceCase("q06b_4k")
+    O_dev, L_dev, _ = case.run(0.9)
+    pin = lambda t: t.cpu().pin_memory()
+    host = {"q": pin(case.Q), "k": pin(case.K), "v": pin(case.V)}
+    host["o"] = torch.zeros((case.cfg.H, case.L, case.cfg.D), dtype=torch.bfloat16).pin_memory()
+    host["lse"] = torch.zeros((case.cfg.H, case.L), dtype=torch.float32).pin_memory()
+    devb = {k: torch.zeros_like(t, device=dev()) for k, t in host.items()}
+    for name, ref in (("kpool", case.KP), ("vpool", case.VP)):
+        devb[name] = torch.full_like(ref, float("nan"))
+    stream = torch.cuda.Stream(device=dev())
+    h2d, d2h = torch.cuda.Stream(device=dev()), torch.cuda.Stream(device=dev())
+    for _ in range(2):
+        case.seq.run_from_host(host, devb, 0.9, stream, h2d, d2h, store_kv=True)
+    stream.synchronize()
+    assert X.xattn_device_error() == 0
+    assert np.array_equal(host["o"].float().numpy(), O_dev)
+    assert np.array_equal(host["lse"].numpy(), L_dev)
+    assert torch.equal(devb["kpool"].view(torch.int16), case.KP.view(torch.int16))
+    assert torch.equal(devb["vpool"].view(torch.int16), case.VP.view(torch.int16))

@@ -141,6 +141,13 @@ def test_entry_point_argument_errors(lib):
     assert lib.xattn_copy_rows_async(fake, 256, fake, 256, 128, -1, 1, None) == -1
     assert lib.xattn_copy_rows_async(None, 256, fake, 256, 128, 4, 0, None) == -1
     assert lib.xattn_copy_rows_async(None, 256, None, 256, 0, 4, 0, None) == 0    # nothing to copy
+    # the KV store: null pools, unaligned pointers, a block table row too short for the chunk
+    assert lib.xattn_store_kv(p.ref(), fake, fake, None, fake, None) == -1
+    assert lib.xattn_store_kv(p.ref(), fake, odd, fake, fake, None) == -2
+    short = _prob([1024], [1024], W=15)  # 8 history + 8 chunk blocks need 16 entries
+    assert lib.xattn_store_kv(short.ref(), fake, fake, fake, fake, None) == -1
+    assert lib.xattn_store_kv(_prob([1024], [0], pages=0).ref(), fake, fake, fake, fake,
+                              None) == -1  # no pool pages
 
 
 def test_missing_library_fails_loudly(tmp_path):

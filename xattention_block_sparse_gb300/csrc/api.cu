@@ -337,6 +337,29 @@ xattn_status lse_merge(const float *o1, const float *lse1, const float *o2, cons
                              lse_out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+xattn_status xattn_store_kv(const xattn_problem *p, const void *k_cur, const void *v_cur,
+                            void *k_pool, void *v_pool, xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!k_cur || !v_cur || !k_pool || !v_pool || !p->block_table || p->num_pages < 1)
+    return XATTN_EINVAL;
+  if (!aligned16(k_cur) || !aligned16(v_cur) || !aligned16(k_pool) || !aligned16(v_pool))
+    return XATTN_EALIGN;
+  int max_blocks = 0;
+  for (int r = 0; r < p->num_requests; ++r) {
+    const ReqDesc &d = pl.geo.req[r];
+    if ((int64_t)(d.kh + d.lq) / p->block_size > p->bt_stride) return XATTN_EINVAL;
+    if (d.lq / p->block_size > max_blocks) max_blocks = d.lq / p->block_size;
+  }
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  return cu(launch_store_kv(pl.geo, max_blocks, static_cast<const __nv_bfloat16 *>(k_cur),
+                            static_cast<const __nv_bfloat16 *>(v_cur),
+                            static_cast<__nv_bfloat16 *>(k_pool),
+                            static_cast<__nv_bfloat16 *>(v_pool),
+                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 xattn_status xattn_device_error(xattn_stream_t stream, int32_t *code, int32_t clear) {
   if (!code) return XATTN_EINVAL;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

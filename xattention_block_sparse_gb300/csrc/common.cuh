@@ -86,6 +86,9 @@ cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const int32_t *sel_page, const int32_t *n_sel, float scale,
                              __nv_bfloat16 *o, float *lse, float *part_o, float *part_lse,
                              int32_t *unit_cnt, cudaStream_t st);
+cudaError_t launch_store_kv(const Geo &g, int max_blocks, const __nv_bfloat16 *kc,
+                            const __nv_bfloat16 *vc, __nv_bfloat16 *kp, __nv_bfloat16 *vp,
+                            cudaStream_t st);
 cudaError_t launch_lse_merge(const float *o1, const float *l1, const float *o2, const float *l2,
                              int64_t rows, int D, void *o_out, int bf16_out, float *l_out,
                              cudaStream_t st);

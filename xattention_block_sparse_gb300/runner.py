@@ -88,21 +88,31 @@ class SequencePrefill:
             if on_chunk is not None:
                 on_chunk(c, self.bufs)
 
-    def run_from_host(self, host, dev, tau, stream, h2d_stream, d2h_stream):
+    def run_from_host(self, host, dev, tau, stream, h2d_stream, d2h_stream, store_kv=False):
         """The whole prefill from pinned host memory, copies overlapped with
-        compute.  On `h2d_stream`: chunk 0's Q, K, V, then the two page pools
-        (one copy each: a chunk's history pages are scattered through the pool
-        by the block table), then the Q, K, V of chunks 1, 2, ...; chunk c
-        computes on `stream` once the copies it reads have landed (an event), so
-        chunk 0 runs while the pools are still coming in and later chunks'
-        inputs arrive under earlier chunks' compute.  Chunk c's O and LSE go
-        device -> host on `d2h_stream` once it is done ([SYNC] 修复方案: every
-        consumer waits on the event of the copy it reads).
+        compute.  Chunk c computes on `stream` once the copies it reads have
+        landed (an event), and its O and LSE go device -> host on `d2h_stream`
+        once it is done ([SYNC] 修复方案: every consumer waits on the event of
+        the copy it reads).
 
-        host, dev: dicts of tensors 'q', 'k', 'v', 'kpool', 'vpool', 'o', 'lse'
-        (host pinned, same shapes).  Work is enqueued after whatever `stream`
-        already holds; the side streams start from that point too.  Returns the
-        event recorded on `stream` after the last read-back."""
+        store_kv=False: the page pools are inputs.  On `h2d_stream`: chunk 0's
+        Q, K, V, then the two pools (one copy each: a chunk's history pages are
+        scattered through the pool by the block table), then the Q, K, V of
+        chunks 1, 2, ...; chunk 0 runs while the pools are still coming in.
+
+        store_kv=True: the pools are built on the device.  Only Q, K, V cross
+        from the host, chunk by chunk; before chunk c runs, xattn_store_kv
+        writes its K and V into the pages the block table gives their positions
+        ("Task Plan: Layerwise Offload Refactoring", Phase 1.2), which is the
+        history chunk c + 1 reads.  With a block table that maps every position
+        of the sequence, the pools end up equal to a prefilled pool of the same
+        sequence, so the results are too.
+
+        host, dev: dicts of tensors 'q', 'k', 'v', 'o', 'lse' (and 'kpool',
+        'vpool' on the device; on the host too unless store_kv), host pinned,
+        same shapes.  Work is enqueued after whatever `stream` already holds;
+        the side streams start from that point too.  Returns the event recorded
+        on `stream` after the last read-back."""
         import torch
         start = torch.cuda.Event()
         start.record(stream)
@@ -121,13 +131,17 @@ class SequencePrefill:
 
         with torch.cuda.stream(h2d_stream):
             chunk_inputs(0)
-            dev["kpool"].copy_(host["kpool"], non_blocking=True)
-            dev["vpool"].copy_(host["vpool"], non_blocking=True)
+            if not store_kv:
+                dev["kpool"].copy_(host["kpool"], non_blocking=True)
+                dev["vpool"].copy_(host["vpool"], non_blocking=True)
             for c in range(1, n):
                 chunk_inputs(c)
         for c in range(n):
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             stream.wait_event(ready[c])
+            if store_kv:
+                X.xattn_store_kv(self.problems[c], dev["k"][:, t0:], dev["v"][:, t0:],
+                                 dev["kpool"], dev["vpool"], stream)
             self.run_chunk(c, dev["q"], dev["k"], dev["v"], dev["kpool"], dev["vpool"], tau,
                            dev["o"], dev["lse"], stream)
             done = torch.cuda.Event()

@@ -27,7 +27,7 @@ STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAG
 
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
             "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
-            "lse_merge",
+            "lse_merge", "xattn_store_kv",
             "xattn_device_error", "xattn_last_device_error", "xattn_copy_rows_async",
             "xattn_status_string"]
 
@@ -83,6 +83,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, sz, vp, vp,
                                                 vp]),
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
+        "xattn_store_kv": (ctypes.c_int, [P, vp, vp, vp, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
         "xattn_last_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "xattn_copy_rows_async": (ctypes.c_int, [vp, i64, vp, i64, i64, i64, i32, vp]),
@@ -244,6 +245,14 @@ def xattn_last_device_error(stream=None) -> int:
     st = load_library().xattn_last_device_error(_stream(stream), ctypes.byref(code))
     _check(st, "xattn_last_device_error")
     return int(code.value)
+
+
+def xattn_store_kv(problem, k_cur, v_cur, k_pool, v_pool, stream=None):
+    """Write the chunk's K/V ([Hkv, tokens, D] views, kv_head_stride apart) into
+    the pool pages the block table gives their positions."""
+    st = load_library().xattn_store_kv(problem.ref(), _ptr(k_cur), _ptr(v_cur), _ptr(k_pool),
+                                       _ptr(v_pool), _stream(stream))
+    _check(st, "xattn_store_kv")
 
 
 def copy_window_async(dst, src, t0, t1, stream=None):
