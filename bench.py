@@ -362,9 +362,10 @@ def run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk):
     return {"value": L * steps / t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3 / steps,
             "copies": "Q, K, V copied chunk by chunk on one side stream, overlapped with "
-                      "earlier chunks' compute; each chunk's K/V stored into its pool pages "
-                      "on the device (xattn_store_kv) before it runs; O and LSE read back "
-                      "per chunk on another side stream"}
+                      "earlier chunks' compute (a chunk's estimate waits for its Q and K, "
+                      "its attention for V too); each chunk's K/V stored into its pool pages "
+                      "on the device (xattn_store_kv) before its attention; O and LSE read "
+                      "back per chunk on another side stream"}
 
 
 # ---------------------------------------------------------------------------

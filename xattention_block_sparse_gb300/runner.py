@@ -46,18 +46,32 @@ def estimation_scale(head_dim: int, stride: int) -> float:
     return 1.0 / (math.sqrt(head_dim) * stride)
 
 
-def prefill_chunk(problem, q, k_cur, v_cur, k_pool, v_pool, tau, bufs: ChunkBuffers, o, lse,
-                  est_scale=None, softmax_scale=None, stream=None):
-    """One chunk of XAttention BSA prefill: estimate, select, attend."""
+def estimate_select(problem, q, k_cur, k_pool, tau, bufs: ChunkBuffers, est_scale=None,
+                    stream=None):
+    """Steps 1 and 2 of a chunk: estimation, then the block selection (sel_page,
+    n_sel in bufs).  Reads Q, the chunk's K and the history pages; not V."""
     D = problem.c.head_dim
     est_scale = estimation_scale(D, problem.c.stride) if est_scale is None else est_scale
-    softmax_scale = 1.0 / math.sqrt(D) if softmax_scale is None else softmax_scale
     X.xattn_estimate(problem, q, k_cur, k_pool, est_scale, bufs.workspace, bufs.block_sums,
                      stream)
     X.xattn_select(problem, bufs.block_sums, tau, bufs.workspace, bufs.mask, bufs.sel_idx,
                    bufs.sel_page, bufs.n_sel, stream)
+
+
+def attend(problem, q, k_cur, v_cur, k_pool, v_pool, bufs: ChunkBuffers, o, lse,
+           softmax_scale=None, stream=None):
+    """Step 3 of a chunk: attention over the selected pages and the causal chunk."""
+    D = problem.c.head_dim
+    softmax_scale = 1.0 / math.sqrt(D) if softmax_scale is None else softmax_scale
     X.bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, bufs.sel_page, bufs.n_sel,
                           softmax_scale, bufs.workspace, o, lse, stream)
+
+
+def prefill_chunk(problem, q, k_cur, v_cur, k_pool, v_pool, tau, bufs: ChunkBuffers, o, lse,
+                  est_scale=None, softmax_scale=None, stream=None):
+    """One chunk of XAttention BSA prefill: estimate, select, attend."""
+    estimate_select(problem, q, k_cur, k_pool, tau, bufs, est_scale, stream)
+    attend(problem, q, k_cur, v_cur, k_pool, v_pool, bufs, o, lse, softmax_scale, stream)
 
 
 class SequencePrefill:
@@ -101,7 +115,7 @@ class SequencePrefill:
         chunks 1, 2, ...; chunk 0 runs while the pools are still coming in.
 
         store_kv=True: the pools are built on the device.  Only Q, K, V cross
-        from the host, chunk by chunk; before chunk c runs, xattn_store_kv
+        from the host, chunk by chunk; before chunk c's attention, xattn_store_kv
         writes its K and V into the pages the block table gives their positions
         ("Task Plan: Layerwise Offload Refactoring", Phase 1.2), which is the
         history chunk c + 1 reads.  With a block table that maps every position
@@ -121,13 +135,18 @@ class SequencePrefill:
         n = len(self.problems)
         ready = []
 
+        ready_v = []
+
         def chunk_inputs(c):
+            # Q and K first (all the estimate reads), then V (read by the
+            # attention): a chunk's estimate starts one third of a copy sooner
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             for name in ("q", "k", "v"):  # one 2-D copy each: a row per head
                 X.copy_window_async(dev[name], host[name], t0, t1, h2d_stream)
-            ev = torch.cuda.Event()
-            ev.record(h2d_stream)
-            ready.append(ev)
+                if name != "q":
+                    ev = torch.cuda.Event()
+                    ev.record(h2d_stream)
+                    (ready if name == "k" else ready_v).append(ev)
 
         with torch.cuda.stream(h2d_stream):
             chunk_inputs(0)
@@ -138,12 +157,15 @@ class SequencePrefill:
                 chunk_inputs(c)
         for c in range(n):
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
+            p = self.problems[c]
+            q, k, v = dev["q"][:, t0:], dev["k"][:, t0:], dev["v"][:, t0:]
             stream.wait_event(ready[c])
-            if store_kv:
-                X.xattn_store_kv(self.problems[c], dev["k"][:, t0:], dev["v"][:, t0:],
-                                 dev["kpool"], dev["vpool"], stream)
-            self.run_chunk(c, dev["q"], dev["k"], dev["v"], dev["kpool"], dev["vpool"], tau,
-                           dev["o"], dev["lse"], stream)
+            estimate_select(p, q, k, dev["kpool"], tau, self.bufs, stream=stream)
+            stream.wait_event(ready_v[c])
+            if store_kv:  # the history of chunk c + 1, before anything reads it
+                X.xattn_store_kv(p, k, v, dev["kpool"], dev["vpool"], stream)
+            attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, dev["o"][:, t0:],
+                   dev["lse"][:, t0:], stream=stream)
             done = torch.cuda.Event()
             done.record(stream)
             d2h_stream.wait_event(done)
