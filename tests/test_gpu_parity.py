@@ -353,3 +353,52 @@ def test_prefill_from_host_with_kv_store_matches_prefilled_pool():
     assert np.array_equal(host["lse"].numpy(), L_dev)
     assert torch.equal(devb["kpool"].view(torch.int16), case.KP.view(torch.int16))
     assert torch.equal(devb["vpool"].view(torch.int16), case.VP.view(torch.int16))
+
+
+@pytest.mark.parametrize("H,Hkv,D,Bk,S", [(3, 1, 128, 128, 8), (2, 2, 64, 64, 8),
+                                           (5, 5, 128, 128, 16)])
+def test_odd_group_sizes_full_path(H, Hkv, D, Bk, S):
+    """Query heads per KV head odd (3 and 1): the score GEMM takes its
+    one-CTA-per-tile form (sibling heads pair up only for even groups).  One
+    chunk with history in a permuted pool: every block sum of every head
+    against the oracle, the selection against the oracle on the GPU's block
+    sums, sampled attention rows against the oracle."""
+    d = dev()
+    rng = np.random.default_rng(500 + H * 10 + Hkv)
+    lq, kh = 4 * Bk, 6 * Bk
+    P = kh // Bk + 3
+    q = I.bf16_round(rng.standard_normal((H, lq, D), dtype=np.float32))
+    kc = I.bf16_round(rng.standard_normal((Hkv, lq, D), dtype=np.float32))
+    vc = I.bf16_round(rng.standard_normal((Hkv, lq, D), dtype=np.float32))
+    kp32 = rng.standard_normal((P, Bk, Hkv, D), dtype=np.float32)
+    kp32[2, 5] *= 4.0  # a few peaked keys so the selection keeps part of the history
+    kp32[4, 17] *= 4.0
+    kp = I.bf16_round(kp32)
+    vp = I.bf16_round(rng.standard_normal((P, Bk, Hkv, D), dtype=np.float32))
+    bt = rng.permutation(P).astype(np.int32)[None, : kh // Bk].copy()
+    prob = X.Problem(H, Hkv, D, S, Bk, [lq], [kh], torch.from_numpy(bt).to(d), P)
+    bufs = RN.ChunkBuffers.for_problems([prob], d, with_mask=True)
+    O_ = torch.empty((H, lq, D), dtype=torch.bfloat16, device=d)
+    LSE = torch.empty((H, lq), dtype=torch.float32, device=d)
+    tau = 0.9
+    RN.prefill_chunk(prob, to_dev_bf16(q), to_dev_bf16(kc), to_dev_bf16(vc), to_dev_bf16(kp),
+                     to_dev_bf16(vp), tau, bufs, O_, LSE)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    f64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    qd, kcd, vcd, kpd, vpd = f64(q), f64(kc), f64(vc), f64(kp), f64(vp)
+    kbh, qb = kh // Bk, lq // Bk
+    bs = bufs.block_sums[: H * qb * (kbh + qb)].cpu().numpy().reshape(H, qb, kbh + qb)
+    ref = O.estimate_request(qd, kcd, kpd, bt[0], kh, H, Hkv, S, Bk,
+                             O.default_estimation_scale(D, S))
+    check_block_sums(bs, ref, Bk // S, f"H={H} Hkv={Hkv}")
+    mk = bufs.mask[: bs.size].cpu().numpy().reshape(bs.shape)
+    sel, pages = check_selection(bs, mk, bufs.sel_idx[0].cpu().numpy(),
+                                 bufs.sel_page[0].cpu().numpy(), int(bufs.n_sel[0].item()), tau,
+                                 Hkv, kbh, bt[0], f"H={H} Hkv={Hkv}")
+    rows = sorted({0, Bk - 1, Bk, lq - 1, *rng.integers(0, lq, 10).tolist()})
+    o_ref, l_ref = O.attend_request(qd, kcd, vcd, kpd, vpd, pages, H, Hkv, 1 / math.sqrt(D),
+                                    rows=rows)
+    idx = np.asarray(rows)
+    check_attention(O_.float().cpu().numpy()[:, idx], LSE.cpu().numpy()[:, idx], o_ref, l_ref,
+                    f"H={H} Hkv={Hkv}")
