@@ -49,6 +49,19 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate_over_ranks(t_local_s, tokens_local, device, dist_mod=None):
+    """Whole-job figures of N replicas: the slowest rank's timed seconds (MAX)
+    and the tokens all ranks processed (SUM).  One process returns its own."""
+    if dist_mod is None or not dist_mod.is_initialized() or dist_mod.get_world_size() == 1:
+        return float(t_local_s), float(tokens_local)
+    import torch
+    t = torch.tensor([float(t_local_s)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens_local)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    dist_mod.all_reduce(n, op=dist_mod.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def workload_desc(name, tau):
     from xattention_block_sparse_gb300 import inputs as I
     c = I.CONFIGS[name]
@@ -253,11 +266,8 @@ def run_ours(args, ws, rank, local):
             att_ms += d
         step_ms.append(events[s][0][0].elapsed_time(events[s][nchunk - 1][3]))
     ms = float(np.mean(step_ms))
-    t_max = sum(step_ms) / 1e3
-    if ws > 1:
-        t = torch.tensor([t_max], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max, tokens = aggregate_over_ranks(sum(step_ms) / 1e3, L * args.steps, dev,
+                                         dist if ws > 1 else None)
 
     work = [chunk_work(cfg, c, chunk, n_sel[c]) for c in range(nchunk)]
     K_ = args.steps
@@ -270,7 +280,6 @@ def run_ours(args, ws, rank, local):
     est_tflops = (f_est / nchunk) / ((est_ms / (K_ * nchunk)) * 1e-3) / 1e12
     stage = {"estimate_ms_per_step": est_ms / K_, "select_ms_per_step": sel_ms / K_,
              "attention_ms_per_step": att_ms / K_}
-    tokens = L * ws * K_
     value = tokens / t_max
 
     # roofline of the step: algorithmic time at peak over measured time
