@@ -325,8 +325,9 @@ def run_ours(args, ws, rank, local):
         "n_sel_per_chunk": n_sel,
         "clocks": clocks,
         "e2e": e2e,
-        # per chunk: gather, score GEMM, stat merge, block sum, select, vote, attention
-        "gpu_launches": 7 * nchunk * K_,
+        # per chunk, this library's kernels: score GEMM, block sum, select (+ vote),
+        # attention; plus two cudaMemsetAsync of counters (not counted)
+        "gpu_launches": 4 * nchunk * K_,
         "wall_s_timed": wall,
     }
     if rank == 0:

@@ -111,8 +111,9 @@ typedef struct xattn_problem {
 /* Bytes of scratch the caller must provide to xattn_estimate, xattn_select and
  * bsa_chunk_attention for this problem (0 on invalid problems).  The workspace
  * holds the estimation's per-(reshaped row, KV block) partial sums and
- * per-tile softmax statistics, the gathered keys, the vote counters and the
- * attention's partial results; its contents between calls are unspecified. */
+ * per-tile softmax statistics, the selection's vote counters (and the counter
+ * that tells its last CTA to run the vote) and the attention's partial
+ * results; its contents between calls are unspecified. */
 size_t xattn_workspace_size(const xattn_problem *p);
 
 /* Number of fp32 elements of block_sums (and bytes of the optional mask):

@@ -68,7 +68,8 @@ def test_workspace_and_block_sum_sizes(lib):
     tstat = H * rq * (ncol // 128) * 8
     al = lambda x: (x + 255) // 256 * 256
     counts = al(al(bpart) + tstat)
-    part_o = al(counts + 512 * 4)        # attention partials: 160 CTAs x 2 slots x 256 rows
+    part_o = al(counts + (512 + 1) * 4)  # vote counters + finishing counter; then attention
+                                         # partials: 160 CTAs x 2 slots x 256 rows
     part_lse = al(part_o + 160 * 2 * 256 * 128 * 4)
     att_cnt = al(part_lse + 160 * 2 * 256 * 4)
     expect = al(att_cnt + 16 * 16 * 2 * 4)  # two part counters per 256-row attention unit

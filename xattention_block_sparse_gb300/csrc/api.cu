@@ -122,7 +122,8 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   w.counts = align_up(w.tstat + tstat * sizeof(float2));
   // attention partial results: two slots of kAttnRows rows per persistent CTA
   const size_t part_rows = (size_t)kAttnMaxCtas * 2 * kAttnRows;
-  w.part_o = align_up(w.counts + (size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) *
+  // vote counters of every request, then the select kernel's finishing counter
+  w.part_o = align_up(w.counts + ((size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) + 1) *
                                      sizeof(int32_t));
   w.part_lse = align_up(w.part_o + part_rows * D * sizeof(float));
   w.att_cnt = align_up(w.part_lse + part_rows * sizeof(float));
@@ -164,7 +165,8 @@ inline xattn_status cu(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XAT
 
 // Vote counters of xattn_select_noalloc: a fixed array the library owns, for
 // callers that cannot hand it any scratch.  Shared by every call on a device.
-static __device__ __align__(256) int32_t xattn_noalloc_counters[XATTN_NOALLOC_MAX_COUNTERS];
+// (one more than the documented limit: the select kernel's finishing counter)
+static __device__ __align__(256) int32_t xattn_noalloc_counters[XATTN_NOALLOC_MAX_COUNTERS + 1];
 
 namespace xattn {
 namespace {
@@ -259,12 +261,10 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
   if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + pl.ws.counts);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  s = cu(cudaMemsetAsync(counts, 0, (size_t)pl.geo.B * p->bt_stride * sizeof(int32_t), st));
+  s = cu(cudaMemsetAsync(counts, 0, ((size_t)pl.geo.B * p->bt_stride + 1) * sizeof(int32_t), st));
   if (s != XATTN_OK) return s;
-  s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
-  if (s != XATTN_OK) return s;
-  return cu(launch_vote(pl.geo, counts, vote_num, vote_den, force_sink_last, sel_idx, sel_page,
-                        n_sel, st));
+  return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
+                          vote_num, vote_den, force_sink_last, sel_idx, sel_page, n_sel, st));
 }
 
 xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
@@ -286,12 +286,10 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
   if ((s = noalloc_counters(&counts)) != XATTN_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the array keeps the previous call's votes: clear the part this call uses
-  s = cu(cudaMemsetAsync(counts, 0, n_counters * sizeof(int32_t), st));
+  s = cu(cudaMemsetAsync(counts, 0, (n_counters + 1) * sizeof(int32_t), st));
   if (s != XATTN_OK) return s;
-  s = cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts, st));
-  if (s != XATTN_OK) return s;
-  return cu(launch_vote(pl.geo, counts, vote_num, vote_den, force_sink_last, sel_idx, sel_page,
-                        n_sel, st));
+  return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
+                          vote_num, vote_den, force_sink_last, sel_idx, sel_page, n_sel, st));
 }
 
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,

@@ -75,11 +75,13 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
                               float *bpart, float2 *tstat, cudaStream_t st);
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
                              float *block_sums, cudaStream_t st);
+// Threshold selection of every (request, KV head, query block), then the GQA
+// vote of every request (run by the CTA that finishes last; counts must hold
+// B * bt_stride + 1 zeroed int32: the vote counters and the finishing counter).
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
-                          double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st);
-cudaError_t launch_vote(const Geo &g, const int32_t *counts, int vote_num, int vote_den,
-                        int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
-                        int32_t *n_sel, cudaStream_t st);
+                          double threshold, uint8_t *mask, int32_t *counts, int vote_num,
+                          int vote_den, int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
+                          int32_t *n_sel, cudaStream_t st);
 cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
                              const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,

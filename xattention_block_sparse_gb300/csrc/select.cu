@@ -11,9 +11,11 @@
 //                  group's rows at once, no barrier in the loop; longer rows
 //                  go through a bitonic sort and a prefix scan.  The group's
 //                  "any" over its heads then votes once per history block.
-//   vote_kernel    one CTA per request: vote test votes*den > num*Hkv*Qb ((1, 2):
-//                  strict majority), sink and last history block forced (when
-//                  asked), ascending compaction, page lookup.
+//                  The CTA that finishes last (a counter) runs the vote of every
+//                  request: test votes*den > num*Hkv*Qb ((1, 2): strict
+//                  majority), sink and last history block forced (when asked),
+//                  ascending compaction, page lookup.
+//   vote_kernel    the same vote alone, for a call with no query rows.
 //
 // Every step is integer or exactly rounded, so the result does not depend on
 // the order in which threads add or compare.
@@ -57,10 +59,52 @@ __device__ unsigned long long block_excl_scan(unsigned long long v, unsigned lon
   return res;
 }
 
+// The vote of request r by the whole CTA (STHR threads): keep history block j
+// when votes_j * den > num * Hkv * Qb, or when forced (sink / last block);
+// ascending compaction into sel_idx, page lookup into sel_page, count in n_sel.
+__device__ void vote_request(const Geo &g, int r, const int32_t *counts, int vote_num,
+                             int vote_den, int force, int32_t *sel_idx, int32_t *sel_page,
+                             int32_t *n_sel, unsigned long long *wbuf) {
+  const ReqDesc &R = g.req[r];
+  const int kbh = R.kh / g.Bk, Qb = R.lq / g.Bk;
+  const int64_t votes_total = (int64_t)g.Hkv * Qb;
+  const int tid = threadIdx.x;
+  const int per = (kbh + STHR - 1) / STHR;
+  const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
+  const int32_t *cnt = counts + (int64_t)r * g.bt_stride;
+  auto keep = [&](int j) {
+    return (int64_t)__ldcg(cnt + j) * vote_den > (int64_t)vote_num * votes_total ||
+           (force && (j == 0 || j == kbh - 1));
+  };
+  unsigned long long mine = 0;
+  for (int j = beg; j < end; ++j) mine += keep(j) ? 1 : 0;
+  unsigned long long total;
+  unsigned long long pos = block_excl_scan(mine, wbuf, &total);
+  for (int j = beg; j < end; ++j) {
+    if (keep(j)) {
+      const int64_t o = (int64_t)r * g.bt_stride + (int64_t)pos;
+      sel_idx[o] = j;
+      int p = g.block_table[(int64_t)r * g.bt_stride + j];
+      if (p < 0 || p >= g.num_pages) {
+        record_error(g.err, XATTN_EPAGE);
+        p = -1;
+      }
+      sel_page[o] = p;
+      ++pos;
+    }
+  }
+  if (tid == 0) n_sel[r] = (int32_t)total;
+}
+
 __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Geo g,
                                                       const float *__restrict__ bs, double tau,
                                                       uint8_t *__restrict__ mask,
-                                                      int32_t *__restrict__ counts, int nkeys) {
+                                                      int32_t *__restrict__ counts, int nkeys,
+                                                      int vote_num, int vote_den, int force,
+                                                      int32_t *__restrict__ sel_idx,
+                                                      int32_t *__restrict__ sel_page,
+                                                      int32_t *__restrict__ n_sel,
+                                                      int32_t *__restrict__ done) {
   extern __shared__ __align__(16) uint8_t sel_smem[];  // any-flags [npad], then keys
   __shared__ unsigned long long wbuf[SWARPS + 1];
   const int cta = blockIdx.x;
@@ -188,54 +232,40 @@ __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Ge
   }
   for (int j = tid; j < kbh; j += STHR)
     if (anyf[j]) atomicAdd(counts + (int64_t)r * g.bt_stride + j, 1);
+
+  // the CTA that finishes last has every vote counted: it runs the votes
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int rr = 0; rr < g.B; ++rr)
+    vote_request(g, rr, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
 }
 
-constexpr int VTHR = 512;
-
-__global__ void __launch_bounds__(VTHR) vote_kernel(const __grid_constant__ Geo g,
+__global__ void __launch_bounds__(STHR) vote_kernel(const __grid_constant__ Geo g,
                                                     const int32_t *__restrict__ counts,
                                                     int vote_num, int vote_den, int force,
                                                     int32_t *__restrict__ sel_idx,
                                                     int32_t *__restrict__ sel_page,
                                                     int32_t *__restrict__ n_sel) {
   __shared__ unsigned long long wbuf[SWARPS + 1];
-  const int r = blockIdx.x;
-  const ReqDesc &R = g.req[r];
-  const int kbh = R.kh / g.Bk, Qb = R.lq / g.Bk;
-  const int64_t votes_total = (int64_t)g.Hkv * Qb;
-  const int tid = threadIdx.x;
-  const int per = (kbh + VTHR - 1) / VTHR;
-  const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
-  const int32_t *cnt = counts + (int64_t)r * g.bt_stride;
-  auto keep = [&](int j) {
-    return (int64_t)cnt[j] * vote_den > (int64_t)vote_num * votes_total ||
-           (force && (j == 0 || j == kbh - 1));
-  };
-  unsigned long long mine = 0;
-  for (int j = beg; j < end; ++j) mine += keep(j) ? 1 : 0;
-  unsigned long long total;
-  unsigned long long pos = block_excl_scan(mine, wbuf, &total);
-  for (int j = beg; j < end; ++j) {
-    if (keep(j)) {
-      const int64_t o = (int64_t)r * g.bt_stride + (int64_t)pos;
-      sel_idx[o] = j;
-      int p = g.block_table[(int64_t)r * g.bt_stride + j];
-      if (p < 0 || p >= g.num_pages) {
-        record_error(g.err, XATTN_EPAGE);
-        p = -1;
-      }
-      sel_page[o] = p;
-      ++pos;
-    }
-  }
-  if (tid == 0) n_sel[r] = (int32_t)total;
+  vote_request(g, blockIdx.x, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
-                          double threshold, uint8_t *mask, int32_t *counts, cudaStream_t st) {
-  if (nctas == 0) return cudaSuccess;
+                          double threshold, uint8_t *mask, int32_t *counts, int vote_num,
+                          int vote_den, int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
+                          int32_t *n_sel, cudaStream_t st) {
+  if (nctas == 0) {  // no query rows: the vote alone (every count is zero)
+    vote_kernel<<<g.B, STHR, 0, st>>>(g, counts, vote_num, vote_den, force_sink_last, sel_idx,
+                                      sel_page, n_sel);
+    return cudaGetLastError();
+  }
   int npad = 1;
   while (npad < max_kb) npad <<= 1;
   const int G = g.H / g.Hkv;
@@ -249,15 +279,11 @@ cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *bloc
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts, (int)nkeys);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_vote(const Geo &g, const int32_t *counts, int vote_num, int vote_den,
-                        int force_sink_last, int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
-                        cudaStream_t st) {
-  vote_kernel<<<g.B, VTHR, 0, st>>>(g, counts, vote_num, vote_den, force_sink_last, sel_idx,
-                                    sel_page, n_sel);
+  // the finishing counter sits right after the vote counters (zeroed with them)
+  int32_t *done = counts + (size_t)g.B * (size_t)g.bt_stride;
+  select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts, (int)nkeys,
+                                           vote_num, vote_den, force_sink_last, sel_idx,
+                                           sel_page, n_sel, done);
   return cudaGetLastError();
 }
 
