@@ -22,6 +22,8 @@
 //                     group: their key tiles are identical, so each CTA loads
 //                     half of the key boxes and multicasts them to both, which
 //                     halves the TMA box count that limits this kernel.
+//                     A launch's last wave, when it would fill at most half of
+//                     the SMs, runs its tiles as 256 x 128 halves instead.
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
 //                  next tile while the epilogue drains TMEM); lane q issues
 //                  key box q of each k-step (of this CTA's half in a pair)
@@ -72,7 +74,8 @@ struct Maps {
 };
 
 struct Tile {
-  int r, h, m0, n0;
+  int r, h, m0, n0;  // n0: first reshaped column of the work item
+  int w;             // its columns: COLS, or 128 for half of a tile of the last wave
 };
 
 // Tile t of the score GEMM: requests in order, then head, then row tile, then
@@ -111,10 +114,28 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t, int rank) {
   return tl;
 }
 
+// Work item w of the launch: tiles 0..nfull-1 whole, then the remaining tiles
+// as two 128-column halves each (the launch's last wave, so that it spreads
+// over as many SMs as it can fill).
+template <bool PAIR>
+__device__ __forceinline__ Tile decode_work(const Geo &g, int w, int nfull, int rank) {
+  if (w < nfull) {
+    Tile tl = decode_tile<PAIR>(g, w, rank);
+    tl.w = COLS;
+    return tl;
+  }
+  const int hh = w - nfull;
+  Tile tl = decode_tile<PAIR>(g, nfull + hh / 2, rank);
+  tl.n0 += (hh & 1) * (COLS / 2);
+  tl.w = COLS / 2;
+  return tl;
+}
+
 template <int BR, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
-    score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int ntiles,
-                      float scale, float *__restrict__ bpart, float2 *__restrict__ tstat) {
+    score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int nwork,
+                      int nfull, float scale, float *__restrict__ bpart,
+                      float2 *__restrict__ tstat) {
   constexpr int NB = kTileCols / BR;  // KV blocks per statistics tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -153,11 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    constexpr int NSUB = COLS / BR;             // key boxes per k-step
-    constexpr int NOWN = PAIR ? NSUB / 2 : NSUB;  // boxes this CTA issues (PAIR: to both CTAs)
     constexpr int SUB_BYTES = BR * KSTEP * 2;   // Br rows of 128 B (a multiple of 1024)
-    static_assert(NSUB <= 32 && SUB_BYTES % 1024 == 0, "key boxes");
-    const int box = rank * NOWN + lane;         // the key box this lane issues
+    static_assert(COLS / BR <= 32 && SUB_BYTES % 1024 == 0, "key boxes");
     if (lane == 0) {
       tma_prefetch_desc(&mp.q);
       tma_prefetch_desc(&mp.kp);
@@ -165,16 +183,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int it = 0;  // k-steps issued so far (ring position)
     bool ok = true;
-    for (int t = tile0; ok && t < ntiles; t += tstep) {
-      const Tile tl = decode_tile<PAIR>(g, t, rank);
+    for (int t = tile0; ok && t < nwork; t += tstep) {
+      const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
       const ReqDesc &R = g.req[tl.r];
       const int kvh = tl.h / (g.H / g.Hkv);
+      const int nsub = tl.w / BR;                 // key boxes per k-step
+      const int nown = PAIR ? nsub / 2 : nsub;    // boxes this CTA issues (PAIR: to both CTAs)
+      const int box = rank * nown + lane;         // the key box this lane issues
       const int ch = R.kh / S, ncol = (R.kh + R.lq) / S;
       // this lane's key box: reshaped columns [b, b + Br) are one history page
       // (its block-table entry) or Br groups of the current chunk
       bool hist = false;
       int src = R.q0 / S;  // columns past the last one: any in-bounds box (masked)
-      if (lane < NOWN) {
+      if (lane < nown) {
         const int b = tl.n0 + box * BR;
         if (b < ch) {
           hist = true;
@@ -197,12 +218,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int i = kk / D, dc = kk % D;
         uint8_t *sA = smem + s * STAGE;
         if (lane == 0) {
-          mbar_expect_tx(&bar.full[s], STAGE);
+          mbar_expect_tx(&bar.full[s], A_BYTES + tl.w * KSTEP * 2);
           // q rows S*a + S-1-i of this tile
           tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
         }
         __syncwarp();
-        if (lane < NOWN) {  // key rows S*b + i
+        if (lane < nown) {  // key rows S*b + i
           uint8_t *dst = sA + A_BYTES + box * SUB_BYTES;
           if (PAIR) {
             if (hist)
@@ -228,13 +249,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(TM, COLS, 0, 0);
+      constexpr uint32_t idesc_w = idesc_bf16(TM, COLS, 0, 0), idesc_h = idesc_bf16(TM, COLS / 2, 0, 0);
       // descriptors are built once and advanced by byte offset / 16
       const uint64_t d0 = sdesc_sw128(smem_addr(smem), 16, 1024);
       int it = 0, n = 0;
       bool ok = true;
-      for (int t = tile0; ok && t < ntiles; t += tstep, ++n) {
-        const Tile tl = decode_tile<PAIR>(g, t, rank);
+      for (int t = tile0; ok && t < nwork; t += tstep, ++n) {
+        const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
+        const uint32_t idesc = tl.w == COLS ? idesc_w : idesc_h;
         const int rq = g.req[tl.r].lq / S;
         const bool two_m = tl.m0 + TM < rq;
         // the epilogue has drained the previous tile's accumulators
@@ -279,10 +301,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row = tid - 128 - x * TM;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + x * COLS;
     int n = 0;
-    for (int t = tile0; t < ntiles; t += tstep, ++n) {
-      const Tile tl = decode_tile<PAIR>(g, t, rank);
+    for (int t = tile0; t < nwork; t += tstep, ++n) {
+      const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
       const ReqDesc &R = g.req[tl.r];
       const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+      const int nj = tl.w / kTileCols;  // statistics tiles of the work item
       const int ntile = (ncol + kTileCols - 1) / kTileCols;
       const bool two_m = tl.m0 + TM < rq;
       const int a = tl.m0 + x * TM + row;
@@ -296,7 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        ((int64_t)(tl.h * Qb + (row_ok ? a : 0) / BR) * Kb) * BR +
                        (row_ok ? a : 0) % BR;
 #pragma unroll 1
-        for (int j = 0; j < COLS / kTileCols; ++j) {
+        for (int j = 0; j < nj; ++j) {
           const int c0 = tl.n0 + j * kTileCols;  // first column of this statistics tile
           uint32_t v[kTileCols];
 #pragma unroll
@@ -304,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(lane_addr + j * kTileCols + c * 32,
                       *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
           tmem_ld_wait();
-          if (j == COLS / kTileCols - 1) {
+          if (j == nj - 1) {
             // all of this tile's accumulators are in registers: release TMEM
             tc_fence_before();
             __syncwarp();
@@ -419,9 +442,14 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
       units = ntiles / 2;  // head pairs
       slots = ncl;
     }
-    const int n = units < slots ? units : slots;
+    // A last wave that fills at most half of the slots runs as half-width tiles
+    // (twice as many, each half the time).
+    const int rem = units % slots;
+    const int nfull = (rem > 0 && 2 * rem <= slots) ? units - rem : units;
+    const int nwork = nfull + 2 * (units - nfull);
+    const int n = nwork < slots ? nwork : slots;
     cfg.gridDim = dim3(pair ? 2 * n : n);
-    e = cudaLaunchKernelEx(&cfg, kernel, g, mp, units, scale, bpart, tstat);
+    e = cudaLaunchKernelEx(&cfg, kernel, g, mp, nwork, nfull, scale, bpart, tstat);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
