@@ -19,7 +19,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   Geo geo;
-  int gemm_ctas = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0;
+  int gemm_tiles = 0, bsum_ctas = 0, sel_ctas = 0, att_ctas = 0;
   int max_kb = 0;
   size_t bs_count = 0;
   WsLayout ws{};
@@ -111,7 +111,7 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     return XATTN_EINVAL;
   if (p->q_head_stride % 8 || p->kv_head_stride % 8) return XATTN_EALIGN;
 
-  pl.gemm_ctas = (int)gemm;
+  pl.gemm_tiles = (int)gemm;
   pl.bsum_ctas = (int)bsum;
   pl.sel_ctas = (int)sel;
   pl.att_ctas = (int)att;
@@ -236,7 +236,7 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
   float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
   float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  s = cu(launch_score_gemm(pl.geo, pl.gemm_ctas, static_cast<const __nv_bfloat16 *>(q),
+  s = cu(launch_score_gemm(pl.geo, pl.gemm_tiles, static_cast<const __nv_bfloat16 *>(q),
                            static_cast<const __nv_bfloat16 *>(k_cur),
                            static_cast<const __nv_bfloat16 *>(k_pool), scale, bpart, tstat, st));
   if (s != XATTN_OK) return s;
