@@ -15,7 +15,9 @@
  *                        (non-causal) and the current chunk (causal), merged
  *                        by log-sum-exp, with the output's LSE
  *
- * and lse_merge, the stand-alone merge of two partial attention results.
+ * and lse_merge, the stand-alone merge of two partial attention results;
+ * xattn_store_kv, which writes a chunk's keys and values into the pool pages
+ * its positions map to (the history of the request's next chunk).
  *
  * Sources: "XAttention BSA Policy 设计文档" (nano-vllm
  * docs/xattn_bsa_policy_design.md), sections 核心算法 1 select_blocks (Steps 1-4)
@@ -23,7 +25,8 @@
  * Fix" (docs/xattn_offload_stream_sync_fix.md), section 技术细节 (three-stage
  * KV chunking, stream configuration); "Atenção paginada" (transformers docs
  * paged_attention.md), Caminho Varlen / Caminho de decodificação (cu_seq_lens,
- * block_table).
+ * block_table); "Task Plan: Layerwise Offload Refactoring" (task_plan.md),
+ * Phase 1.2 (per-block KV store).
  *
  * Conventions common to every entry point
  * ---------------------------------------
