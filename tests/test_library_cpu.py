@@ -154,3 +154,25 @@ def test_entry_point_argument_errors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(FileNotFoundError):
         X.load_library(str(tmp_path / "nope.so"))
+
+
+def test_sequence_prefill_chunk_problems(lib):
+    """SequencePrefill's per-chunk problems on the host: chunk c queries tokens
+    [c*chunk, (c+1)*chunk) with c*chunk history tokens, heads strided over the
+    whole sequence, and one set of buffers sized for the largest chunk (the
+    last, whose history is longest)."""
+    import torch
+    from xattention_block_sparse_gb300 import runner as RN
+    H, Hkv, D, S, Bk, L, chunk = 16, 8, 128, 8, 128, 32768, 4096
+    bt = torch.arange(L // Bk, dtype=torch.int32)[None, :]
+    seq = RN.SequencePrefill(H, Hkv, D, S, Bk, L, chunk, bt, L // Bk)
+    assert len(seq.problems) == L // chunk
+    for c, p in enumerate(seq.problems):
+        assert (p.B, p.bt_stride) == (1, L // Bk)
+        assert (p.c.q_head_stride, p.c.kv_head_stride, p.c.lse_head_stride) == (L * D, L * D, L)
+        assert (p.q_lens, p.kh_lens) == ([chunk], [c * chunk])
+    sizes = [X.xattn_workspace_size(p) for p in seq.problems]
+    assert sizes == sorted(sizes) and sizes[0] > 0
+    assert seq.bufs.workspace.numel() == sizes[-1]
+    assert seq.bufs.block_sums.numel() == X.xattn_block_sums_count(seq.problems[-1])
+    assert tuple(seq.bufs.sel_page.shape) == (1, L // Bk) and seq.bufs.mask is None
