@@ -15,7 +15,8 @@ Sources (page title, then section):
          (nano-vllm docs/xattn_offload_stream_sync_fix.md)
          -- 技术细节 "三阶段 KV Chunking 流程", 测试结果
   [PLAN] "Task Plan: Layerwise Offload Refactoring" (nano-vllm task_plan.md)
-         -- Phase 1.1 ring buffer layout, Phase 4 ring-buffer schedule
+         -- Phase 1.1 ring buffer layout, Phase 1.2 per-block KV store,
+            Phase 4 ring-buffer schedule
   [PAGED] "Atenção paginada" (transformers docs paged_attention.md)
          -- Caminho Varlen "Mecanismo de indexação"/"Exemplo",
             Caminho de decodificação "Exemplo"
@@ -89,6 +90,24 @@ def gather_history(pool, block_table_row, n_tokens: int, kvh: int) -> np.ndarray
         p, off = paged_location([block_table_row], 0, t, page_size)
         rows[t] = pool[p, off, kvh]
     return rows
+
+
+def store_chunk(pool, block_table_row, kh_len: int, chunk_kv) -> np.ndarray:
+    """The pool after a chunk's keys (or values) are stored ([PLAN] Phase 1.2,
+    offload_layer_kv_async: a prefill's K/V go block by block into the cache
+    blocks named by its block ids).  chunk_kv [Hkv, n, D] holds tokens at
+    positions kh_len .. kh_len + n - 1 of the request; each lands at the
+    [PAGED] location of its position.  A position whose page is unallocated
+    (-1) is left out.  pool: [pages, page_size, Hkv, D]; returns a copy."""
+    out = np.array(pool, copy=True)
+    page_size = pool.shape[1]
+    for t in range(chunk_kv.shape[1]):
+        try:
+            p, off = paged_location([block_table_row], 0, kh_len + t, page_size)
+        except IndexError:
+            continue
+        out[p, off] = chunk_kv[:, t]
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -286,10 +286,10 @@ def test_prefill_from_host_matches_device_resident_run():
 
 @pytest.mark.parametrize("Hkv,D,Bk", [(8, 128, 128), (1, 64, 64)])
 def test_store_kv_writes_each_chunk_block_to_its_page(Hkv, D, Bk):
-    """xattn_store_kv on a two-request varlen chunk: every chunk block lands,
-    bit for bit, on the page its position names in the block table; history
-    pages and pages no block names keep their contents; a -1 entry records
-    XATTN_EPAGE and leaves that block unwritten."""
+    """xattn_store_kv on a two-request varlen chunk equals the oracle's store
+    bit for bit: every chunk block lands on the page its position names in the
+    block table; history pages and pages no block names keep their contents; a
+    -1 entry records XATTN_EPAGE and leaves that block unwritten."""
     d = dev()
     rng = np.random.default_rng(7 + D)
     q_lens, kh_lens = [2 * Bk, 3 * Bk], [Bk, 0]
@@ -311,17 +311,13 @@ def test_store_kv_writes_each_chunk_block_to_its_page(Hkv, D, Bk):
     X.xattn_store_kv(prob, KC, VC, KP, VP)
     torch.cuda.synchronize()
     assert X.xattn_last_device_error() == -3  # XATTN_EPAGE
-    want_k, want_v = kp.copy(), vp.copy()
+    want_k, want_v = kp, vp
     q0 = 0
-    for r in range(2):
-        for j in range(q_lens[r] // Bk):
-            page = bt[r, kh_lens[r] // Bk + j]
-            if page < 0:
-                continue
-            toks = slice(q0 + j * Bk, q0 + (j + 1) * Bk)
-            want_k[page] = kc[:, toks].transpose(1, 0, 2)
-            want_v[page] = vc[:, toks].transpose(1, 0, 2)
-        q0 += q_lens[r]
+    for r in range(2):  # the oracle's store, request after request
+        q1 = q0 + q_lens[r]
+        want_k = O.store_chunk(want_k, bt[r], kh_lens[r], kc[:, q0:q1])
+        want_v = O.store_chunk(want_v, bt[r], kh_lens[r], vc[:, q0:q1])
+        q0 = q1
     got_k = KP.view(torch.int16).cpu().numpy().view(np.uint16)
     got_v = VP.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got_k, want_k)

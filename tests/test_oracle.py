@@ -485,3 +485,29 @@ def test_planted_mistakes_are_caught(monkeypatch):
                                    include_current=False)
     assert np.isfinite(s_nomask).all() and not np.isfinite(
         O.estimation_scores(q, kh, kc, S, 0.37)).all()
+
+
+def test_store_chunk_builds_the_sequence_pool():
+    """Storing every chunk of a sequence, in order, into an empty pool gives the
+    pool the input recipe lays out directly (logical page j of the sequence on
+    physical page perm[j]): two independent statements of the same placement."""
+    from xattention_block_sparse_gb300 import inputs as I
+    rng = np.random.default_rng(11)
+    Hkv, L, D, Bk, chunk = 2, 512, 8, 64, 128
+    kv = rng.integers(1, 1 << 15, size=(Hkv, L, D)).astype(np.uint16)
+    P = L // Bk + 2
+    perm = rng.permutation(P).astype(np.int32)
+    want = I._pages_from_seq(kv, Bk, perm, P)
+    pool = np.zeros_like(want)
+    for c in range(L // chunk):
+        pool = O.store_chunk(pool, perm, c * chunk, kv[:, c * chunk:(c + 1) * chunk])
+    assert np.array_equal(pool, want)
+
+
+def test_store_chunk_skips_unallocated_pages():
+    Hkv, D, Bk = 1, 4, 64
+    pool = np.full((3, Bk, Hkv, D), 7.0)
+    kv = np.arange(Hkv * 2 * Bk * D, dtype=np.float64).reshape(Hkv, 2 * Bk, D)
+    out = O.store_chunk(pool, np.array([2, -1, 0]), Bk, kv)  # positions 64..191
+    assert np.array_equal(out[0], kv[:, Bk:].transpose(1, 0, 2))   # block 2 -> page 0
+    assert (out[1] == 7.0).all() and (out[2] == 7.0).all()         # block 1 is -1: skipped
