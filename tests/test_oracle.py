@@ -93,6 +93,7 @@ def test_ring_buffer_arithmetic_and_schedule():
             assert loaded[l] == s and slot_owner[s] == l
             done.add(l)
     assert len(done) == 8
+    assert sorted(loaded) == list(range(8))   # no load of a layer that does not exist
 
 
 # ---------------------------------------------------------------------------
@@ -419,6 +420,92 @@ def test_history_then_causal_merge_equals_one_shot():
 # ---------------------------------------------------------------------------
 # Whole chunk: threshold 1.0 reduces to full causal attention
 # ---------------------------------------------------------------------------
+
+
+def test_chunk_attention_head_matches_textbook_loops():
+    """One head of the chunk attention against explicit loops whose visibility
+    is spelled out key by key: every selected history key, then current key j
+    for query i only when j <= i (the aligned causal diagonal)."""
+    rng = np.random.default_rng(13)
+    lq, lh, D = 6, 5, 3
+    q = rng.standard_normal((lq, D))
+    kh, vh = rng.standard_normal((lh, D)), rng.standard_normal((lh, D))
+    kc, vc = rng.standard_normal((lq, D)), rng.standard_normal((lq, D))
+    vis = np.zeros((lq, lh + lq), dtype=bool)
+    for i in range(lq):
+        for j in range(lh):
+            vis[i, j] = True
+        for j in range(i + 1):
+            vis[i, lh + j] = True
+    ref_o, ref_l = _textbook_attention(q, np.concatenate([kh, kc]), np.concatenate([vh, vc]),
+                                       0.6, vis)
+    o, lse = O.bsa_chunk_attention_head(q, kh, vh, kc, vc, 0.6)
+    assert np.allclose(o, ref_o, atol=1e-12) and np.allclose(lse, ref_l, atol=1e-12)
+    # query 0 with no history sees exactly its own key: O = v_0
+    o0, l0 = O.bsa_chunk_attention_head(q, kh[:0], vh[:0], kc, vc, 0.6)
+    assert np.allclose(o0[0], vc[0], atol=1e-15)
+    assert abs(l0[0] - 0.6 * float(np.dot(q[0], kc[0]))) < 1e-14
+
+
+def _paged_sequence(rng, H, Hkv, D, lh, lq, block):
+    """A sequence [history; chunk] of one request, its keys/values laid out in a
+    pool whose pages are a permutation of the logical blocks."""
+    Lt = lh + lq
+    q = rng.standard_normal((H, lq, D)) * 0.5
+    k_all = rng.standard_normal((Hkv, Lt, D)) * 0.5
+    v_all = rng.standard_normal((Hkv, Lt, D))
+    npg = Lt // block
+    perm = rng.permutation(npg)
+    pool_k = np.zeros((npg, block, Hkv, D))
+    pool_v = np.zeros((npg, block, Hkv, D))
+    for j in range(npg):
+        for t in range(block):
+            for kvh in range(Hkv):
+                pool_k[perm[j], t, kvh] = k_all[kvh, j * block + t]
+                pool_v[perm[j], t, kvh] = v_all[kvh, j * block + t]
+    return q, k_all, v_all, perm, pool_k, pool_v
+
+
+def test_estimate_request_reads_each_heads_group_through_the_pages():
+    """The block sums of a request, read through a permuted page pool, equal the
+    per-head block sums over the contiguous sequence, query head h using KV
+    head floor(h / G) ([BSA] Step 1 repeats each KV head over its G query
+    heads)."""
+    rng = np.random.default_rng(17)
+    H, Hkv, D, S, block = 6, 2, 4, 4, 8
+    lh, lq = 24, 16
+    q, k_all, _, perm, pool_k, _ = _paged_sequence(rng, H, Hkv, D, lh, lq, block)
+    bs = O.estimate_request(q, k_all[:, lh:], pool_k, perm, lh, H, Hkv, S, block, 0.4)
+    G = H // Hkv
+    for h in range(H):
+        ref = O.block_sums_one_head(q[h], k_all[h // G, :lh], k_all[h // G, lh:], S, block, 0.4)
+        assert np.allclose(bs[h], ref, rtol=1e-13, atol=0)
+    # the KV heads differ, so a head mapped to the wrong group is visible
+    assert not np.allclose(bs[0], bs[G])
+
+
+def test_attend_request_sampled_rows_and_partial_selection():
+    """attend_request on a subset of query rows equals those rows of the full
+    call, and with a partial page selection each head equals the one-head
+    chunk attention over the selected pages' tokens, gathered from the
+    contiguous sequence."""
+    rng = np.random.default_rng(19)
+    H, Hkv, D, block = 4, 2, 4, 8
+    lh, lq = 32, 16
+    q, k_all, v_all, perm, pool_k, pool_v = _paged_sequence(rng, H, Hkv, D, lh, lq, block)
+    sel = [0, 2, 3]                              # logical history blocks kept
+    pages = [int(perm[j]) for j in sel]
+    kc, vc = k_all[:, lh:], v_all[:, lh:]
+    o, lse = O.attend_request(q, kc, vc, pool_k, pool_v, pages, H, Hkv, 0.5)
+    G = H // Hkv
+    toks = np.concatenate([np.arange(j * block, (j + 1) * block) for j in sel])
+    for h in range(H):
+        ro, rl = O.bsa_chunk_attention_head(q[h], k_all[h // G, toks], v_all[h // G, toks],
+                                            kc[h // G], vc[h // G], 0.5)
+        assert np.allclose(o[h], ro, atol=1e-12) and np.allclose(lse[h], rl, atol=1e-12)
+    rows = [0, 5, 15]
+    o2, l2 = O.attend_request(q, kc, vc, pool_k, pool_v, pages, H, Hkv, 0.5, rows=rows)
+    assert np.allclose(o2, o[:, rows], atol=1e-13) and np.allclose(l2, lse[:, rows], atol=1e-13)
 
 
 def test_tau_one_is_full_causal_attention():
