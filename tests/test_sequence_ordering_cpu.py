@@ -1,0 +1,132 @@
+"""Host logic of SequencePrefill.run_from_host on the CPU: the cross-stream
+order of the host-fed chunked prefill, checked with recording stand-ins for
+CUDA streams and events ("XAttention Offload Stream Synchronization Fix",
+修复方案: every consumer waits on the event of the copy it reads; "Task Plan:
+Layerwise Offload Refactoring", Phase 1.2: a chunk's K/V stored into its
+pages, the next chunk's history).
+
+The library calls are replaced by recorders, so no kernel and no copy runs;
+the test checks, on CUDA's happens-before order rebuilt from the log:
+
+  * chunk c's estimate follows the host-to-device copies of its Q and K (and,
+    with prefilled pools, of both pools when it has history);
+  * its KV store and its attention follow the copy of its V;
+  * with the store, the estimate of chunk c + 1 follows chunk c's store;
+  * its O and LSE leave the device only after its attention;
+  * the side streams start after the work already on the compute stream,
+    and the returned event follows every read-back.
+"""
+import pytest
+import torch
+
+import fake_streams as FS
+from xattention_block_sparse_gb300 import build as B
+from xattention_block_sparse_gb300 import runner as RN
+from xattention_block_sparse_gb300 import xattn as X
+
+
+class _Pool:
+    """A device pool stand-in whose bulk copy is logged on the current stream."""
+
+    def __init__(self, log, name):
+        self.log, self.name = log, name
+
+    def copy_(self, src, non_blocking=False):
+        self.log.append(("copy", FS.CURRENT[0], (self.name, 0)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    B.build()
+    X.load_library()
+
+
+def _run(monkeypatch, store_kv, n_chunks=3):
+    log, _ = FS.install(monkeypatch)
+    H, Hkv, D, S, Bk, chunk = 2, 1, 64, 8, 64, 64
+    L = chunk * n_chunks
+    bt = torch.arange(L // Bk, dtype=torch.int32)[None]
+    seq = RN.SequencePrefill(H, Hkv, D, S, Bk, L, chunk, bt, L // Bk)
+    chunk_of = {id(p): c for c, p in enumerate(seq.problems)}
+    host = {n: torch.zeros(s) for n, s in (("q", (H, L, D)), ("k", (Hkv, L, D)),
+                                           ("v", (Hkv, L, D)), ("o", (H, L, D)), ("lse", (H, L)))}
+    dev = {n: torch.zeros_like(t) for n, t in host.items()}
+    dev["kpool"], dev["vpool"] = _Pool(log, "kpool"), _Pool(log, "vpool")
+    if not store_kv:
+        host["kpool"], host["vpool"] = object(), object()
+    names = {id(t): n for n, t in list(host.items()) + list(dev.items())}
+
+    def copy_window(dst, src, t0, t1, stream=None):
+        assert t1 - t0 == chunk
+        log.append(("copy", stream, (names[id(dst)], t0 // chunk)))
+
+    def rec(kind):
+        def f(p, *a, **k):
+            stream = a[-1] if a else k.get("stream")
+            log.append((kind, stream, chunk_of[id(p)]))
+        return f
+
+    monkeypatch.setattr(X, "copy_window_async", copy_window)
+    for kind, fn in (("estimate", "xattn_estimate"), ("select", "xattn_select"),
+                     ("attend", "bsa_chunk_attention"), ("store", "xattn_store_kv")):
+        monkeypatch.setattr(X, fn, rec(kind))
+    compute, h2d, d2h = (FS.Stream(log, n) for n in ("compute", "h2d", "d2h"))
+    log.append(("earlier work", compute, None))
+    back = seq.run_from_host(host, dev, 0.9, compute, h2d, d2h, store_kv=store_kv)
+    return log, back, (compute, h2d, d2h), n_chunks
+
+
+def _index(log, kind, payload):
+    hits = [i for i, op in enumerate(log) if op[0] == kind and op[2] == payload]
+    assert len(hits) == 1, (kind, payload, hits)
+    return hits[0]
+
+
+@pytest.mark.parametrize("store_kv", [True, False])
+def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatch, store_kv):
+    log, back, (compute, h2d, d2h), n = _run(monkeypatch, store_kv)
+    before = FS.happens_before(log)
+    for c in range(n):
+        est, att = _index(log, "estimate", c), _index(log, "attend", c)
+        assert log[est][1] is compute and log[att][1] is compute
+        for name in ("q", "k"):
+            assert before(_index(log, "copy", (name, c)), est)
+        assert before(_index(log, "copy", ("v", c)), att)
+        assert before(est, _index(log, "select", c)) and before(_index(log, "select", c), att)
+        for name in ("o", "lse"):
+            rb = _index(log, "copy", (name, c))
+            assert log[rb][1] is d2h and before(att, rb)
+            assert before(rb, FS.record_index(log, back))
+        if store_kv:
+            st = _index(log, "store", c)
+            assert before(_index(log, "copy", ("k", c)), st)
+            assert before(_index(log, "copy", ("v", c)), st) and before(st, att)
+            if c + 1 < n:
+                assert before(st, _index(log, "estimate", c + 1))
+        elif c > 0:
+            for pool in ("kpool", "vpool"):
+                assert before(_index(log, "copy", (pool, 0)), est)
+    assert any(op[0] == "store" for op in log) == store_kv
+    first = _index(log, "earlier work", None)
+    for s in (h2d, d2h):
+        ops = [i for i, op in enumerate(log) if op[1] is s and op[0] != "record"]
+        assert all(before(first, i) for i in ops)
+
+
+def test_estimate_does_not_wait_for_its_v(built, monkeypatch):
+    """Q and K are all the estimate reads: its wait ends at the K copy, so the
+    V copy of the same chunk can still be in flight (the copies are issued
+    Q, K, V)."""
+    log, _, _, n = _run(monkeypatch, True)
+    before = FS.happens_before(log)
+    for c in range(n):
+        assert not before(_index(log, "copy", ("v", c)), _index(log, "estimate", c))
+
+
+def test_a_missing_wait_is_caught(built, monkeypatch):
+    """The check has teeth: without the compute stream's waits, chunk 1's
+    estimate no longer follows its copies."""
+    log, _, (compute, _, _), _ = _run(monkeypatch, True)
+    log2 = [op for op in log if not (op[0] == "wait" and op[1] is compute)]
+    before = FS.happens_before(log2)
+    assert not before(_index(log2, "copy", ("k", 1)), _index(log2, "estimate", 1))
