@@ -300,6 +300,8 @@ def run_ours(args, ws, rank, local):
         "steps": K_,
         "warmup": args.warmup,
         "ms_per_step": ms,
+        "ms_per_step_median": float(np.median(step_ms)),
+        "ms_per_step_best": float(min(step_ms)),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
