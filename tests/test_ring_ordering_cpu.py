@@ -93,3 +93,39 @@ def test_a_refill_without_the_done_wait_is_caught(monkeypatch):
     comp0 = next(i for i, op in enumerate(log) if op[0] == "compute")
     layer, si, _ = _loads(log, ring)[2]
     assert layer == 2 and not before(comp0, si)
+
+
+def test_reused_selection_estimates_once_per_chunk(monkeypatch):
+    """With the selection shared across layers, layer 0 runs estimate + select +
+    attention and every later layer only attention, on the same buffers (the
+    sel_page / n_sel layer 0 wrote); the ring's order is unchanged."""
+    log, _ = FS.install(monkeypatch)
+    P, Bk, Hkv, D, H, chunk, c, nl = 8, 4, 1, 2, 2, 8, 1, 6
+    layers = [_Layer(l, P, Bk, Hkv, D, H, P * Bk) for l in range(nl)]
+    ring = RN.LayerRing(4, P, Bk, Hkv, D, "cpu")
+    compute = FS.Stream(log, "compute")
+    bufs = object()
+    seen = []
+
+    def full(problem, q, kc, vc, kp, vp, tau, b, o, lse, stream=None):
+        seen.append(b)
+        log.append(("full", stream, len([op for op in log if op[0] in ("full", "attend")])))
+
+    def attend_only(problem, q, kc, vc, kp, vp, b, o, lse, softmax_scale=None, stream=None):
+        seen.append(b)
+        log.append(("attend", stream, len([op for op in log if op[0] in ("full", "attend")])))
+
+    monkeypatch.setattr(RN, "prefill_chunk", full)
+    monkeypatch.setattr(RN, "attend", attend_only)
+    outs = [(torch.zeros((H, P * Bk, D)), torch.zeros((H, P * Bk))) for _ in layers]
+    RN.ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, 2, Bk, 0.9, bufs, None, outs,
+                          compute, reuse_selection=True)
+    kinds = [(op[0], op[2]) for op in log if op[0] in ("full", "attend")]
+    assert kinds == [("full", 0)] + [("attend", l) for l in range(1, nl)]
+    assert all(b is bufs for b in seen)
+    before = FS.happens_before(log)
+    comp = {op[2]: i for i, op in enumerate(log) if op[0] in ("full", "attend")}
+    for layer, si, ri in _loads(log, ring):
+        assert before(ri, comp[layer])
+        if layer >= 4:
+            assert before(comp[layer - 4], si)

@@ -2,6 +2,7 @@
 fed from pinned host memory on a side stream.
 
     python -m xattention_block_sparse_gb300.ring_bench [--chunks 28,29,30,31]
+                                                       [--reuse-selection]
 
 For each chunk, every layer's history (and current chunk) pages are copied
 host -> device into slot (layer mod 4) while the compute stream works on the
@@ -34,6 +35,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--chunks", default="28,29,30,31")
     ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--reuse-selection", action="store_true",
+                    help="estimate and select on layer 0 only; later layers reuse its pages")
     a = ap.parse_args()
     from __graft_entry__ import build
     build()
@@ -55,7 +58,8 @@ def main():
     stream = torch.cuda.Stream(device=d)
     tau = cfg.taus[0]
     RN.ring_prefill_chunk(ring, layers, chunks[0], chunk, H, Hkv, D, S, Bk, tau, bufs,
-                          problems[chunks[0]], outs, stream)  # warm-up
+                          problems[chunks[0]], outs, stream,
+                          reuse_selection=a.reuse_selection)  # warm-up
     torch.cuda.synchronize()
     per_chunk = []
     for c in chunks:
@@ -66,7 +70,8 @@ def main():
         w0.record(stream)
         ring.copy_stream.wait_stream(stream)
         RN.ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, S, Bk, tau, bufs, problems[c],
-                              outs, stream, compute_events=comp)
+                              outs, stream, compute_events=comp,
+                              reuse_selection=a.reuse_selection)
         w1.record(stream)
         torch.cuda.synchronize()
         per_chunk.append({
@@ -85,7 +90,9 @@ def main():
     print(json.dumps({
         "workload": (f"q4b_128k: {H} Q / {Hkv} KV heads, head_dim {D}, stride {S}, chunks "
                      f"{chunks} of {chunk} tokens at 128K context, {nl} layers through "
-                     f"{cfg.ring_slots} ring slots, tau {tau}"),
+                     f"{cfg.ring_slots} ring slots, tau {tau}"
+                     + (", layer 0's selection reused by every layer" if a.reuse_selection
+                        else "")),
         "compute_ms": comp, "copy_ms": copy, "wall_ms": wall,
         "h2d_GB": byts / 1e9, "h2d_GBps": byts / 1e9 / (copy / 1e3) if copy else None,
         "overlap": 1.0 - (wall - comp) / copy if copy else None,

@@ -236,10 +236,15 @@ class LayerRing:
 
 
 def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bufs, problem,
-                       outs, stream, on_layer=None, compute_events=None):
+                       outs, stream, on_layer=None, compute_events=None, reuse_selection=False):
     """Chunk c of every layer through the ring: history pages [0, c*chunk/block)
     of each layer are loaded into its slot, the current chunk's K/V are the
-    next chunk/block pages of the same host cache (copied in the same load)."""
+    next chunk/block pages of the same host cache (copied in the same load).
+
+    reuse_selection: only layer 0 estimates and selects; every later layer
+    attends over the pages layer 0 selected ("XAttention BSA Policy 设计文档",
+    性能分析, 优化方向 1: share the estimate across layers).  The page ids
+    stay valid because every slot lays its layer out under one block table."""
     n_hist = c * chunk // block
     n_load = n_hist + chunk // block
     L = len(layers)
@@ -256,8 +261,12 @@ def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bu
             vc = vp[n_hist:n_load].reshape(chunk, Hkv, D).permute(1, 0, 2).contiguous()
             q = layers[l].q[:, c * chunk:]
             o, lse = outs[l]
-            prefill_chunk(problem, q, kc, vc, kp, vp, tau, bufs, o[:, c * chunk:],
-                          lse[:, c * chunk:], stream=stream)
+            if reuse_selection and l > 0:
+                attend(problem, q, kc, vc, kp, vp, bufs, o[:, c * chunk:], lse[:, c * chunk:],
+                       stream=stream)
+            else:
+                prefill_chunk(problem, q, kc, vc, kp, vp, tau, bufs, o[:, c * chunk:],
+                              lse[:, c * chunk:], stream=stream)
             if compute_events is not None:
                 e1.record(stream)
                 compute_events.append((e0, e1))
