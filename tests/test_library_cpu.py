@@ -176,3 +176,46 @@ def test_sequence_prefill_chunk_problems(lib):
     assert seq.bufs.workspace.numel() == sizes[-1]
     assert seq.bufs.block_sums.numel() == X.xattn_block_sums_count(seq.problems[-1])
     assert tuple(seq.bufs.sel_page.shape) == (1, L // Bk) and seq.bufs.mask is None
+
+
+class _DevT:
+    """A GPU-tensor stand-in for the binding's checks: the checks raise before
+    any library call, so its pointer is never used."""
+
+    is_cuda = True
+    shape = (4, 128)
+
+    def __init__(self, dtype, n=16):
+        self.dtype, self._n = dtype, n
+
+    def data_ptr(self):
+        return 0x20000
+
+    def numel(self):
+        return self._n
+
+    def element_size(self):
+        return 1
+
+
+def test_binding_refuses_host_tensors_and_wrong_types(lib):
+    """A host tensor handed to a kernel would be read as device memory, and a
+    wrong element type as garbage: the binding stops both before the call."""
+    import torch
+    p = _prob([1024], [0])
+    bf, f32, i32 = _DevT("torch.bfloat16"), _DevT("torch.float32"), _DevT("torch.int32")
+    ws = _DevT("torch.uint8")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        X.xattn_estimate(p, torch.zeros(4, dtype=torch.bfloat16), bf, bf, 0.1, ws, f32)
+    with pytest.raises(TypeError, match="q: element type"):
+        X.xattn_estimate(p, f32, bf, bf, 0.1, ws, f32)
+    with pytest.raises(TypeError, match="block_sums"):
+        X.xattn_estimate(p, bf, bf, bf, 0.1, ws, bf)
+    with pytest.raises(TypeError, match="sel_page"):
+        X.xattn_select(p, f32, 0.9, ws, None, i32, f32, i32)
+    with pytest.raises(TypeError, match="o: element type"):
+        X.bsa_chunk_attention(p, bf, bf, bf, bf, bf, i32, i32, 0.1, ws, f32, f32)
+    with pytest.raises(TypeError, match="lse_out"):
+        X.lse_merge(f32, f32, f32, f32, bf, bf)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        X.xattn_store_kv(p, bf, bf, torch.zeros(4, dtype=torch.bfloat16), bf)

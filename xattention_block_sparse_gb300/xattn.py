@@ -148,8 +148,21 @@ class Problem:
         return ctypes.byref(self.c)
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+_BF16, _F32, _I32, _U8 = "torch.bfloat16", "torch.float32", "torch.int32", "torch.uint8"
+
+
+def _dev(t, what, *dtypes):
+    """Device pointer of tensor t, after checking that it lives on a GPU and has
+    one of the element types the header gives for the argument: a host
+    pointer handed to a kernel would be read as device memory.  None passes
+    through (the library answers XATTN_EINVAL where it needs the pointer)."""
+    if t is None:
+        return None
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{what}: a CUDA tensor is required (the kernels read it on the GPU)")
+    if dtypes and str(t.dtype) not in dtypes:
+        raise TypeError(f"{what}: element type {t.dtype}, expected {' or '.join(dtypes)}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -182,10 +195,11 @@ def xattn_block_sums_offset(problem: Problem, r: int) -> int:
 
 
 def xattn_estimate(problem, q, k_cur, k_pool, scale, workspace, block_sums, stream=None):
-    st = load_library().xattn_estimate(problem.ref(), _ptr(q), _ptr(k_cur), _ptr(k_pool),
-                                       float(scale), _ptr(workspace),
+    st = load_library().xattn_estimate(problem.ref(), _dev(q, "q", _BF16),
+                                       _dev(k_cur, "k_cur", _BF16), _dev(k_pool, "k_pool", _BF16),
+                                       float(scale), _dev(workspace, "workspace"),
                                        workspace.numel() * workspace.element_size(),
-                                       _ptr(block_sums), _stream(stream))
+                                       _dev(block_sums, "block_sums", _F32), _stream(stream))
     _check(st, "xattn_estimate")
 
 
@@ -193,10 +207,13 @@ def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_p
                  stream=None, vote=(1, 2), force_sink_last=True):
     """vote = (num, den): a history block is selected when its votes exceed
     num/den of the (KV head, query block) pairs; (1, 2) is the strict majority."""
-    st = load_library().xattn_select(problem.ref(), _ptr(block_sums), float(threshold),
+    st = load_library().xattn_select(problem.ref(), _dev(block_sums, "block_sums", _F32),
+                                     float(threshold),
                                      int(vote[0]), int(vote[1]), int(bool(force_sink_last)),
-                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                     _ptr(mask), _ptr(sel_idx), _ptr(sel_page), _ptr(n_sel),
+                                     _dev(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(),
+                                     _dev(mask, "mask", _U8), _dev(sel_idx, "sel_idx", _I32),
+                                     _dev(sel_page, "sel_page", _I32), _dev(n_sel, "n_sel", _I32),
                                      _stream(stream))
     _check(st, "xattn_select")
 
@@ -206,21 +223,29 @@ def xattn_select_noalloc(problem, block_sums, threshold, mask, sel_idx, sel_page
     """xattn_select without a workspace, for callers that cannot allocate device
     memory on the prefill path; its vote counters live in a fixed array inside
     the library (one per GPU), so calls that overlap on the GPU race."""
-    st = load_library().xattn_select_noalloc(problem.ref(), _ptr(block_sums), float(threshold),
-                                             int(vote[0]), int(vote[1]),
+    st = load_library().xattn_select_noalloc(problem.ref(),
+                                             _dev(block_sums, "block_sums", _F32),
+                                             float(threshold), int(vote[0]), int(vote[1]),
                                              int(bool(force_sink_last)),
-                                             _ptr(mask), _ptr(sel_idx), _ptr(sel_page),
-                                             _ptr(n_sel), _stream(stream))
+                                             _dev(mask, "mask", _U8),
+                                             _dev(sel_idx, "sel_idx", _I32),
+                                             _dev(sel_page, "sel_page", _I32),
+                                             _dev(n_sel, "n_sel", _I32), _stream(stream))
     _check(st, "xattn_select_noalloc")
 
 
 def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
                         workspace, o, lse, stream=None):
-    st = load_library().bsa_chunk_attention(problem.ref(), _ptr(q), _ptr(k_cur), _ptr(v_cur),
-                                            _ptr(k_pool), _ptr(v_pool), _ptr(sel_page),
-                                            _ptr(n_sel), float(softmax_scale), _ptr(workspace),
+    st = load_library().bsa_chunk_attention(problem.ref(), _dev(q, "q", _BF16),
+                                            _dev(k_cur, "k_cur", _BF16),
+                                            _dev(v_cur, "v_cur", _BF16),
+                                            _dev(k_pool, "k_pool", _BF16),
+                                            _dev(v_pool, "v_pool", _BF16),
+                                            _dev(sel_page, "sel_page", _I32),
+                                            _dev(n_sel, "n_sel", _I32), float(softmax_scale),
+                                            _dev(workspace, "workspace"),
                                             workspace.numel() * workspace.element_size(),
-                                            _ptr(o), _ptr(lse),
+                                            _dev(o, "o", _BF16), _dev(lse, "lse", _F32),
                                             _stream(stream))
     _check(st, "bsa_chunk_attention")
 
@@ -228,8 +253,10 @@ def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_se
 def lse_merge(o1, lse1, o2, lse2, o_out, lse_out, stream=None):
     rows, d = o1.shape[0], o1.shape[-1]
     bf16 = 1 if str(o_out.dtype).endswith("bfloat16") else 0
-    st = load_library().lse_merge(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), rows, d,
-                                  _ptr(o_out), bf16, _ptr(lse_out), _stream(stream))
+    st = load_library().lse_merge(_dev(o1, "o1", _F32), _dev(lse1, "lse1", _F32),
+                                  _dev(o2, "o2", _F32), _dev(lse2, "lse2", _F32), rows, d,
+                                  _dev(o_out, "o_out", _BF16, _F32), bf16,
+                                  _dev(lse_out, "lse_out", _F32), _stream(stream))
     _check(st, "lse_merge")
 
 
@@ -250,8 +277,10 @@ def xattn_last_device_error(stream=None) -> int:
 def xattn_store_kv(problem, k_cur, v_cur, k_pool, v_pool, stream=None):
     """Write the chunk's K/V ([Hkv, tokens, D] views, kv_head_stride apart) into
     the pool pages the block table gives their positions."""
-    st = load_library().xattn_store_kv(problem.ref(), _ptr(k_cur), _ptr(v_cur), _ptr(k_pool),
-                                       _ptr(v_pool), _stream(stream))
+    st = load_library().xattn_store_kv(problem.ref(), _dev(k_cur, "k_cur", _BF16),
+                                       _dev(v_cur, "v_cur", _BF16),
+                                       _dev(k_pool, "k_pool", _BF16),
+                                       _dev(v_pool, "v_pool", _BF16), _stream(stream))
     _check(st, "xattn_store_kv")
 
 
