@@ -268,7 +268,7 @@ def _brute_select(q, tau):
 @pytest.mark.parametrize("seed", range(40))
 def test_threshold_select_bruteforce(seed):
     rng = np.random.default_rng(seed)
-    n = int(rng.integers(1, 11))
+    n = int(rng.integers(1, 15))          # rows of up to 14 blocks
     # mix of continuous values, exact ties and zeros, like block sums
     v = rng.exponential(1.0, n).astype(np.float32)
     if n > 3:
