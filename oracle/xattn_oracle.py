@@ -299,6 +299,19 @@ def gqa_vote(mask: np.ndarray, num_kv_heads: int, kb_hist: int, force: bool = Tr
     return np.nonzero(keep)[0].astype(np.int64)
 
 
+def per_kv_head_select(mask: np.ndarray, num_kv_heads: int, kb_hist: int, force: bool = True,
+                       vote=(1, 2)):
+    """One block set per KV head, the selection [BSA] Step 4 sets beside the vote
+    across KV heads ("为什么使用 Majority Voting?").  Reading: KV head g keeps
+    history block j when more than num/den of its query blocks chose it, any
+    query head of its group counting for the block; sink and last forced.  It
+    is the vote above restricted to one KV head.  Returns one ascending id
+    array per KV head."""
+    G = mask.shape[0] // num_kv_heads
+    return [gqa_vote(mask[g * G:(g + 1) * G], 1, kb_hist, force=force, vote=vote)
+            for g in range(num_kv_heads)]
+
+
 def density(selected: int, available: int) -> float:
     """[BSA] Density 统计 API: selected / available history blocks."""
     return selected / available if available else 0.0
@@ -419,6 +432,19 @@ def attend_request(q, k_cur, v_cur, pool_k, pool_v, sel_pages, H, Hkv, scale,
                  np.arange(lq)[None, :] <= rows[:, None]], axis=1)
             o[h], lse[h] = attention_with_lse(q[h, rows], K, V, scale, vis)
     return o, lse
+
+
+def attend_request_per_kv(q, k_cur, v_cur, pool_k, pool_v, pages_per_kv, H, Hkv, scale,
+                          rows=None):
+    """attend_request with its own selected pages for each KV head
+    (per_kv_head_select): the query heads of group g attend over the pages in
+    pages_per_kv[g] and the causal current chunk."""
+    G = H // Hkv
+    outs = [attend_request(q[g * G:(g + 1) * G], k_cur[g:g + 1], v_cur[g:g + 1],
+                           pool_k[:, :, g:g + 1], pool_v[:, :, g:g + 1], pages_per_kv[g], G, 1,
+                           scale, rows) for g in range(Hkv)]
+    return (np.concatenate([o for o, _ in outs], axis=0),
+            np.concatenate([l for _, l in outs], axis=0))
 
 
 def default_estimation_scale(head_dim: int, stride: int) -> float:

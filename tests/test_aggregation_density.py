@@ -50,8 +50,7 @@ def chunk_densities(wl, c, tau):
     n_all = cfg.Hkv * qb + 1
     for name, vote in (("any", (0, 1)), ("majority", (1, 2)), ("all", (n_all - 1, n_all))):
         out[name] = O.density(len(O.gqa_vote(mask, cfg.Hkv, kbh, vote=vote)), kbh)
-    G = cfg.H // cfg.Hkv
-    per_kv = [len(O.gqa_vote(mask[g * G:(g + 1) * G], 1, kbh)) for g in range(cfg.Hkv)]
+    per_kv = [len(s) for s in O.per_kv_head_select(mask, cfg.Hkv, kbh)]
     out["per_kv_head"] = O.density(sum(per_kv), kbh * cfg.Hkv)
     return out
 

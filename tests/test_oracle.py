@@ -334,6 +334,56 @@ def test_vote_hand_cases():
     assert O.gqa_vote(m1, 2, 1).tolist() == [0]
 
 
+def test_per_kv_head_selection_hand_cases():
+    # H=4, Hkv=2 (G=2), Qb=2, 5 history blocks
+    m = np.zeros((4, 2, 5), dtype=bool)
+    m[0, 0, 1] = m[1, 1, 1] = True     # kv 0: block 1 in both query blocks (two heads)
+    m[2, 0, 2] = True                  # kv 1: block 2 in one query block of two
+    m[3, :, 3] = True                  # kv 1: block 3 in both
+    got = O.per_kv_head_select(m, 2, 5)
+    assert [g.tolist() for g in got] == [[0, 1, 4], [0, 3, 4]]
+    got = O.per_kv_head_select(m, 2, 5, force=False, vote=(0, 1))
+    assert [g.tolist() for g in got] == [[1], [2, 3]]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_majority_vote_is_inside_the_union_of_per_kv_head_sets(seed):
+    """A block with more than half of all (KV head, query block) votes has more
+    than half of some KV head's own votes (pigeonhole), so the vote across KV
+    heads never keeps a block that every per-KV-head selection drops."""
+    rng = np.random.default_rng(seed)
+    Hkv, G, qb, kb = 4, 2, 3, 9
+    m = rng.random((Hkv * G, qb, kb)) < rng.uniform(0.1, 0.6)
+    vote = O.gqa_vote(m, Hkv, kb, force=False)
+    union = set().union(*[set(g.tolist()) for g in O.per_kv_head_select(m, Hkv, kb, force=False)])
+    assert set(vote.tolist()) <= union
+
+
+def test_attention_with_pages_per_kv_head():
+    """Each group attends over its own pages: equal to the one-head chunk
+    attention over that group's selected tokens, and to attend_request when all
+    groups hold the same pages."""
+    rng = np.random.default_rng(23)
+    H, Hkv, D, block = 4, 2, 4, 8
+    lh, lq = 32, 16
+    q, k_all, v_all, perm, pool_k, pool_v = _paged_sequence(rng, H, Hkv, D, lh, lq, block)
+    kc, vc = k_all[:, lh:], v_all[:, lh:]
+    sel = [[0, 3], [1, 2, 3]]
+    pages = [[int(perm[j]) for j in s] for s in sel]
+    o, lse = O.attend_request_per_kv(q, kc, vc, pool_k, pool_v, pages, H, Hkv, 0.5)
+    G = H // Hkv
+    for h in range(H):
+        g = h // G
+        toks = np.concatenate([np.arange(j * block, (j + 1) * block) for j in sel[g]])
+        ro, rl = O.bsa_chunk_attention_head(q[h], k_all[g, toks], v_all[g, toks], kc[g], vc[g],
+                                            0.5)
+        assert np.allclose(o[h], ro, atol=1e-12) and np.allclose(lse[h], rl, atol=1e-12)
+    same = [pages[1], pages[1]]
+    o2, l2 = O.attend_request_per_kv(q, kc, vc, pool_k, pool_v, same, H, Hkv, 0.5)
+    o3, l3 = O.attend_request(q, kc, vc, pool_k, pool_v, pages[1], H, Hkv, 0.5)
+    assert np.allclose(o2, o3, atol=1e-13) and np.allclose(l2, l3, atol=1e-13)
+
+
 # ---------------------------------------------------------------------------
 # Attention and the LSE merge
 # ---------------------------------------------------------------------------

@@ -55,6 +55,10 @@ PINS = {
     "estimate_request": P.test_estimate_request_reads_each_heads_group_through_the_pages,
     "attend_request": P.test_attend_request_sampled_rows_and_partial_selection,
     "tau_one": P.test_tau_one_is_full_causal_attention,
+    "per_kv_select": P.test_per_kv_head_selection_hand_cases,
+    "per_kv_union": _each(P.test_majority_vote_is_inside_the_union_of_per_kv_head_sets,
+                          *[(s,) for s in range(6)]),
+    "per_kv_attend": P.test_attention_with_pages_per_kv_head,
 }
 
 # (oracle function, exact source fragment, its mistaken replacement, pins that must catch it)
@@ -116,6 +120,10 @@ MUTANTS = [
     ("gqa_vote", "keep[0] = True", "keep[0] = keep[0]", ["vote"]),
     ("gqa_vote", "mask[:, :, :kb_hist]", "mask[:, :, -kb_hist:]", ["vote"]),
     ("select_request", "int(bt_row[j])", "int(j)", ["tau_one"]),
+    ("per_kv_head_select", "mask[g * G:(g + 1) * G]", "mask[g::num_kv_heads]",
+     ["per_kv_select", "per_kv_union"]),
+    ("per_kv_head_select", "gqa_vote(mask[g * G:(g + 1) * G], 1,",
+     "gqa_vote(mask[g * G:(g + 1) * G], G,", ["per_kv_select", "per_kv_union"]),
     ("density", "return selected / available", "return available / selected",
      ["policy_arithmetic"]),
     # attention and the merge ([BSA] compute_chunked_prefill)
@@ -142,6 +150,10 @@ MUTANTS = [
      "np.arange(lq)[None, :] <= np.arange(len(rows))[:, None]", ["attend_request"]),
     ("attend_request", "np.arange(lq)[None, :] <= rows[:, None]",
      "np.arange(lq)[None, :] < rows[:, None]", ["attend_request", "tau_one"]),
+    ("attend_request_per_kv", "pages_per_kv[g], G, 1,", "pages_per_kv[0], G, 1,",
+     ["per_kv_attend"]),
+    ("attend_request_per_kv", "pool_k[:, :, g:g + 1], pool_v[:, :, g:g + 1]",
+     "pool_k[:, :, 0:1], pool_v[:, :, 0:1]", ["per_kv_attend"]),
     # layer ring ([PLAN] Phases 1.1 and 4)
     ("ring_slot", "layer % num_buffers", "layer // num_buffers", ["ring"]),
     ("ring_schedule", "if l + num_buffers < num_layers", "if l + num_buffers <= num_layers",
