@@ -219,3 +219,17 @@ def test_binding_refuses_host_tensors_and_wrong_types(lib):
         X.lse_merge(f32, f32, f32, f32, bf, bf)
     with pytest.raises(ValueError, match="CUDA tensor"):
         X.xattn_store_kv(p, bf, bf, torch.zeros(4, dtype=torch.bfloat16), bf)
+
+
+def test_runner_estimation_scale_equals_the_oracle_reading():
+    """The product path's estimation scale (runner.estimation_scale, what the
+    bench and the prefill driver pass to xattn_estimate) and the oracle's
+    reading (default_estimation_scale, what the parity tests pass) are written
+    out separately; they must agree on every workload's head size and stride,
+    or the parity tests would pass while the bench selects with another scale."""
+    from oracle import xattn_oracle as O
+    from xattention_block_sparse_gb300 import inputs as I
+    from xattention_block_sparse_gb300 import runner as RN
+    for cfg in I.CONFIGS.values():
+        assert RN.estimation_scale(cfg.D, cfg.stride) == O.default_estimation_scale(
+            cfg.D, cfg.stride), cfg.name

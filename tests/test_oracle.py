@@ -232,6 +232,39 @@ def test_block_sums_uniform_scores_closed_form():
     assert np.allclose(bs, exp, rtol=1e-14, atol=1e-15)
 
 
+def test_default_estimation_scale_hand_values():
+    """The estimation logit scale, read as 1/(sqrt(D) * stride) (the BSA page
+    passes an unnamed `scale` to its block-sum step, select_blocks Step 2):
+    values worked out by hand for the two head sizes of the workloads."""
+    assert O.default_estimation_scale(128, 8) == pytest.approx(0.011048543456039806, rel=1e-15)
+    assert O.default_estimation_scale(128, 16) == pytest.approx(0.005524271728019903, rel=1e-15)
+    assert O.default_estimation_scale(64, 16) == 0.0078125       # 1 / (8 * 16)
+    assert O.default_estimation_scale(4, 2) == 0.25              # 1 / (2 * 2)
+
+
+def test_estimation_scale_decides_block_sums_and_selection():
+    """One reshaped row (S = 2, D = 4, one KV block per reshaped column) whose
+    antidiagonal products are 8, 0 and 4 by construction: with the default
+    scale 1/(2*2) the scores are 2, 0, 1, so the block sums are
+    e^2, 1, e over e^2 + e + 1 (closed form), and tau = 0.7 keeps blocks 0 and
+    2 (0.665 < 0.7 <= 0.910).  A scale without the stride factor (0.5) or with
+    sqrt(D*S) would keep block 0 alone."""
+    S, block, D = 2, 2, 4
+    scale = O.default_estimation_scale(D, S)
+    q = np.zeros((2, D))
+    q[1, 0] = 4.0                      # row a = 0 reads q[1] with key phase 0
+    kh = np.zeros((4, D))
+    kh[0, 0] = 2.0                     # history column 0: 4 * 2 = 8
+    kc = np.zeros((2, D))
+    kc[0, 0] = 1.0                     # current column 0 (visible from row 0): 4
+    bs = O.block_sums_one_head(q, kh, kc, S, block, scale)
+    e = math.e
+    z = e * e + e + 1.0
+    assert np.allclose(bs, [[e * e / z, 1.0 / z, e / z]], rtol=1e-14, atol=0)
+    keep = O.threshold_select_row(bs[0].astype(np.float32), 0.7)
+    assert keep.tolist() == [True, False, True]
+
+
 def test_block_sums_of_sampled_query_blocks_match_full():
     q, kh, kc, S, block = _rand_problem(5, lh=32, lq=32, S=4, block=8)
     full = O.block_sums_one_head(q, kh, kc, S, block, 0.45)

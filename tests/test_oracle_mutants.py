@@ -59,6 +59,8 @@ PINS = {
     "per_kv_union": _each(P.test_majority_vote_is_inside_the_union_of_per_kv_head_sets,
                           *[(s,) for s in range(6)]),
     "per_kv_attend": P.test_attention_with_pages_per_kv_head,
+    "est_scale": P.test_default_estimation_scale_hand_values,
+    "est_scale_bs": P.test_estimation_scale_decides_block_sums_and_selection,
 }
 
 # (oracle function, exact source fragment, its mistaken replacement, pins that must catch it)
@@ -154,6 +156,13 @@ MUTANTS = [
      ["per_kv_attend"]),
     ("attend_request_per_kv", "pool_k[:, :, g:g + 1], pool_v[:, :, g:g + 1]",
      "pool_k[:, :, 0:1], pool_v[:, :, 0:1]", ["per_kv_attend"]),
+    # the estimation scale reading (1/(sqrt(D) * S))
+    ("default_estimation_scale", "math.sqrt(head_dim) * stride", "math.sqrt(head_dim)",
+     ["est_scale", "est_scale_bs"]),
+    ("default_estimation_scale", "math.sqrt(head_dim) * stride", "math.sqrt(head_dim * stride)",
+     ["est_scale", "est_scale_bs"]),
+    ("default_estimation_scale", "math.sqrt(head_dim) * stride", "head_dim * stride",
+     ["est_scale", "est_scale_bs"]),
     # layer ring ([PLAN] Phases 1.1 and 4)
     ("ring_slot", "layer % num_buffers", "layer // num_buffers", ["ring"]),
     ("ring_schedule", "if l + num_buffers < num_layers", "if l + num_buffers <= num_layers",
