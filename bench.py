@@ -194,7 +194,7 @@ def run_ours(args, ws, rank, local):
     KP, VP = up(wl.kpool_bits), up(wl.vpool_bits)
     BT = torch.from_numpy(wl.block_table).to(dev)
     seq = RN.SequencePrefill(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, L, chunk, BT,
-                             KP.shape[0])
+                             KP.shape[0], est_from_pages=args.est_from_pages)
     O_ = torch.empty((cfg.H, L, cfg.D), dtype=torch.bfloat16, device=dev)
     LSE = torch.empty((cfg.H, L), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -208,8 +208,14 @@ def run_ours(args, ws, rank, local):
             b = seq.bufs
             if ev is not None:
                 ev[c][0].record(stream)
-            X.xattn_estimate(p, Q[:, t0:], K[:, t0:], KP, RN.estimation_scale(cfg.D, cfg.stride),
-                             b.workspace, b.block_sums, stream)
+            if args.est_from_pages:
+                X.xattn_estimate(p, Q[:, t0:], K[:, t0:], KP,
+                                 RN.estimation_scale(cfg.D, cfg.stride), b.workspace,
+                                 b.block_sums, stream)
+            else:  # keys in token order: K [Hkv, L, D] holds the history and the chunk
+                X.xattn_estimate_seq(p, Q[:, t0:], K, [0],
+                                     RN.estimation_scale(cfg.D, cfg.stride), b.workspace,
+                                     b.block_sums, stream)
             if ev is not None:
                 ev[c][1].record(stream)
             X.xattn_select(p, b.block_sums, tau, b.workspace, None, b.sel_idx, b.sel_page,
@@ -228,8 +234,7 @@ def run_ours(args, ws, rank, local):
         for c in range(nchunk):
             p = seq.problems[c]
             t0 = c * chunk
-            RN.prefill_chunk(p, Q[:, t0:], K[:, t0:], V[:, t0:], KP, VP, tau, seq.bufs,
-                             O_[:, t0:], LSE[:, t0:], stream=stream)
+            seq.run_chunk(c, Q, K, V, KP, VP, tau, O_, LSE, stream=stream)
             n_sel.append(int(seq.bufs.n_sel[0].item()))
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
@@ -486,6 +491,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="q06b_32k")
     ap.add_argument("--tau", type=float, default=0.9)
+    ap.add_argument("--est-from-pages", action="store_true",
+                    help="estimate from the history pages (xattn_estimate) instead of the "
+                         "keys in token order (xattn_estimate_seq)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":

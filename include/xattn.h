@@ -44,7 +44,11 @@
  *            and has cu_seqlens_kh[r+1]-cu_seqlens_kh[r] history tokens stored
  *            in the paged pool.  Every length is a multiple of block_size.
  * Layouts:   q, o      bf16 [H, tokens, D]   (head h at h*q_head_stride)
- *            k_cur,v_cur bf16 [Hkv, tokens, D] (head at h*kv_head_stride)
+ *            k_cur,v_cur bf16, element (KV head h, token t, d) at
+ *                      h*kv_head_stride + t*kv_token_stride + d: [Hkv, tokens, D]
+ *                      (kv_token_stride = D) or [tokens, Hkv, D]
+ *                      (kv_head_stride = D, kv_token_stride = Hkv*D, e.g. the
+ *                      chunk's own pages of a pool laid out in logical order)
  *            lse       fp32 [H, tokens]      (head at h*lse_head_stride)
  *            k_pool,v_pool bf16 [num_pages, block_size, Hkv, D]
  *            block_table int32 [B, bt_stride]; history token t of request r is
@@ -58,6 +62,11 @@
  *            first such fault in a device error word and continues; read it
  *            with xattn_device_error.  Every wait inside a kernel is bounded:
  *            one that runs out records XATTN_ETIMEOUT and the kernel returns.
+ * Lifetime:  the library looks up, once per device, the device addresses of its
+ *            own __device__ variables (the error word, the counters of
+ *            xattn_select_noalloc) and keeps them for the life of the process.
+ *            Do not use it across cudaDeviceReset or any other teardown of a
+ *            device's primary context: the kept addresses would be stale.
  */
 #ifndef XATTN_H
 #define XATTN_H
@@ -109,6 +118,13 @@ typedef struct xattn_problem {
   int64_t q_head_stride;          /* elements between heads of q and o */
   int64_t kv_head_stride;         /* elements between heads of k_cur and v_cur */
   int64_t lse_head_stride;        /* elements between heads of lse */
+  int64_t kv_token_stride;        /* elements between tokens of k_cur and v_cur;
+                                     0 means head_dim (the [Hkv, tokens, D] layout).
+                                     The two strides must describe [Hkv, tokens, D]
+                                     (kv_head_stride >= tokens * kv_token_stride) or
+                                     [tokens, Hkv, D] (kv_token_stride >= Hkv *
+                                     kv_head_stride), both >= D, multiples of 8
+                                     (XATTN_EINVAL / XATTN_EALIGN otherwise). */
 } xattn_problem;
 
 /* Bytes of scratch the caller must provide to xattn_estimate, xattn_select and
@@ -147,6 +163,30 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
                             size_t workspace_bytes, float *block_sums,
                             xattn_stream_t stream);
 
+/* The same estimation, reading each request's keys -- history, then the
+ * current chunk -- from one buffer in logical token order instead of the pool
+ * pages and k_cur.  The BSA policy page's select_blocks (Step 1) copies every
+ * history K block to the GPU and transposes it to [heads, k_len, D] before
+ * its GEMM; here the caller keeps the keys in that order (as a prefill holds
+ * its K anyway), so the GEMM fetches the 256 keys of a score tile at one
+ * stride phase as a single strided copy rather than one copy per page.
+ * Results equal xattn_estimate's on the same keys bit for bit.
+ *   k_seq               DEVICE bf16, element (KV head h, token t, d) at
+ *                       h*k_seq_head_stride + t*k_seq_token_stride + d
+ *   k_seq_head_stride, k_seq_token_stride   elements, multiples of 8, >= D;
+ *                       token stride 0 means D; the layout is [Hkv, tokens, D]
+ *                       or [tokens, Hkv, D] (as for k_cur)
+ *   k_seq_start         HOST int64 [B]: request r's kh_r + q_r keys are tokens
+ *                       [k_seq_start[r], k_seq_start[r] + kh_r + q_r) of k_seq,
+ *                       its history first; each a multiple of the stride
+ * The buffer must hold max_r(k_seq_start[r] + kh_r + q_r) tokens.  Other
+ * arguments, outputs and errors as xattn_estimate. */
+xattn_status xattn_estimate_seq(const xattn_problem *p, const void *q, const void *k_seq,
+                                int64_t k_seq_head_stride, int64_t k_seq_token_stride,
+                                const int64_t *k_seq_start, float scale, void *workspace,
+                                size_t workspace_bytes, float *block_sums,
+                                xattn_stream_t stream);
+
 /* Selection (BSA policy page, select_blocks Steps 3-4).
  * Per (request, head, query block) row, with integer masses
  * q_j = round_half_even(block_sums_j * 2^32), T = sum_j q_j, R = fl64(threshold*T):
@@ -170,6 +210,23 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
                           void *workspace, size_t workspace_bytes, uint8_t *mask,
                           int32_t *sel_idx, int32_t *sel_page, int32_t *n_sel,
                           xattn_stream_t stream);
+
+/* Selection with one block set per KV head (BSA policy page, select_blocks
+ * Step 4, "为什么使用 Majority Voting?": per-head selection beside the vote
+ * across heads).  Threshold masks and the GQA "any" as for xattn_select; then
+ * KV head k of request r keeps history block j when
+ *   votes_k,j * vote_den > vote_num * Qb_r   (its own votes over its query blocks)
+ * and, if force_sink_last != 0, blocks 0 and Kb_h-1.  Outputs are per
+ * (request, KV head), row r*Hkv + k:
+ *   sel_idx, sel_page   DEVICE int32 [B, Hkv, bt_stride]
+ *   n_sel               DEVICE int32 [B, Hkv]
+ * Other arguments and errors as xattn_select; feed the result to
+ * bsa_chunk_attention_per_kv_head. */
+xattn_status xattn_select_per_kv_head(const xattn_problem *p, const float *block_sums,
+                                      double threshold, int32_t vote_num, int32_t vote_den,
+                                      int32_t force_sink_last, void *workspace,
+                                      size_t workspace_bytes, uint8_t *mask, int32_t *sel_idx,
+                                      int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream);
 
 /* Capacity of the fixed counter array behind xattn_select_noalloc:
  * num_requests * bt_stride must not exceed it (1 MiB of int32 counters). */
@@ -224,6 +281,20 @@ xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const vo
                                  float softmax_scale, void *workspace, size_t workspace_bytes,
                                  void *o, float *lse, xattn_stream_t stream);
 
+/* bsa_chunk_attention over a selection per KV head (xattn_select_per_kv_head):
+ * the query heads of KV head k of request r attend the pages in
+ * sel_page[r][k][0..n_sel[r][k]) and the causal current chunk.
+ *   sel_page  DEVICE int32 [B, Hkv, bt_stride];  n_sel  DEVICE int32 [B, Hkv]
+ * Needs num_requests * num_kv_heads <= XATTN_MAX_REQUESTS (XATTN_EUNSUPPORTED
+ * otherwise).  Other arguments, outputs and errors as bsa_chunk_attention. */
+xattn_status bsa_chunk_attention_per_kv_head(const xattn_problem *p, const void *q,
+                                             const void *k_cur, const void *v_cur,
+                                             const void *k_pool, const void *v_pool,
+                                             const int32_t *sel_page, const int32_t *n_sel,
+                                             float softmax_scale, void *workspace,
+                                             size_t workspace_bytes, void *o, float *lse,
+                                             xattn_stream_t stream);
+
 /* merge_attention_outputs (BSA policy page, compute_chunked_prefill): for each
  * of `rows` rows, lse = log(exp(lse1) + exp(lse2)) and
  * o = o1 * exp(lse1 - lse) + o2 * exp(lse2 - lse); two empty parts (-inf, -inf)
@@ -242,7 +313,7 @@ xattn_status lse_merge(const float *o1, const float *lse1, const float *o2,
  *   k_pool[page][row][kvh][:] = k_cur[kvh][q0_r + t][:]   (v likewise),
  *   page = block_table[r][(kh_r + t) / block_size], row = (kh_r + t) % block_size,
  * which makes the chunk's blocks history for the request's next chunk.
- *   k_cur, v_cur    DEVICE bf16 [Hkv, tokens, D] (kv_head_stride), as for
+ *   k_cur, v_cur    DEVICE bf16 (kv_head_stride, kv_token_stride), as for
  *                   bsa_chunk_attention
  *   k_pool, v_pool  DEVICE bf16 [num_pages, block_size, Hkv, D], written
  * The block table row must reach the chunk's last block: (kh_r + lq_r) /

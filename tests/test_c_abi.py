@@ -45,6 +45,7 @@ int main(void) {
   p.block_table = (const int32_t *)0x10000;   /* device pointer: never read on the host */
   p.bt_stride = 64; p.num_pages = 256;
   p.q_head_stride = 1536 * 128; p.kv_head_stride = 1536 * 128; p.lse_head_stride = 1536;
+  p.kv_token_stride = 0;
 
   for (i = 0; i < sizeof(entry_points) / sizeof(entry_points[0]); ++i)
     if (!entry_points[i]) return 2;

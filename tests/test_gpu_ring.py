@@ -39,9 +39,7 @@ def test_q4b_128k_layer_ring_parity():
     ring = RN.LayerRing(cfg.ring_slots, P, Bk, Hkv, D, d)
     BT = torch.arange(P, dtype=torch.int32, device=d)[None]
     chunks = [0, 1, 2, L // chunk - 1]
-    problems = {c: X.Problem(H, Hkv, D, S, Bk, [chunk], [c * chunk], BT, P,
-                             q_head_stride=L * D, kv_head_stride=chunk * D, lse_head_stride=L)
-                for c in chunks}
+    problems = {c: RN.ring_problem(H, Hkv, D, S, Bk, L, chunk, c, BT, P) for c in chunks}
     bufs = RN.ChunkBuffers.for_problems(list(problems.values()), d, with_mask=True)
     outs = [(torch.zeros((H, L, D), dtype=torch.bfloat16, device=d),
              torch.zeros((H, L), dtype=torch.float32, device=d)) for _ in layers]

@@ -1,0 +1,230 @@
+"""GPU parity of the library's variants of the chunk path, through the C-ABI.
+
+* xattn_estimate_seq (keys in token order) against xattn_estimate (keys from
+  the pool pages): the same block sums bit for bit, for head-major and
+  token-major key layouts, a chunked sequence and the varlen batch.
+* k_cur / v_cur given as a [tokens, Hkv, D] view (kv_token_stride): the
+  same outputs as the packed [Hkv, tokens, D] copy.
+* one block set per KV head (xattn_select_per_kv_head ->
+  bsa_chunk_attention_per_kv_head): the selection bit-exact against the
+  oracle's per-KV-head selection on the GPU's block sums, the attention
+  within the usual bands of the oracle over each KV head's own pages.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import xattn_oracle as O
+from xattention_block_sparse_gb300 import inputs as I
+from xattention_block_sparse_gb300 import runner as RN
+from xattention_block_sparse_gb300 import xattn as X
+
+from gpu_common import SequenceCase, check_attention, check_block_sums, dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _estimate_both(prob, Q, Kc, KP, k_seq, starts, hs, ts, scale):
+    bufs = RN.ChunkBuffers.for_problems([prob], dev())
+    n = X.xattn_block_sums_count(prob)
+    X.xattn_estimate(prob, Q, Kc, KP, scale, bufs.workspace, bufs.block_sums)
+    a = bufs.block_sums[:n].clone()
+    bufs.block_sums.fill_(float("nan"))
+    X.xattn_estimate_seq(prob, Q, k_seq, starts, scale, bufs.workspace, bufs.block_sums,
+                         head_stride=hs, token_stride=ts)
+    b = bufs.block_sums[:n].clone()
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    return a, b
+
+
+@pytest.mark.parametrize("name", ["tiny", "q06b_4k"])
+def test_estimate_seq_equals_paged_estimate_every_chunk(name):
+    case = SequenceCase(name)
+    cfg = case.cfg
+    scale = RN.estimation_scale(cfg.D, cfg.stride)
+    Kt = case.K.permute(1, 0, 2).contiguous()   # [L, Hkv, D]: token-major keys
+    for c in range(case.L // case.chunk):
+        p, t0 = case.seq.problems[c], c * case.chunk
+        a, b = _estimate_both(p, case.Q[:, t0:], case.K[:, t0:], case.KP, case.K, [0],
+                              case.K.stride(0), 0, scale)
+        assert torch.equal(a, b), f"{name} chunk {c}: head-major keys"
+        _, b2 = _estimate_both(p, case.Q[:, t0:], case.K[:, t0:], case.KP, Kt, [0],
+                               cfg.D, cfg.Hkv * cfg.D, scale)
+        assert torch.equal(a, b2), f"{name} chunk {c}: token-major keys"
+
+
+def test_estimate_seq_equals_paged_estimate_varlen():
+    """Three requests (history 0, 16384, 65536 tokens): each request's keys,
+    history then chunk, are laid one after another in a [Hkv, tokens, D]
+    buffer with a gap between requests."""
+    wl = I.make_workload("varlen")
+    cfg, call = wl.cfg, wl.calls[0]
+    d = dev()
+    Q, Kc = to_dev_bf16(wl.q_bits), to_dev_bf16(wl.k_bits)
+    KP = to_dev_bf16(wl.kpool_bits)
+    BT = torch.from_numpy(wl.block_table).to(d)
+    prob = X.Problem(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, call.q_lens, call.kh_lens, BT,
+                     KP.shape[0])
+    parts, starts, pos = [], [], 0
+    for r in range(call.B):
+        nh = call.kh_lens[r] // cfg.block
+        hist = KP[BT[r, :nh].long()].permute(2, 0, 1, 3).reshape(cfg.Hkv, -1, cfg.D)
+        q0, q1 = int(call.cu_q[r]), int(call.cu_q[r + 1])
+        gap = torch.zeros((cfg.Hkv, 3 * cfg.stride, cfg.D), dtype=torch.bfloat16, device=d)
+        parts += [gap, hist, Kc[:, q0:q1]]
+        pos += gap.shape[1]
+        starts.append(pos)
+        pos += hist.shape[1] + (q1 - q0)
+    kseq = torch.cat(parts, dim=1).contiguous()
+    a, b = _estimate_both(prob, Q, Kc, KP, kseq, starts, kseq.stride(0), 0,
+                          RN.estimation_scale(cfg.D, cfg.stride))
+    assert torch.equal(a, b)
+
+
+def test_token_major_current_chunk_matches_packed():
+    """k_cur / v_cur as [tokens, Hkv, D] views (kv_head_stride = D,
+    kv_token_stride = Hkv * D) give exactly the block sums, selection, O and
+    LSE of the packed [Hkv, tokens, D] copies, and xattn_store_kv writes the
+    same pages from them."""
+    case = SequenceCase("q06b_4k")
+    cfg = case.cfg
+    c, t0 = 2, 2 * case.chunk
+    Kt = case.K.permute(1, 0, 2).contiguous()
+    Vt = case.V.permute(1, 0, 2).contiguous()
+    res = []
+    for tm in (False, True):
+        if tm:
+            p = X.Problem(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, [case.chunk], [t0],
+                          case.BT, case.KP.shape[0], q_head_stride=case.L * cfg.D,
+                          kv_head_stride=cfg.D, lse_head_stride=case.L,
+                          kv_token_stride=cfg.Hkv * cfg.D)
+            kc, vc = Kt[t0:], Vt[t0:]
+        else:
+            p = case.seq.problems[c]
+            kc, vc = case.K[:, t0:], case.V[:, t0:]
+        bufs = RN.ChunkBuffers.for_problems([p], dev(), with_mask=True)
+        O_ = torch.zeros((cfg.H, case.L, cfg.D), dtype=torch.bfloat16, device=dev())
+        LSE = torch.zeros((cfg.H, case.L), dtype=torch.float32, device=dev())
+        RN.prefill_chunk(p, case.Q[:, t0:], kc, vc, case.KP, case.VP, 0.9, bufs, O_[:, t0:],
+                         LSE[:, t0:])
+        kp, vp = torch.zeros_like(case.KP), torch.zeros_like(case.VP)
+        X.xattn_store_kv(p, kc, vc, kp, vp)
+        torch.cuda.synchronize()
+        assert X.xattn_device_error() == 0
+        n = int(bufs.n_sel[0].item())
+        res.append((bufs.block_sums.clone(), bufs.sel_page[0, :n].clone(), O_, LSE, kp, vp))
+    for x, y in zip(res[0], res[1]):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+
+
+def _per_kv_case(case, c, tau, vote=(1, 2)):
+    """Chunk c of a SequenceCase with one block set per KV head: returns the
+    GPU's block sums, mask, per-KV-head selection, O and LSE."""
+    cfg = case.cfg
+    p, t0 = case.seq.problems[c], c * case.chunk
+    bufs = RN.ChunkBuffers.for_problems([p], dev(), with_mask=True)
+    W = p.bt_stride
+    bufs.sel_idx = torch.full((cfg.Hkv, W), -7, dtype=torch.int32, device=dev())
+    bufs.sel_page = torch.full((cfg.Hkv, W), -7, dtype=torch.int32, device=dev())
+    bufs.n_sel = torch.full((cfg.Hkv,), -7, dtype=torch.int32, device=dev())
+    O_ = torch.zeros((cfg.H, case.L, cfg.D), dtype=torch.bfloat16, device=dev())
+    LSE = torch.zeros((cfg.H, case.L), dtype=torch.float32, device=dev())
+    RN.estimate_select(p, case.Q[:, t0:], case.K[:, t0:], case.KP, tau, bufs,
+                       k_seq=case.seq.key_seq(case.K), per_kv_head=True)
+    if vote != (1, 2):  # re-select with another ratio over the same block sums
+        X.xattn_select_per_kv_head(p, bufs.block_sums, tau, bufs.workspace, bufs.mask,
+                                   bufs.sel_idx, bufs.sel_page, bufs.n_sel, vote=vote)
+    RN.attend(p, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], case.KP, case.VP, bufs,
+              O_[:, t0:], LSE[:, t0:], per_kv_head=True)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    n = X.xattn_block_sums_count(p)
+    kbh, qb = t0 // cfg.block, case.chunk // cfg.block
+    bs = bufs.block_sums[:n].cpu().numpy().reshape(cfg.H, qb, kbh + qb)
+    mk = bufs.mask[:n].cpu().numpy().reshape(bs.shape).astype(bool)
+    sel = [bufs.sel_idx[k, :int(bufs.n_sel[k])].cpu().numpy() for k in range(cfg.Hkv)]
+    pages = [bufs.sel_page[k, :int(bufs.n_sel[k])].cpu().numpy() for k in range(cfg.Hkv)]
+    return bs, mk, sel, pages, O_.float().cpu().numpy(), LSE.cpu().numpy()
+
+
+@pytest.mark.parametrize("tau,vote", [(0.9, (1, 2)), (0.6, (1, 2)), (0.6, (0, 1))])
+def test_per_kv_head_selection_and_attention_q06b_4k(tau, vote):
+    case = SequenceCase("q06b_4k")
+    cfg = case.cfg
+    q, k, v, kp, vp = case.oracle_inputs()
+    bt_row = case.wl.block_table[0]
+    rng = np.random.default_rng(11)
+    for c in (1, 3):
+        t0, t1 = c * case.chunk, (c + 1) * case.chunk
+        kbh = t0 // cfg.block
+        bs, mk, sel, pages, Og, Lg = _per_kv_case(case, c, tau, vote)
+        # threshold masks and the per-KV-head vote against the oracle on the GPU's sums
+        want_mask = O.threshold_select(bs, tau)
+        assert np.array_equal(want_mask, mk), f"chunk {c}: mask"
+        want = O.per_kv_head_select(want_mask, cfg.Hkv, kbh, vote=vote)
+        for kvh in range(cfg.Hkv):
+            assert np.array_equal(sel[kvh], want[kvh]), f"chunk {c} kv {kvh}: ids"
+            assert np.array_equal(pages[kvh], bt_row[want[kvh]]), f"chunk {c} kv {kvh}: pages"
+        # attention of every KV head's group over its own pages
+        rows = sorted({0, case.chunk - 1, *rng.integers(0, case.chunk, 12).tolist()})
+        o_ref, l_ref = O.attend_request_per_kv(q[:, t0:t1], k[:, t0:t1], v[:, t0:t1], kp, vp,
+                                               [bt_row[w] for w in want], cfg.H, cfg.Hkv,
+                                               1 / math.sqrt(cfg.D), rows=rows)
+        idx = t0 + np.asarray(rows)
+        check_attention(Og[:, idx], Lg[:, idx], o_ref, l_ref, f"chunk {c}")
+
+
+def test_per_kv_head_varlen():
+    """The varlen batch with a selection per KV head: three requests x eight KV
+    heads run as 24 groups in one attention launch."""
+    wl = I.make_workload("varlen")
+    cfg, call = wl.cfg, wl.calls[0]
+    d = dev()
+    Q, K, V = to_dev_bf16(wl.q_bits), to_dev_bf16(wl.k_bits), to_dev_bf16(wl.v_bits)
+    KP, VP = to_dev_bf16(wl.kpool_bits), to_dev_bf16(wl.vpool_bits)
+    BT = torch.from_numpy(wl.block_table).to(d)
+    prob = X.Problem(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, call.q_lens, call.kh_lens, BT,
+                     KP.shape[0])
+    bufs = RN.ChunkBuffers.for_problems([prob], d, with_mask=True)
+    W = prob.bt_stride
+    bufs.sel_idx = torch.full((call.B, cfg.Hkv, W), -7, dtype=torch.int32, device=d)
+    bufs.sel_page = torch.full((call.B, cfg.Hkv, W), -7, dtype=torch.int32, device=d)
+    bufs.n_sel = torch.full((call.B, cfg.Hkv), -7, dtype=torch.int32, device=d)
+    tot = sum(call.q_lens)
+    O_ = torch.empty((cfg.H, tot, cfg.D), dtype=torch.bfloat16, device=d)
+    LSE = torch.empty((cfg.H, tot), dtype=torch.float32, device=d)
+    tau = 0.6
+    RN.prefill_chunk(prob, Q, K, V, KP, VP, tau, bufs, O_, LSE, per_kv_head=True)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    q, k, v = wl.f64("q"), wl.f64("k"), wl.f64("v")
+    kp, vp = wl.f64("kpool"), wl.f64("vpool")
+    bs_all, mask_all = bufs.block_sums.cpu().numpy(), bufs.mask.cpu().numpy()
+    sel_all, page_all = bufs.sel_idx.cpu().numpy(), bufs.sel_page.cpu().numpy()
+    nsel = bufs.n_sel.cpu().numpy()
+    Og, Lg = O_.float().cpu().numpy(), LSE.cpu().numpy()
+    rng = np.random.default_rng(3)
+    for r in range(call.B):
+        q0, q1 = int(call.cu_q[r]), int(call.cu_q[r + 1])
+        kbh, qb = call.kh_lens[r] // cfg.block, (q1 - q0) // cfg.block
+        off = X.xattn_block_sums_offset(prob, r)
+        bs = bs_all[off:off + cfg.H * qb * (kbh + qb)].reshape(cfg.H, qb, kbh + qb)
+        mk = mask_all[off:off + bs.size].reshape(bs.shape).astype(bool)
+        want_mask = O.threshold_select(bs, tau)
+        assert np.array_equal(want_mask, mk), f"request {r}: mask"
+        want = O.per_kv_head_select(want_mask, cfg.Hkv, kbh)
+        for kvh in range(cfg.Hkv):
+            n = int(nsel[r, kvh])
+            assert np.array_equal(sel_all[r, kvh, :n], want[kvh]), f"request {r} kv {kvh}"
+            assert np.array_equal(page_all[r, kvh, :n], wl.block_table[r][want[kvh]])
+        rows = sorted({0, q1 - q0 - 1, *rng.integers(0, q1 - q0, 8).tolist()})
+        o_ref, l_ref = O.attend_request_per_kv(
+            q[:, q0:q1], k[:, q0:q1], v[:, q0:q1], kp, vp,
+            [wl.block_table[r][w] for w in want], cfg.H, cfg.Hkv, 1 / math.sqrt(cfg.D),
+            rows=rows)
+        idx = q0 + np.asarray(rows)
+        check_attention(Og[:, idx], Lg[:, idx], o_ref, l_ref, f"request {r}")

@@ -68,8 +68,9 @@ def test_workspace_and_block_sum_sizes(lib):
     tstat = H * rq * (ncol // 128) * 8
     al = lambda x: (x + 255) // 256 * 256
     counts = al(al(bpart) + tstat)
-    part_o = al(counts + (512 + 1) * 4)  # vote counters + finishing counter; then attention
-                                         # partials: 160 CTAs x 2 slots x 256 rows
+    part_o = al(counts + (8 * 512 + 1) * 4)  # vote counters of every (request, KV head) +
+                                             # the finishing counter; then attention
+                                             # partials: 160 CTAs x 2 slots x 256 rows
     part_lse = al(part_o + 160 * 2 * 256 * 128 * 4)
     att_cnt = al(part_lse + 160 * 2 * 256 * 4)
     expect = al(att_cnt + 16 * 16 * 2 * 4)  # two part counters per 256-row attention unit
@@ -94,6 +95,10 @@ def test_workspace_and_block_sum_sizes(lib):
     dict(q_lens=[128] * 65, kh_lens=[0] * 65),       # too many requests
     dict(q_lens=[128], kh_lens=[0], q_head_stride=100),  # head stride too small
     dict(q_lens=[128], kh_lens=[128 * 8200], W=9000),    # > 8192 blocks in a row
+    dict(q_lens=[128], kh_lens=[0], kv_token_stride=100),  # token stride not 16-byte
+    dict(q_lens=[128], kh_lens=[0], kv_token_stride=64),   # token stride below head_dim
+    dict(q_lens=[256], kh_lens=[0], kv_head_stride=128 * 8,  # views of k_cur overlap
+         kv_token_stride=128 * 4),
 ])
 def test_invalid_problems_rejected(lib, kw):
     p = _prob(**kw)

@@ -52,7 +52,11 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   g.num_pages = p->num_pages;
   g.q_hs = p->q_head_stride;
   g.kv_hs = p->kv_head_stride;
+  g.kv_ts = p->kv_token_stride > 0 ? p->kv_token_stride : D;
+  g.kv_head_inner = g.kv_hs < g.kv_ts ? 1 : 0;
   g.lse_hs = p->lse_head_stride;
+  g.H_all = H;
+  g.Hkv_all = Hkv;
   g.block_table = p->block_table;
 
   int64_t gemm = 0, bsum = 0, sel = 0, att = 0;
@@ -106,10 +110,14 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   if (any_hist && (!p->block_table || p->num_pages < 1)) return XATTN_EINVAL;
   if (p->bt_stride < 0) return XATTN_EINVAL;
   const int64_t tot_q = p->cu_seqlens_q[B];
-  if (p->q_head_stride < tot_q * D || p->kv_head_stride < tot_q * D ||
-      p->lse_head_stride < tot_q)
+  if (p->q_head_stride < tot_q * D || p->lse_head_stride < tot_q) return XATTN_EINVAL;
+  // k_cur / v_cur: heads apart by kv_head_stride, tokens by kv_token_stride,
+  // either head-major [Hkv, tokens, D] or token-major [tokens, Hkv, D]
+  if (p->kv_token_stride < 0) return XATTN_EINVAL;
+  if (g.kv_ts < D || p->kv_head_stride < D) return XATTN_EINVAL;
+  if (!(p->kv_head_stride >= tot_q * g.kv_ts || g.kv_ts >= (int64_t)Hkv * p->kv_head_stride))
     return XATTN_EINVAL;
-  if (p->q_head_stride % 8 || p->kv_head_stride % 8) return XATTN_EALIGN;
+  if (p->q_head_stride % 8 || p->kv_head_stride % 8 || g.kv_ts % 8) return XATTN_EALIGN;
 
   pl.gemm_tiles = (int)gemm;
   pl.bsum_ctas = (int)bsum;
@@ -122,9 +130,11 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   w.counts = align_up(w.tstat + tstat * sizeof(float2));
   // attention partial results: two slots of kAttnRows rows per persistent CTA
   const size_t part_rows = (size_t)kAttnMaxCtas * 2 * kAttnRows;
-  // vote counters of every request, then the select kernel's finishing counter
-  w.part_o = align_up(w.counts + ((size_t)B * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) + 1) *
-                                     sizeof(int32_t));
+  // vote counters of every (request, KV head) -- one row per request for the
+  // vote across KV heads, one per KV head for the selection per KV head --
+  // then the select kernel's finishing counter
+  w.part_o = align_up(w.counts + ((size_t)B * Hkv * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) +
+                                  1) * sizeof(int32_t));
   w.part_lse = align_up(w.part_o + part_rows * D * sizeof(float));
   w.att_cnt = align_up(w.part_lse + part_rows * sizeof(float));
   w.total = align_up(w.att_cnt + (size_t)att * 2 * sizeof(int32_t));  // two per attention unit
@@ -198,6 +208,108 @@ xattn_status noalloc_counters(int32_t **out) {
 
 using namespace xattn;
 
+// Launches the estimation (score GEMM, then block sums) for a validated plan.
+static xattn_status run_estimate(Plan &pl, const void *q, const void *k_cur, const void *k_pool,
+                                 const KeySeq *kseq, float scale, void *workspace,
+                                 size_t workspace_bytes, float *block_sums, cudaStream_t st) {
+  xattn_status s;
+  if (!isfinite(scale)) return XATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(workspace) || !aligned16(block_sums)) return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  char *ws = static_cast<char *>(workspace);
+  float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
+  float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
+  s = cu(launch_score_gemm(pl.geo, pl.gemm_tiles, static_cast<const __nv_bfloat16 *>(q),
+                           static_cast<const __nv_bfloat16 *>(k_cur),
+                           static_cast<const __nv_bfloat16 *>(k_pool), kseq, scale, bpart, tstat,
+                           st));
+  if (s != XATTN_OK) return s;
+  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, bpart, tstat, block_sums, st));
+}
+
+// Checks shared by the selection entry points; counters come from the caller.
+static xattn_status check_select(const xattn_problem *p, const float *block_sums,
+                                 double threshold, int32_t vote_num, int32_t vote_den,
+                                 int32_t force_sink_last, const int32_t *sel_idx,
+                                 const int32_t *sel_page, const int32_t *n_sel) {
+  if (!block_sums || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
+  if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
+  if (!vote_ok(vote_num, vote_den, force_sink_last)) return XATTN_EINVAL;
+  if (p->bt_stride < 1) return XATTN_EINVAL;
+  if (reinterpret_cast<uintptr_t>(block_sums) & 3) return XATTN_EALIGN;
+  return XATTN_OK;
+}
+
+// Clears `rows` counter rows of bt_stride (plus the finishing counter) on the
+// stream and launches the selection.
+static xattn_status run_select(Plan &pl, const xattn_problem *p, const float *block_sums,
+                               double threshold, int32_t vote_num, int32_t vote_den,
+                               int32_t force_sink_last, int32_t *counts, int per_kv,
+                               uint8_t *mask, int32_t *sel_idx, int32_t *sel_page,
+                               int32_t *n_sel, cudaStream_t st) {
+  xattn_status s;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  const size_t rows = (size_t)pl.geo.B * (per_kv ? (size_t)pl.geo.Hkv : 1);
+  s = cu(cudaMemsetAsync(counts, 0, (rows * (size_t)p->bt_stride + 1) * sizeof(int32_t), st));
+  if (s != XATTN_OK) return s;
+  return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
+                          vote_num, vote_den, force_sink_last, per_kv, sel_idx, sel_page, n_sel,
+                          st));
+}
+
+// Launches the attention of a validated plan; per_kv: the selection holds one
+// page list per (request, KV head), and each request's KV-head groups run as
+// requests of their own (G query heads, one KV head).
+static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *q,
+                                  const void *k_cur, const void *v_cur, const void *k_pool,
+                                  const void *v_pool, const int32_t *sel_page,
+                                  const int32_t *n_sel, float softmax_scale, void *workspace,
+                                  size_t workspace_bytes, void *o, float *lse, int per_kv,
+                                  cudaStream_t st) {
+  xattn_status s;
+  if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse || !workspace)
+    return XATTN_EINVAL;
+  if ((!k_pool || !v_pool) && pl.geo.num_pages > 0) return XATTN_EINVAL;
+  if (p->bt_stride < 1) return XATTN_EINVAL;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return XATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(o) ||
+      (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)) || !aligned16(workspace))
+    return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
+  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  Geo g = pl.geo;
+  if (per_kv) {
+    // request r, KV head k -> request r * Hkv + k with the G query heads of
+    // the group; its selection row is r * Hkv + k of sel_page / n_sel
+    const int B = g.B, Hkv = g.Hkv, G = g.H / g.Hkv;
+    if ((int64_t)B * Hkv > kMaxReq) return XATTN_EUNSUPPORTED;
+    int att = 0;
+    for (int r = B - 1; r >= 0; --r)
+      for (int k = Hkv - 1; k >= 0; --k) g.req[r * Hkv + k] = pl.geo.req[r];
+    for (int v = 0; v < B * Hkv; ++v) {
+      ReqDesc &d = g.req[v];
+      d.head0 = (v % Hkv) * G;
+      d.kvh0 = v % Hkv;
+      d.att0 = att;
+      att += G * ((d.lq + kAttnRows - 1) / kAttnRows);
+    }
+    g.B = B * Hkv;
+    g.H = G;
+    g.Hkv = 1;
+  }
+  char *ws = static_cast<char *>(workspace);
+  return cu(launch_attention(g, pl.att_ctas, static_cast<const __nv_bfloat16 *>(q),
+                             static_cast<const __nv_bfloat16 *>(k_cur),
+                             static_cast<const __nv_bfloat16 *>(v_cur),
+                             static_cast<const __nv_bfloat16 *>(k_pool),
+                             static_cast<const __nv_bfloat16 *>(v_pool), sel_page, n_sel,
+                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse,
+                             reinterpret_cast<float *>(ws + pl.ws.part_o),
+                             reinterpret_cast<float *>(ws + pl.ws.part_lse),
+                             reinterpret_cast<int32_t *>(ws + pl.ws.att_cnt), st));
+}
+
 extern "C" {
 
 size_t xattn_workspace_size(const xattn_problem *p) {
@@ -226,22 +338,38 @@ xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k
   if (s != XATTN_OK) return s;
   if (!q || !k_cur || !workspace || !block_sums) return XATTN_EINVAL;
   if (!k_pool && pl.geo.num_pages > 0) return XATTN_EINVAL;
-  if (!isfinite(scale)) return XATTN_EINVAL;
-  if (!aligned16(q) || !aligned16(k_cur) || (k_pool && !aligned16(k_pool)) ||
-      !aligned16(workspace) || !aligned16(block_sums))
-    return XATTN_EALIGN;
-  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
-  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
-  char *ws = static_cast<char *>(workspace);
-  float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
-  float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  s = cu(launch_score_gemm(pl.geo, pl.gemm_tiles, static_cast<const __nv_bfloat16 *>(q),
-                           static_cast<const __nv_bfloat16 *>(k_cur),
-                           static_cast<const __nv_bfloat16 *>(k_pool), scale, bpart, tstat, st));
+  if (!aligned16(k_cur) || (k_pool && !aligned16(k_pool))) return XATTN_EALIGN;
+  return run_estimate(pl, q, k_cur, k_pool, nullptr, scale, workspace, workspace_bytes,
+                      block_sums, reinterpret_cast<cudaStream_t>(stream));
+}
+
+xattn_status xattn_estimate_seq(const xattn_problem *p, const void *q, const void *k_seq,
+                                int64_t k_seq_head_stride, int64_t k_seq_token_stride,
+                                const int64_t *k_seq_start, float scale, void *workspace,
+                                size_t workspace_bytes, float *block_sums,
+                                xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  return cu(launch_block_sum(pl.geo, pl.bsum_ctas, bpart, tstat,
-                             block_sums, st));
+  if (!q || !k_seq || !k_seq_start || !workspace || !block_sums) return XATTN_EINVAL;
+  const int D = p->head_dim, S = p->stride, Hkv = p->num_kv_heads;
+  const int64_t hs = k_seq_head_stride, ts = k_seq_token_stride > 0 ? k_seq_token_stride : D;
+  if (k_seq_token_stride < 0 || hs < D || ts < D) return XATTN_EINVAL;
+  if (!aligned16(k_seq) || hs % 8 || ts % 8) return XATTN_EALIGN;
+  int64_t end = 0;
+  for (int r = 0; r < p->num_requests; ++r) {
+    const int64_t st0 = k_seq_start[r];
+    const ReqDesc &d = pl.geo.req[r];
+    if (st0 < 0 || st0 % S) return XATTN_EINVAL;
+    if (st0 / S + (int64_t)(d.kh + d.lq) / S > INT32_MAX) return XATTN_EINVAL;
+    pl.geo.req[r].ks0 = (int32_t)(st0 / S);
+    if (st0 + d.kh + d.lq > end) end = st0 + d.kh + d.lq;
+  }
+  // the two views of the keys must not overlap: head-major or token-major
+  if (Hkv > 1 && !(hs >= end * ts || ts >= (int64_t)Hkv * hs)) return XATTN_EINVAL;
+  const KeySeq ks{static_cast<const __nv_bfloat16 *>(k_seq), hs, ts};
+  return run_estimate(pl, q, nullptr, nullptr, &ks, scale, workspace, workspace_bytes,
+                      block_sums, reinterpret_cast<cudaStream_t>(stream));
 }
 
 xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,
@@ -252,19 +380,34 @@ xattn_status xattn_select(const xattn_problem *p, const float *block_sums, doubl
   Plan pl;
   xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  if (!block_sums || !workspace || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
-  if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
-  if (!vote_ok(vote_num, vote_den, force_sink_last)) return XATTN_EINVAL;
-  if (p->bt_stride < 1) return XATTN_EINVAL;
-  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_sums) & 3)) return XATTN_EALIGN;
+  if (!workspace) return XATTN_EINVAL;
+  if ((s = check_select(p, block_sums, threshold, vote_num, vote_den, force_sink_last, sel_idx,
+                        sel_page, n_sel)) != XATTN_OK)
+    return s;
+  if (!aligned16(workspace)) return XATTN_EALIGN;
   if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
-  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + pl.ws.counts);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  s = cu(cudaMemsetAsync(counts, 0, ((size_t)pl.geo.B * p->bt_stride + 1) * sizeof(int32_t), st));
+  return run_select(pl, p, block_sums, threshold, vote_num, vote_den, force_sink_last, counts, 0,
+                    mask, sel_idx, sel_page, n_sel, reinterpret_cast<cudaStream_t>(stream));
+}
+
+xattn_status xattn_select_per_kv_head(const xattn_problem *p, const float *block_sums,
+                                      double threshold, int32_t vote_num, int32_t vote_den,
+                                      int32_t force_sink_last, void *workspace,
+                                      size_t workspace_bytes, uint8_t *mask, int32_t *sel_idx,
+                                      int32_t *sel_page, int32_t *n_sel, xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
-                          vote_num, vote_den, force_sink_last, sel_idx, sel_page, n_sel, st));
+  if (!workspace) return XATTN_EINVAL;
+  if ((s = check_select(p, block_sums, threshold, vote_num, vote_den, force_sink_last, sel_idx,
+                        sel_page, n_sel)) != XATTN_OK)
+    return s;
+  if (!aligned16(workspace)) return XATTN_EALIGN;
+  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
+  int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + pl.ws.counts);
+  return run_select(pl, p, block_sums, threshold, vote_num, vote_den, force_sink_last, counts, 1,
+                    mask, sel_idx, sel_page, n_sel, reinterpret_cast<cudaStream_t>(stream));
 }
 
 xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sums,
@@ -274,22 +417,17 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
   Plan pl;
   xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  if (!block_sums || !sel_idx || !sel_page || !n_sel) return XATTN_EINVAL;
-  if (!(threshold > 0.0) || !isfinite(threshold)) return XATTN_EINVAL;
-  if (!vote_ok(vote_num, vote_den, force_sink_last)) return XATTN_EINVAL;
-  if (p->bt_stride < 1) return XATTN_EINVAL;
-  if (reinterpret_cast<uintptr_t>(block_sums) & 3) return XATTN_EALIGN;
+  if ((s = check_select(p, block_sums, threshold, vote_num, vote_den, force_sink_last, sel_idx,
+                        sel_page, n_sel)) != XATTN_OK)
+    return s;
   const size_t n_counters = (size_t)pl.geo.B * (size_t)p->bt_stride;
   if (n_counters > (size_t)XATTN_NOALLOC_MAX_COUNTERS) return XATTN_EWORKSPACE;
-  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   int32_t *counts = nullptr;
   if ((s = noalloc_counters(&counts)) != XATTN_OK) return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's votes: clear the part this call uses
-  s = cu(cudaMemsetAsync(counts, 0, (n_counters + 1) * sizeof(int32_t), st));
-  if (s != XATTN_OK) return s;
-  return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
-                          vote_num, vote_den, force_sink_last, sel_idx, sel_page, n_sel, st));
+  // the array keeps the previous call's votes: run_select clears the part
+  // this call uses
+  return run_select(pl, p, block_sums, threshold, vote_num, vote_den, force_sink_last, counts, 0,
+                    mask, sel_idx, sel_page, n_sel, reinterpret_cast<cudaStream_t>(stream));
 }
 
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
@@ -300,27 +438,24 @@ xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const vo
   Plan pl;
   xattn_status s = make_plan(p, pl);
   if (s != XATTN_OK) return s;
-  if (!q || !k_cur || !v_cur || !sel_page || !n_sel || !o || !lse || !workspace)
-    return XATTN_EINVAL;
-  if ((!k_pool || !v_pool) && pl.geo.num_pages > 0) return XATTN_EINVAL;
-  if (p->bt_stride < 1) return XATTN_EINVAL;
-  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return XATTN_EINVAL;
-  if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(o) ||
-      (k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)) || !aligned16(workspace))
-    return XATTN_EALIGN;
-  if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
-  if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(workspace);
-  return cu(launch_attention(pl.geo, pl.att_ctas, static_cast<const __nv_bfloat16 *>(q),
-                             static_cast<const __nv_bfloat16 *>(k_cur),
-                             static_cast<const __nv_bfloat16 *>(v_cur),
-                             static_cast<const __nv_bfloat16 *>(k_pool),
-                             static_cast<const __nv_bfloat16 *>(v_pool), sel_page, n_sel,
-                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse,
-                             reinterpret_cast<float *>(ws + pl.ws.part_o),
-                             reinterpret_cast<float *>(ws + pl.ws.part_lse),
-                             reinterpret_cast<int32_t *>(ws + pl.ws.att_cnt), st));
+  return run_attention(pl, p, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
+                       workspace, workspace_bytes, o, lse, 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+xattn_status bsa_chunk_attention_per_kv_head(const xattn_problem *p, const void *q,
+                                             const void *k_cur, const void *v_cur,
+                                             const void *k_pool, const void *v_pool,
+                                             const int32_t *sel_page, const int32_t *n_sel,
+                                             float softmax_scale, void *workspace,
+                                             size_t workspace_bytes, void *o, float *lse,
+                                             xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  return run_attention(pl, p, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel, softmax_scale,
+                       workspace, workspace_bytes, o, lse, 1,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 xattn_status lse_merge(const float *o1, const float *lse1, const float *o2, const float *lse2,

@@ -194,6 +194,7 @@ __device__ void schedule(const Geo &g, Bars &bar, int Gsk) {
 // One contiguous piece of a unit handled by this CTA: tiles [t0, t1).
 struct Seg {
   int r, h, mt, t0, t1, kvh, m0, n_hist, uid;
+  int hq;          // query head of the tensors (h within the request's heads)
   int64_t ustart;  // work item of the unit's tile 0
   Unit u;
   bool partial;
@@ -223,7 +224,8 @@ __device__ __forceinline__ Seg make_seg(const Geo &g, const Bars &bar, int64_t p
   s.ustart = pos - s.t0;
   s.u = unit_geom<NK>(R, s.n_hist, s.mt);
   s.t1 = (int)min((int64_t)s.u.n_tiles, (int64_t)s.t0 + (end - pos));
-  s.kvh = s.h / (g.H / g.Hkv);
+  s.kvh = R.kvh0 + s.h / (g.H / g.Hkv);
+  s.hq = R.head0 + s.h;
   s.m0 = s.mt * ROWS;
   s.uid = bar.req_unit0[s.r] + s.h * ((R.lq + ROWS - 1) / ROWS) + s.mt;
   s.partial = !(s.t0 == 0 && s.t1 == s.u.n_tiles);
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(&bar.q_full[x], LY::Q_BYTES);
           for (int hf = 0; hf < LY::HALVES; ++hf)
             tma_load_3d(smem + LY::OFF_Q + x * LY::Q_BYTES + hf * (BM * 128), &tm.q,
-                        &bar.q_full[x], hf * 64, R.q0 + sg.m0 + x * BM, sg.h);
+                        &bar.q_full[x], hf * 64, R.q0 + sg.m0 + x * BM, sg.hq);
         }
         ++qn[x];
       }
@@ -382,9 +384,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                             sg.kvh, tok, p);
             } else {
               const int j0 = (t - sg.n_hist) * NK;
-              for (int hf = 0; hf < LY::HALVES; ++hf)
-                tma_load_3d(dst + hf * (NK * 128), kv ? &tm.vc : &tm.kc, &bar.full[s], hf * 64,
-                            R.q0 + j0, sg.kvh);
+              for (int hf = 0; hf < LY::HALVES; ++hf) {
+                if (g.kv_head_inner)  // k_cur / v_cur laid out [tokens, Hkv, D]
+                  tma_load_3d(dst + hf * (NK * 128), kv ? &tm.vc : &tm.kc, &bar.full[s],
+                              hf * 64, sg.kvh, R.q0 + j0);
+                else
+                  tma_load_3d(dst + hf * (NK * 128), kv ? &tm.vc : &tm.kc, &bar.full[s],
+                              hf * 64, R.q0 + j0, sg.kvh);
+              }
             }
           }
         }
@@ -654,8 +661,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       const int64_t prow = ((int64_t)csk * 2 + sg.slot) * ROWS + x * BM + row;
-      __nv_bfloat16 *orow = o + (int64_t)sg.h * g.q_hs + (int64_t)(R.q0 + qrow) * D;
-      float *lrow = lse + (int64_t)sg.h * g.lse_hs + R.q0 + qrow;
+      __nv_bfloat16 *orow = o + (int64_t)sg.hq * g.q_hs + (int64_t)(R.q0 + qrow) * D;
+      float *lrow = lse + (int64_t)sg.hq * g.lse_hs + R.q0 + qrow;
       if (nx > 0) {
         if (!mbar_wait(&bar.pv_done[x], (cnt - 1) & 1, abort, g.err)) break;
         tc_fence_after();
@@ -805,23 +812,29 @@ cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv
   TMaps tm;
   const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
   {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tot_q, (cuuint64_t)g.H};
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tot_q, (cuuint64_t)g.H_all};
     const cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)g.q_hs * 2};
     const cuuint32_t box[3] = {64, BM, 1};
     if (!encode_bf16(&tm.q, q, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tot_q, (cuuint64_t)g.Hkv};
-    const cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)g.kv_hs * 2};
+  if (g.kv_head_inner) {  // k_cur / v_cur as (d, head, token): [tokens, Hkv, D]
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)g.Hkv_all, (cuuint64_t)tot_q};
+    const cuuint64_t str[2] = {(cuuint64_t)g.kv_hs * 2, (cuuint64_t)g.kv_ts * 2};
+    const cuuint32_t box[3] = {64, 1, NK};
+    if (!encode_bf16(&tm.kc, kcur, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16(&tm.vc, vcur, 3, dims, str, box)) return cudaErrorInvalidValue;
+  } else {  // (d, token, head): [Hkv, tokens, D]
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tot_q, (cuuint64_t)g.Hkv_all};
+    const cuuint64_t str[2] = {(cuuint64_t)g.kv_ts * 2, (cuuint64_t)g.kv_hs * 2};
     const cuuint32_t box[3] = {64, NK, 1};
     if (!encode_bf16(&tm.kc, kcur, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_bf16(&tm.vc, vcur, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   if (g.num_pages > 0 && kpool && vpool) {
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)g.Hkv, (cuuint64_t)g.Bk,
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)g.Hkv_all, (cuuint64_t)g.Bk,
                                 (cuuint64_t)g.num_pages};
-    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)g.Hkv * D * 2,
-                               (cuuint64_t)g.Bk * g.Hkv * D * 2};
+    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)g.Hkv_all * D * 2,
+                               (cuuint64_t)g.Bk * g.Hkv_all * D * 2};
     const cuuint32_t box[4] = {64, 1, NK, 1};
     if (!encode_bf16(&tm.kp, kpool, 4, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_bf16(&tm.vp, vpool, 4, dims, str, box)) return cudaErrorInvalidValue;

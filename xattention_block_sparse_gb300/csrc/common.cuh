@@ -25,7 +25,10 @@ struct ReqDesc {
   int32_t bsum0;   // first CTA of the request in the block-sum grid
   int32_t sel0;    // ... in the selection grid
   int32_t att0;    // ... in the attention grid
-  int32_t pad_;
+  int32_t ks0;     // xattn_estimate_seq: first key group (token / S) of the request's keys
+  int32_t head0;   // first query head of the request's heads (nonzero only when a
+                   // request stands for one KV head's group: per-KV-head attention)
+  int32_t kvh0;    // KV head of head0 (idem)
   int64_t bpart_off;  // float offset of the request's [H, Qb, Kb, Br] block partial sums
   int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
   int64_t bs_off;     // offset of its [H, Qb, Kb] block sums / mask
@@ -34,6 +37,9 @@ struct ReqDesc {
 struct Geo {
   int32_t B, H, Hkv, D, S, Bk, bt_stride, num_pages;
   int64_t q_hs, kv_hs, lse_hs;
+  int64_t kv_ts;          // elements between tokens of k_cur / v_cur
+  int32_t kv_head_inner;  // 1 when kv_hs < kv_ts (a [tokens, Hkv, D] layout)
+  int32_t H_all, Hkv_all; // heads of the q / k tensors (H, Hkv unless a request is one group)
   const int32_t *block_table;
   int32_t *err;  // device error word
   ReqDesc req[kMaxReq];
@@ -70,18 +76,30 @@ struct WsLayout {
   size_t bpart, tstat, counts, part_o, part_lse, att_cnt, total;
 };
 
+// Keys of every request in logical order (xattn_estimate_seq): element
+// (kv head h, token t, d) at base[h * hs + t * ts + d]; request r's keys start
+// at token S * req[r].ks0.
+struct KeySeq {
+  const __nv_bfloat16 *base;
+  int64_t hs, ts;
+};
+
+// Score GEMM with its epilogue (block partial sums, tile statistics).  Keys
+// come from kseq when it is given, else from the pool pages and k_cur.
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
-                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
-                              float *bpart, float2 *tstat, cudaStream_t st);
+                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool,
+                              const KeySeq *kseq, float scale, float *bpart, float2 *tstat,
+                              cudaStream_t st);
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
                              float *block_sums, cudaStream_t st);
 // Threshold selection of every (request, KV head, query block), then the GQA
 // vote of every request (run by the CTA that finishes last; counts must hold
-// B * bt_stride + 1 zeroed int32: the vote counters and the finishing counter).
+// rows * bt_stride + 1 zeroed int32: the vote counters and the finishing
+// counter, with rows = B, or B * Hkv when per_kv: one selection per KV head).
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
                           double threshold, uint8_t *mask, int32_t *counts, int vote_num,
-                          int vote_den, int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
-                          int32_t *n_sel, cudaStream_t st);
+                          int vote_den, int force_sink_last, int per_kv, int32_t *sel_idx,
+                          int32_t *sel_page, int32_t *n_sel, cudaStream_t st);
 cudaError_t launch_attention(const Geo &g, int nctas, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *vcur,
                              const __nv_bfloat16 *kpool, const __nv_bfloat16 *vpool,

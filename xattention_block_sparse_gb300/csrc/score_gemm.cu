@@ -10,23 +10,24 @@
 //                     MMA tiles; both accumulators fill the 512 TMEM columns).
 //                     The stride reversal costs nothing: TMA views (d, phase,
 //                     group, ...) of q and of the keys pick phase S-1-i of q for
-//                     the k-step that uses phase i of k.  The keys are read where
-//                     they live: a tile's 256 reshaped columns are 256/Br boxes of
-//                     Br rows, each one history page -- a 5-D view
-//                     (d, KV head, phase, group, page) of the pool, addressed
-//                     through the block table -- or Br columns of the current
-//                     chunk; the boxes land back to back, which is the layout of
-//                     one 256-row box.
-//                     When the query heads per KV head are even, two CTAs
-//                     of a cluster take the same tile of two heads of one KV
-//                     group: their key tiles are identical, so each CTA loads
-//                     half of the key boxes and multicasts them to both, which
-//                     halves the TMA box count that limits this kernel.
+//                     the k-step that uses phase i of k.  Two key sources:
+//                     * pages (xattn_estimate): a tile's 256 reshaped columns
+//                       are 256/Br boxes of Br rows, each one history page -- a
+//                       5-D view (d, KV head, phase, group, page) of the pool,
+//                       addressed through the block table -- or Br columns of
+//                       the current chunk; the boxes land back to back, which is
+//                       the layout of one 256-row box;
+//                     * a logical-order key sequence (xattn_estimate_seq): the
+//                       request's history and current keys in token order, so
+//                       the tile's 256 columns at phase i are one strided box of
+//                       256 rows -- one TMA instruction per k-step instead of
+//                       256/Br (the box count per SM is what bounds the paged
+//                       form).
 //                     A launch's last wave, when it would fill at most half of
 //                     the SMs, runs its tiles as 256 x 128 halves instead.
 //     warp 0       TMA producer over an NST-stage ring (runs ahead into the
-//                  next tile while the epilogue drains TMEM); lane q issues
-//                  key box q of each k-step (of this CTA's half in a pair)
+//                  next tile while the epilogue drains TMEM); paged form: lane
+//                  q issues key box q of each k-step
 //     warp 1       MMA issuer: per k-step 4 x tcgen05.mma (K = 16) per M tile
 //     warps 4..11  epilogue, one thread per row, per 128-column statistics
 //                  tile: the tile max m_t over the visible cells, and for each
@@ -42,6 +43,8 @@
 //                  exactly the two-pass normalise-then-sum of the pages, with
 //                  pass 2 folded into pass 1 per tile.  Tiles right of the
 //                  causal diagonal are never scheduled.
+#include <string.h>
+
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -70,7 +73,11 @@ struct Bars {
 };
 
 struct Maps {
-  CUtensorMap q, kp, kc;  // queries, pool keys (5-D), current-chunk keys (4-D)
+  CUtensorMap q;         // queries (d, phase, group, head)
+  CUtensorMap kp, kc;    // paged form: pool keys (5-D), current-chunk keys (4-D)
+  CUtensorMap ks, ksh;   // sequence form: logical-order keys, 256- and 128-row boxes
+  int kc_head_inner;     // the current-chunk key view is (d, head, phase, group)
+  int ks_head_inner;     // the key-sequence view is (d, head, phase, group)
 };
 
 struct Tile {
@@ -79,13 +86,9 @@ struct Tile {
 };
 
 // Tile t of the score GEMM: requests in order, then head, then row tile, then
-// column tile; only tiles holding visible cells exist.  With PAIR the index runs
-// over head pairs (2p, 2p + 1) -- two query heads of one KV group, which read the
-// same key tile -- and the CTA of cluster rank `rank` takes head 2p + rank.
-template <bool PAIR>
-__device__ __forceinline__ Tile decode_tile(const Geo &g, int t, int rank) {
-  constexpr int div = PAIR ? 2 : 1;
-  const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0 / div; });
+// column tile; only tiles holding visible cells exist.
+__device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
+  const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0; });
   const ReqDesc &R = g.req[r];
   const int S = g.S;
   const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
@@ -94,12 +97,11 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t, int rank) {
     const int vis = min(ch + min(m0 + ROWS, rq), ncol);
     per_head += (vis + COLS - 1) / COLS;
   }
-  int local = t - R.gemm0 / div;
+  int local = t - R.gemm0;
   Tile tl;
   tl.r = r;
   tl.h = local / per_head;
   local -= tl.h * per_head;
-  if (PAIR) tl.h = 2 * tl.h + rank;
   for (int m0 = 0; m0 < rq; m0 += ROWS) {
     const int vis = min(ch + min(m0 + ROWS, rq), ncol);
     const int n = (vis + COLS - 1) / COLS;
@@ -117,21 +119,22 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t, int rank) {
 // Work item w of the launch: tiles 0..nfull-1 whole, then the remaining tiles
 // as two 128-column halves each (the launch's last wave, so that it spreads
 // over as many SMs as it can fill).
-template <bool PAIR>
-__device__ __forceinline__ Tile decode_work(const Geo &g, int w, int nfull, int rank) {
+__device__ __forceinline__ Tile decode_work(const Geo &g, int w, int nfull) {
   if (w < nfull) {
-    Tile tl = decode_tile<PAIR>(g, w, rank);
+    Tile tl = decode_tile(g, w);
     tl.w = COLS;
     return tl;
   }
   const int hh = w - nfull;
-  Tile tl = decode_tile<PAIR>(g, nfull + hh / 2, rank);
+  Tile tl = decode_tile(g, nfull + hh / 2);
   tl.n0 += (hh & 1) * (COLS / 2);
   tl.w = COLS / 2;
   return tl;
 }
 
-template <int BR, bool PAIR>
+// SEQ: keys from the logical-order key sequence (one box per k-step), else
+// from the pool pages and the current chunk (one box per page per k-step).
+template <int BR, bool SEQ>
 __global__ void __launch_bounds__(THREADS, 1)
     score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int nwork,
                       int nfull, float scale, float *__restrict__ bpart,
@@ -145,16 +148,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = g.S, D = g.D;
   const int ksteps = S * D / KSTEP;
-  const int rank = PAIR ? (int)cluster_rank() : 0;
-  // a pair's tiles: cluster c of the grid walks pair tiles c, c + nclusters, ...
-  const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int tile0 = (int)blockIdx.x, tstep = (int)gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar.full[s], 1);
-      // with PAIR a slot is refilled (in both CTAs) once both CTAs' MMAs read it
-      mbar_init(&bar.empty[s], PAIR ? 2 : 1);
+      mbar_init(&bar.empty[s], 1);
     }
     mbar_init(&bar.acc_full, 1);
     mbar_init(&bar.acc_empty, 8);  // one arrival per epilogue warp
@@ -168,8 +167,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the peer's multicast loads and commits target barriers this CTA has initialised
-  if (PAIR) cluster_sync();
   const uint32_t tmem = bar.tmem_base;
 
   if (warp == 0) {
@@ -178,25 +175,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     static_assert(COLS / BR <= 32 && SUB_BYTES % 1024 == 0, "key boxes");
     if (lane == 0) {
       tma_prefetch_desc(&mp.q);
-      tma_prefetch_desc(&mp.kp);
-      tma_prefetch_desc(&mp.kc);
+      if (SEQ) {
+        tma_prefetch_desc(&mp.ks);
+        tma_prefetch_desc(&mp.ksh);
+      } else {
+        tma_prefetch_desc(&mp.kp);
+        tma_prefetch_desc(&mp.kc);
+      }
     }
     int it = 0;  // k-steps issued so far (ring position)
     bool ok = true;
     for (int t = tile0; ok && t < nwork; t += tstep) {
-      const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
+      const Tile tl = decode_work(g, t, nfull);
       const ReqDesc &R = g.req[tl.r];
       const int kvh = tl.h / (g.H / g.Hkv);
-      const int nsub = tl.w / BR;                 // key boxes per k-step
-      const int nown = PAIR ? nsub / 2 : nsub;    // boxes this CTA issues (PAIR: to both CTAs)
-      const int box = rank * nown + lane;         // the key box this lane issues
+      const int nsub = tl.w / BR;  // paged form: key boxes per k-step
       const int ch = R.kh / S, ncol = (R.kh + R.lq) / S;
-      // this lane's key box: reshaped columns [b, b + Br) are one history page
-      // (its block-table entry) or Br groups of the current chunk
+      // paged form, this lane's key box: reshaped columns [b, b + Br) are one
+      // history page (its block-table entry) or Br groups of the current chunk
       bool hist = false;
       int src = R.q0 / S;  // columns past the last one: any in-bounds box (masked)
-      if (lane < nown) {
-        const int b = tl.n0 + box * BR;
+      if (!SEQ && lane < nsub) {
+        const int b = tl.n0 + lane * BR;
         if (b < ch) {
           hist = true;
           src = page_of(g, tl.r, b / BR);  // -1 (and a recorded error) if out of the pool
@@ -221,18 +221,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(&bar.full[s], A_BYTES + tl.w * KSTEP * 2);
           // q rows S*a + S-1-i of this tile
           tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
-        }
-        __syncwarp();
-        if (lane < nown) {  // key rows S*b + i
-          uint8_t *dst = sA + A_BYTES + box * SUB_BYTES;
-          if (PAIR) {
-            if (hist)
-              tma_load_5d_mc(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src, 3);
+          if (SEQ) {  // key rows S*b + i, b over the tile's columns: one box
+            const CUtensorMap *km = tl.w == COLS ? &mp.ks : &mp.ksh;
+            const int grp = R.ks0 + tl.n0;
+            if (mp.ks_head_inner)
+              tma_load_4d(sA + A_BYTES, km, &bar.full[s], dc, kvh, i, grp);
             else
-              tma_load_4d_mc(dst, &mp.kc, &bar.full[s], dc, i, src, kvh, 3);
-          } else {
+              tma_load_4d(sA + A_BYTES, km, &bar.full[s], dc, i, grp, kvh);
+          }
+        }
+        if (!SEQ) {
+          __syncwarp();
+          if (lane < nsub) {  // key rows S*b + i
+            uint8_t *dst = sA + A_BYTES + lane * SUB_BYTES;
             if (hist)
               tma_load_5d(dst, &mp.kp, &bar.full[s], dc, kvh, i, 0, src);
+            else if (mp.kc_head_inner)
+              tma_load_4d(dst, &mp.kc, &bar.full[s], dc, kvh, i, src);
             else
               tma_load_4d(dst, &mp.kc, &bar.full[s], dc, i, src, kvh);
           }
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0, n = 0;
       bool ok = true;
       for (int t = tile0; ok && t < nwork; t += tstep, ++n) {
-        const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
+        const Tile tl = decode_work(g, t, nfull);
         const uint32_t idesc = tl.w == COLS ? idesc_w : idesc_h;
         const int rq = g.req[tl.r].lq / S;
         const bool two_m = tl.m0 + TM < rq;
@@ -277,23 +282,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               mma_f16_ss(tmem + x * COLS, a0 + (uint64_t)((x * (TM * 128) + kq * 32) >> 4),
                          b0 + (uint64_t)((kq * 32) >> 4), idesc, (ks > 0 || kq > 0) ? 1u : 0u);
           }
-          if (PAIR)
-            mma_commit_mc(&bar.empty[s], 3);  // both CTAs' slot s may be refilled
-          else
-            mma_commit(&bar.empty[s]);
+          mma_commit(&bar.empty[s]);
         }
         mma_commit(&bar.acc_full);
       }
       // every MMA issued has completed before TMEM is freed: the epilogue waited
-      // for each tile's acc_full, and no MMA follows the last commit.  With PAIR
-      // the peer's arrivals on this CTA's slots have landed too before it exits.
-      if (PAIR) {
-        for (int k = max(0, it - NST); k < it; ++k) {
-          const uint32_t par = (k / NST) & 1;
-          for (uint32_t q = 0; q < kSpinLimit && !mbar_try_wait(&bar.empty[k % NST], par); ++q) {
-          }
-        }
-      }
+      // for each tile's acc_full, and no MMA follows the last commit
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
@@ -302,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + x * COLS;
     int n = 0;
     for (int t = tile0; t < nwork; t += tstep, ++n) {
-      const Tile tl = decode_work<PAIR>(g, t, nfull, rank);
+      const Tile tl = decode_work(g, t, nfull);
       const ReqDesc &R = g.req[tl.r];
       const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
       const int nj = tl.w / kTileCols;  // statistics tiles of the work item
@@ -372,91 +366,98 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // no CTA of a pair leaves while the other may still write its shared memory
-  if (PAIR) cluster_sync();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// A view (d, phase, group, head) of a [heads, tokens, D]-strided bf16 tensor,
+// or (d, head, phase, group) when heads are closer than tokens (a
+// [tokens, heads, D] layout), so that the strides of the view grow; returns
+// whether the head comes second.  box_rows groups of one phase per box.
+bool encode_phase_view(CUtensorMap *m, const void *base, int D, int S, int64_t groups,
+                       int heads, int64_t hs, int64_t ts, int box_rows, bool *head_inner) {
+  *head_inner = hs < ts;
+  if (*head_inner) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)S,
+                                (cuuint64_t)groups};
+    const cuuint64_t str[3] = {(cuuint64_t)hs * 2, (cuuint64_t)ts * 2, (cuuint64_t)S * ts * 2};
+    const cuuint32_t box[4] = {KSTEP, 1, 1, (cuuint32_t)box_rows};
+    return encode_bf16(m, base, 4, dims, str, box);
+  }
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)groups,
+                              (cuuint64_t)heads};
+  const cuuint64_t str[3] = {(cuuint64_t)ts * 2, (cuuint64_t)S * ts * 2, (cuuint64_t)hs * 2};
+  const cuuint32_t box[4] = {KSTEP, 1, (cuuint32_t)box_rows, 1};
+  return encode_bf16(m, base, 4, dims, str, box);
 }
 
 }  // namespace
 
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
-                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool, float scale,
-                              float *bpart, float2 *tstat, cudaStream_t st) {
+                              const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool,
+                              const KeySeq *kseq, float scale, float *bpart, float2 *tstat,
+                              cudaStream_t st) {
   if (ntiles == 0) return cudaSuccess;
   const int S = g.S, D = g.D, BRc = g.Bk / S;
   const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
   Maps mp;
-  {  // q as (d, phase i, group, head)
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(tot_q / S),
-                                (cuuint64_t)g.H};
-    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2, (cuuint64_t)g.q_hs * 2};
-    const cuuint32_t box[4] = {KSTEP, 1, ROWS, 1};
-    if (!encode_bf16(&mp.q, q, 4, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  {  // current-chunk keys as (d, phase i, group, kv head), Br groups per box
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)(tot_q / S),
-                                (cuuint64_t)g.Hkv};
-    const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2, (cuuint64_t)g.kv_hs * 2};
-    const cuuint32_t box[4] = {KSTEP, 1, (cuuint32_t)BRc, 1};
-    if (!encode_bf16(&mp.kc, kcur, 4, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  if (g.num_pages > 0 && kpool) {  // pool keys as (d, kv head, phase i, group, page)
-    const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)g.Hkv, (cuuint64_t)S, (cuuint64_t)BRc,
-                                (cuuint64_t)g.num_pages};
-    const cuuint64_t str[4] = {(cuuint64_t)D * 2, (cuuint64_t)g.Hkv * D * 2,
-                               (cuuint64_t)S * g.Hkv * D * 2, (cuuint64_t)g.Bk * g.Hkv * D * 2};
-    const cuuint32_t box[5] = {KSTEP, 1, 1, (cuuint32_t)BRc, 1};
-    if (!encode_bf16(&mp.kp, kpool, 5, dims, str, box)) return cudaErrorInvalidValue;
+  memset(&mp, 0, sizeof(mp));
+  bool hi = false;
+  // q as (d, phase i, group, head)
+  if (!encode_phase_view(&mp.q, q, D, S, tot_q / S, g.H, g.q_hs, D, ROWS, &hi))
+    return cudaErrorInvalidValue;
+  if (kseq) {
+    // the keys of every request in logical order: as many groups as the
+    // furthest request reaches
+    int64_t groups = 1;
+    for (int r = 0; r < g.B; ++r) {
+      const int64_t e = (int64_t)g.req[r].ks0 + (g.req[r].kh + g.req[r].lq) / S;
+      if (e > groups) groups = e;
+    }
+    if (!encode_phase_view(&mp.ks, kseq->base, D, S, groups, g.Hkv, kseq->hs, kseq->ts, COLS,
+                           &hi))
+      return cudaErrorInvalidValue;
+    mp.ks_head_inner = hi;
+    if (!encode_phase_view(&mp.ksh, kseq->base, D, S, groups, g.Hkv, kseq->hs, kseq->ts,
+                           COLS / 2, &hi))
+      return cudaErrorInvalidValue;
   } else {
-    mp.kp = mp.kc;  // no history anywhere: never used
+    // current-chunk keys, Br groups per box
+    if (!encode_phase_view(&mp.kc, kcur, D, S, tot_q / S, g.Hkv, g.kv_hs, g.kv_ts, BRc, &hi))
+      return cudaErrorInvalidValue;
+    mp.kc_head_inner = hi;
+    if (g.num_pages > 0 && kpool) {  // pool keys as (d, kv head, phase i, group, page)
+      const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)g.Hkv, (cuuint64_t)S,
+                                  (cuuint64_t)BRc, (cuuint64_t)g.num_pages};
+      const cuuint64_t str[4] = {(cuuint64_t)D * 2, (cuuint64_t)g.Hkv * D * 2,
+                                 (cuuint64_t)S * g.Hkv * D * 2, (cuuint64_t)g.Bk * g.Hkv * D * 2};
+      const cuuint32_t box[5] = {KSTEP, 1, 1, (cuuint32_t)BRc, 1};
+      if (!encode_bf16(&mp.kp, kpool, 5, dims, str, box)) return cudaErrorInvalidValue;
+    } else {
+      mp.kp = mp.kc;  // no history anywhere: never used
+    }
   }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidValue;
-  // Pairs of query heads of one KV group run as 2-CTA clusters that share each
-  // key tile: every CTA issues half of the key boxes, multicast to both.
-  const bool pair = (g.H / g.Hkv) % 2 == 0;
   auto run = [&](auto kernel) {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_ALLOC;
-    cfg.stream = st;
-    int units = ntiles, slots = sms;
-    if (pair) {
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      cfg.gridDim = dim3(2);
-      int ncl = 0;
-      e = cudaOccupancyMaxActiveClusters(&ncl, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-      if (ncl < 1) return cudaErrorInvalidConfiguration;
-      units = ntiles / 2;  // head pairs
-      slots = ncl;
-    }
-    // A last wave that fills at most half of the slots runs as half-width tiles
+    // A last wave that fills at most half of the SMs runs as half-width tiles
     // (twice as many, each half the time).
-    const int rem = units % slots;
-    const int nfull = (rem > 0 && 2 * rem <= slots) ? units - rem : units;
-    const int nwork = nfull + 2 * (units - nfull);
-    const int n = nwork < slots ? nwork : slots;
-    cfg.gridDim = dim3(pair ? 2 * n : n);
-    e = cudaLaunchKernelEx(&cfg, kernel, g, mp, nwork, nfull, scale, bpart, tstat);
-    if (e != cudaSuccess) return e;
+    const int rem = ntiles % sms;
+    const int nfull = (rem > 0 && 2 * rem <= sms) ? ntiles - rem : ntiles;
+    const int nwork = nfull + 2 * (ntiles - nfull);
+    const int n = nwork < sms ? nwork : sms;
+    kernel<<<n, THREADS, SMEM_ALLOC, st>>>(g, mp, nwork, nfull, scale, bpart, tstat);
     return cudaGetLastError();
   };
+  const bool sq = kseq != nullptr;
   switch (g.Bk / S) {  // Br: reshaped columns per KV block
-    case 8: return pair ? run(score_gemm_kernel<8, true>) : run(score_gemm_kernel<8, false>);
-    case 16: return pair ? run(score_gemm_kernel<16, true>) : run(score_gemm_kernel<16, false>);
-    case 32: return pair ? run(score_gemm_kernel<32, true>) : run(score_gemm_kernel<32, false>);
+    case 8: return sq ? run(score_gemm_kernel<8, true>) : run(score_gemm_kernel<8, false>);
+    case 16: return sq ? run(score_gemm_kernel<16, true>) : run(score_gemm_kernel<16, false>);
+    case 32: return sq ? run(score_gemm_kernel<32, true>) : run(score_gemm_kernel<32, false>);
     default: return cudaErrorInvalidValue;
   }
 }

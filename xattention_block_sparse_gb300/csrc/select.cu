@@ -62,16 +62,19 @@ __device__ unsigned long long block_excl_scan(unsigned long long v, unsigned lon
 // The vote of request r by the whole CTA (STHR threads): keep history block j
 // when votes_j * den > num * Hkv * Qb, or when forced (sink / last block);
 // ascending compaction into sel_idx, page lookup into sel_page, count in n_sel.
-__device__ void vote_request(const Geo &g, int r, const int32_t *counts, int vote_num,
+// kvh >= 0: the vote of that KV head alone (its votes over its Qb query
+// blocks, out of Qb), in row r * Hkv + kvh of the counters and outputs.
+__device__ void vote_request(const Geo &g, int r, int kvh, const int32_t *counts, int vote_num,
                              int vote_den, int force, int32_t *sel_idx, int32_t *sel_page,
                              int32_t *n_sel, unsigned long long *wbuf) {
   const ReqDesc &R = g.req[r];
   const int kbh = R.kh / g.Bk, Qb = R.lq / g.Bk;
-  const int64_t votes_total = (int64_t)g.Hkv * Qb;
+  const int64_t votes_total = kvh < 0 ? (int64_t)g.Hkv * Qb : (int64_t)Qb;
+  const int64_t row = kvh < 0 ? r : (int64_t)r * g.Hkv + kvh;
   const int tid = threadIdx.x;
   const int per = (kbh + STHR - 1) / STHR;
   const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
-  const int32_t *cnt = counts + (int64_t)r * g.bt_stride;
+  const int32_t *cnt = counts + row * g.bt_stride;
   auto keep = [&](int j) {
     return (int64_t)__ldcg(cnt + j) * vote_den > (int64_t)vote_num * votes_total ||
            (force && (j == 0 || j == kbh - 1));
@@ -82,7 +85,7 @@ __device__ void vote_request(const Geo &g, int r, const int32_t *counts, int vot
   unsigned long long pos = block_excl_scan(mine, wbuf, &total);
   for (int j = beg; j < end; ++j) {
     if (keep(j)) {
-      const int64_t o = (int64_t)r * g.bt_stride + (int64_t)pos;
+      const int64_t o = row * g.bt_stride + (int64_t)pos;
       sel_idx[o] = j;
       int p = g.block_table[(int64_t)r * g.bt_stride + j];
       if (p < 0 || p >= g.num_pages) {
@@ -93,7 +96,7 @@ __device__ void vote_request(const Geo &g, int r, const int32_t *counts, int vot
       ++pos;
     }
   }
-  if (tid == 0) n_sel[r] = (int32_t)total;
+  if (tid == 0) n_sel[row] = (int32_t)total;
 }
 
 __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Geo g,
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Ge
                                                       uint8_t *__restrict__ mask,
                                                       int32_t *__restrict__ counts, int nkeys,
                                                       int vote_num, int vote_den, int force,
+                                                      int per_kv,
                                                       int32_t *__restrict__ sel_idx,
                                                       int32_t *__restrict__ sel_page,
                                                       int32_t *__restrict__ n_sel,
@@ -230,8 +234,10 @@ __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Ge
     }
     __syncthreads();
   }
+  // votes: per request (over its KV heads), or per (request, KV head)
+  int32_t *crow = counts + (per_kv ? (int64_t)r * g.Hkv + kvh : (int64_t)r) * g.bt_stride;
   for (int j = tid; j < kbh; j += STHR)
-    if (anyf[j]) atomicAdd(counts + (int64_t)r * g.bt_stride + j, 1);
+    if (anyf[j]) atomicAdd(crow + j, 1);
 
   // the CTA that finishes last has every vote counted: it runs the votes
   __shared__ int last;
@@ -241,29 +247,38 @@ __global__ void __launch_bounds__(STHR) select_kernel(const __grid_constant__ Ge
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int rr = 0; rr < g.B; ++rr)
-    vote_request(g, rr, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
+  for (int rr = 0; rr < g.B; ++rr) {
+    if (per_kv) {
+      for (int k = 0; k < g.Hkv; ++k)
+        vote_request(g, rr, k, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
+    } else {
+      vote_request(g, rr, -1, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(STHR) vote_kernel(const __grid_constant__ Geo g,
                                                     const int32_t *__restrict__ counts,
                                                     int vote_num, int vote_den, int force,
+                                                    int per_kv,
                                                     int32_t *__restrict__ sel_idx,
                                                     int32_t *__restrict__ sel_page,
                                                     int32_t *__restrict__ n_sel) {
   __shared__ unsigned long long wbuf[SWARPS + 1];
-  vote_request(g, blockIdx.x, counts, vote_num, vote_den, force, sel_idx, sel_page, n_sel, wbuf);
+  const int r = per_kv ? blockIdx.x / g.Hkv : blockIdx.x;
+  vote_request(g, r, per_kv ? (int)(blockIdx.x % g.Hkv) : -1, counts, vote_num, vote_den, force,
+               sel_idx, sel_page, n_sel, wbuf);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *block_sums,
                           double threshold, uint8_t *mask, int32_t *counts, int vote_num,
-                          int vote_den, int force_sink_last, int32_t *sel_idx, int32_t *sel_page,
-                          int32_t *n_sel, cudaStream_t st) {
+                          int vote_den, int force_sink_last, int per_kv, int32_t *sel_idx,
+                          int32_t *sel_page, int32_t *n_sel, cudaStream_t st) {
   if (nctas == 0) {  // no query rows: the vote alone (every count is zero)
-    vote_kernel<<<g.B, STHR, 0, st>>>(g, counts, vote_num, vote_den, force_sink_last, sel_idx,
-                                      sel_page, n_sel);
+    vote_kernel<<<per_kv ? g.B * g.Hkv : g.B, STHR, 0, st>>>(
+        g, counts, vote_num, vote_den, force_sink_last, per_kv, sel_idx, sel_page, n_sel);
     return cudaGetLastError();
   }
   int npad = 1;
@@ -280,9 +295,9 @@ cudaError_t launch_select(const Geo &g, int nctas, int max_kb, const float *bloc
     if (e != cudaSuccess) return e;
   }
   // the finishing counter sits right after the vote counters (zeroed with them)
-  int32_t *done = counts + (size_t)g.B * (size_t)g.bt_stride;
+  int32_t *done = counts + (size_t)g.B * (per_kv ? (size_t)g.Hkv : 1) * (size_t)g.bt_stride;
   select_kernel<<<nctas, STHR, smem, st>>>(g, block_sums, threshold, mask, counts, (int)nkeys,
-                                           vote_num, vote_den, force_sink_last, sel_idx,
+                                           vote_num, vote_den, force_sink_last, per_kv, sel_idx,
                                            sel_page, n_sel, done);
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // KV store of a prefill chunk ("Task Plan: Layerwise Offload Refactoring",
-// Phase 1.2, offload_layer_kv_async): the chunk's keys and values, stored
-// head-major [Hkv, tokens, D], are written block by block into the pool pages
+// Phase 1.2, offload_layer_kv_async): the chunk's keys and values, strided
+// views (KV head, token, d) -- [Hkv, tokens, D] or [tokens, Hkv, D] -- are
+// written block by block into the pool pages
 // the block table assigns to their positions, [page, row, Hkv, D].
 //
 // A page is a contiguous block_size * Hkv * D run of the pool, cut into slices
@@ -30,6 +31,7 @@ __global__ void __launch_bounds__(kStoreThreads)
   const int per_page = g.Bk * per_tok;
   const int dq = g.D / 8;                   // pieces per head row
   const int64_t hs = g.kv_hs / 8;           // pieces between heads of k_cur / v_cur
+  const int64_t ts = g.kv_ts / 8;           // pieces between their tokens
   const int64_t tok0 = (int64_t)R.q0 + (int64_t)j * g.Bk;  // chunk block's first token
   const int64_t dst0 = (int64_t)page * per_page;
   const int u0 = sl * kSlice + threadIdx.x;
@@ -40,7 +42,7 @@ __global__ void __launch_bounds__(kStoreThreads)
     if (u < per_page) {
       const int row = u / per_tok, rem = u - row * per_tok;
       const int kvh = rem / dq, c = rem - kvh * dq;
-      const int64_t src = kvh * hs + (tok0 + row) * dq + c;
+      const int64_t src = kvh * hs + (tok0 + row) * ts + c;
       a[k] = __ldg(kc + src);
       b[k] = __ldg(vc + src);
     }

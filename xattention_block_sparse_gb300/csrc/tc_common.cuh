@@ -1,8 +1,7 @@
 // Blackwell (sm_100a / sm_103a) building blocks written as inline PTX:
-// mbarriers with bounded waits, TMA tiled loads (also multicast to the CTAs of
-// a cluster), cluster rank and barrier, tcgen05 TMEM allocation,
-// MMA issue/commit and TMEM loads/stores, and the shared-memory matrix and
-// instruction descriptors of tcgen05.mma.kind::f16.
+// mbarriers with bounded waits, TMA tiled loads into this CTA's shared memory,
+// tcgen05 TMEM allocation, MMA issue/commit and TMEM loads/stores, and the
+// shared-memory matrix and instruction descriptors of tcgen05.mma.kind::f16.
 #pragma once
 
 #include <cuda.h>
@@ -179,53 +178,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
           smem_addr(bar))
-      : "memory");
-}
-
-// mma_commit that arrives on the mbarrier at this offset in every CTA of the
-// cluster named by cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;\n" ::"r"(smem_addr(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// thread-block clusters
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;\n" ::
-          : "memory");
-}
-// TMA loads whose box lands at the same shared-memory offset in every CTA of
-// cta_mask and completes its bytes on the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_4d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
-                                               int c0, int c1, int c2, int c3, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(smem_addr(bar)), "h"(cta_mask)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_5d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
-                                               int c0, int c1, int c2, int c3, int c4,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(smem_addr(bar)), "h"(cta_mask)
       : "memory");
 }
 

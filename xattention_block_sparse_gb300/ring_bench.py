@@ -49,9 +49,7 @@ def main():
     ring = RN.LayerRing(cfg.ring_slots, P, Bk, Hkv, D, d)
     BT = torch.arange(P, dtype=torch.int32, device=d)[None]
     chunks = [int(x) for x in a.chunks.split(",")]
-    problems = {c: X.Problem(H, Hkv, D, S, Bk, [chunk], [c * chunk], BT, P,
-                             q_head_stride=L * D, kv_head_stride=chunk * D, lse_head_stride=L)
-                for c in chunks}
+    problems = {c: RN.ring_problem(H, Hkv, D, S, Bk, L, chunk, c, BT, P) for c in chunks}
     bufs = RN.ChunkBuffers.for_problems(list(problems.values()), d)
     outs = [(torch.empty((H, L, D), dtype=torch.bfloat16, device=d),
              torch.empty((H, L), dtype=torch.float32, device=d)) for _ in layers]

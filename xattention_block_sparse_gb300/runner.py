@@ -46,32 +46,54 @@ def estimation_scale(head_dim: int, stride: int) -> float:
     return 1.0 / (math.sqrt(head_dim) * stride)
 
 
+@dataclass
+class KeySeq:
+    """Keys of every request in logical token order (xattn_estimate_seq):
+    request r's history and current keys are tokens [starts[r], ...) of
+    `keys`, with element strides between heads and between tokens."""
+    keys: object
+    starts: list
+    head_stride: int
+    token_stride: int = 0
+
+
 def estimate_select(problem, q, k_cur, k_pool, tau, bufs: ChunkBuffers, est_scale=None,
-                    stream=None):
+                    stream=None, k_seq: KeySeq | None = None, per_kv_head=False):
     """Steps 1 and 2 of a chunk: estimation, then the block selection (sel_page,
-    n_sel in bufs).  Reads Q, the chunk's K and the history pages; not V."""
+    n_sel in bufs).  Reads Q and the keys -- the chunk's K and the history
+    pages, or the same keys in logical order when k_seq is given; not V.
+    per_kv_head: one block set per KV head instead of the vote across them."""
     D = problem.c.head_dim
     est_scale = estimation_scale(D, problem.c.stride) if est_scale is None else est_scale
-    X.xattn_estimate(problem, q, k_cur, k_pool, est_scale, bufs.workspace, bufs.block_sums,
-                     stream)
-    X.xattn_select(problem, bufs.block_sums, tau, bufs.workspace, bufs.mask, bufs.sel_idx,
-                   bufs.sel_page, bufs.n_sel, stream)
+    if k_seq is not None:
+        X.xattn_estimate_seq(problem, q, k_seq.keys, k_seq.starts, est_scale, bufs.workspace,
+                             bufs.block_sums, stream, head_stride=k_seq.head_stride,
+                             token_stride=k_seq.token_stride)
+    else:
+        X.xattn_estimate(problem, q, k_cur, k_pool, est_scale, bufs.workspace, bufs.block_sums,
+                         stream)
+    select = X.xattn_select_per_kv_head if per_kv_head else X.xattn_select
+    select(problem, bufs.block_sums, tau, bufs.workspace, bufs.mask, bufs.sel_idx,
+           bufs.sel_page, bufs.n_sel, stream)
 
 
 def attend(problem, q, k_cur, v_cur, k_pool, v_pool, bufs: ChunkBuffers, o, lse,
-           softmax_scale=None, stream=None):
+           softmax_scale=None, stream=None, per_kv_head=False):
     """Step 3 of a chunk: attention over the selected pages and the causal chunk."""
     D = problem.c.head_dim
     softmax_scale = 1.0 / math.sqrt(D) if softmax_scale is None else softmax_scale
-    X.bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, bufs.sel_page, bufs.n_sel,
-                          softmax_scale, bufs.workspace, o, lse, stream)
+    att = X.bsa_chunk_attention_per_kv_head if per_kv_head else X.bsa_chunk_attention
+    att(problem, q, k_cur, v_cur, k_pool, v_pool, bufs.sel_page, bufs.n_sel, softmax_scale,
+        bufs.workspace, o, lse, stream)
 
 
 def prefill_chunk(problem, q, k_cur, v_cur, k_pool, v_pool, tau, bufs: ChunkBuffers, o, lse,
-                  est_scale=None, softmax_scale=None, stream=None):
+                  est_scale=None, softmax_scale=None, stream=None, k_seq: KeySeq | None = None,
+                  per_kv_head=False):
     """One chunk of XAttention BSA prefill: estimate, select, attend."""
-    estimate_select(problem, q, k_cur, k_pool, tau, bufs, est_scale, stream)
-    attend(problem, q, k_cur, v_cur, k_pool, v_pool, bufs, o, lse, softmax_scale, stream)
+    estimate_select(problem, q, k_cur, k_pool, tau, bufs, est_scale, stream, k_seq, per_kv_head)
+    attend(problem, q, k_cur, v_cur, k_pool, v_pool, bufs, o, lse, softmax_scale, stream,
+           per_kv_head)
 
 
 class SequencePrefill:
@@ -80,21 +102,35 @@ class SequencePrefill:
     Q [H, L, D], K/V [Hkv, L, D] (current-chunk views are windows of these),
     pools [P, Bk, Hkv, D] and block_table [1, P] as device tensors.  Chunk c
     queries tokens [c*chunk, (c+1)*chunk) and reads history [0, c*chunk)
-    through the block table."""
+    through the block table for its attention.  The estimation reads the keys
+    [0, (c+1)*chunk) of K in token order (xattn_estimate_seq), or, with
+    est_from_pages, the history pages and the chunk's K (xattn_estimate): the
+    two give the same bits.  per_kv_head selects one block set per KV head."""
 
     def __init__(self, H, Hkv, D, stride, block, L, chunk, block_table, num_pages,
-                 with_mask=False):
+                 with_mask=False, est_from_pages=False, per_kv_head=False):
         self.H, self.Hkv, self.D, self.L, self.chunk = H, Hkv, D, L, chunk
+        self.est_from_pages = est_from_pages
+        self.per_kv_head = per_kv_head
         self.problems = [
             X.Problem(H, Hkv, D, stride, block, [chunk], [c * chunk], block_table, num_pages,
                       q_head_stride=L * D, kv_head_stride=L * D, lse_head_stride=L)
             for c in range(L // chunk)]
         self.bufs = ChunkBuffers.for_problems(self.problems, block_table.device, with_mask)
+        if per_kv_head:  # selections per (request, KV head)
+            dev = block_table.device
+            self.bufs.sel_idx = torch.empty((Hkv, L // block), dtype=torch.int32, device=dev)
+            self.bufs.sel_page = torch.empty((Hkv, L // block), dtype=torch.int32, device=dev)
+            self.bufs.n_sel = torch.empty(Hkv, dtype=torch.int32, device=dev)
+
+    def key_seq(self, K):
+        return None if self.est_from_pages else KeySeq(K, [0], K.stride(0))
 
     def run_chunk(self, c, Q, K, V, kpool, vpool, tau, O, LSE, stream=None):
         t0 = c * self.chunk
         prefill_chunk(self.problems[c], Q[:, t0:], K[:, t0:], V[:, t0:], kpool, vpool, tau,
-                      self.bufs, O[:, t0:], LSE[:, t0:], stream=stream)
+                      self.bufs, O[:, t0:], LSE[:, t0:], stream=stream, k_seq=self.key_seq(K),
+                      per_kv_head=self.per_kv_head)
 
     def run(self, Q, K, V, kpool, vpool, tau, O, LSE, stream=None, on_chunk=None):
         for c in range(len(self.problems)):
@@ -159,13 +195,14 @@ class SequencePrefill:
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             p = self.problems[c]
             q, k, v = dev["q"][:, t0:], dev["k"][:, t0:], dev["v"][:, t0:]
-            stream.wait_event(ready[c])
-            estimate_select(p, q, k, dev["kpool"], tau, self.bufs, stream=stream)
+            stream.wait_event(ready[c])  # K of chunks 0..c have landed (one copy stream)
+            estimate_select(p, q, k, dev["kpool"], tau, self.bufs, stream=stream,
+                            k_seq=self.key_seq(dev["k"]), per_kv_head=self.per_kv_head)
             stream.wait_event(ready_v[c])
             if store_kv:  # the history of chunk c + 1, before anything reads it
                 X.xattn_store_kv(p, k, v, dev["kpool"], dev["vpool"], stream)
             attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, dev["o"][:, t0:],
-                   dev["lse"][:, t0:], stream=stream)
+                   dev["lse"][:, t0:], stream=stream, per_kv_head=self.per_kv_head)
             done = torch.cuda.Event()
             done.record(stream)
             d2h_stream.wait_event(done)
@@ -235,11 +272,24 @@ class LayerRing:
         self.done[self.slot(layer)].record(stream)
 
 
+def ring_problem(H, Hkv, D, stride, block, L, chunk, c, block_table, num_pages):
+    """The problem of chunk c in the layer ring: history [0, c*chunk) through
+    the block table, the chunk's own K/V read where the ring slot holds them --
+    its pages, [tokens, Hkv, D] (heads D apart, tokens Hkv*D apart)."""
+    return X.Problem(H, Hkv, D, stride, block, [chunk], [c * chunk], block_table, num_pages,
+                     q_head_stride=L * D, kv_head_stride=D, lse_head_stride=L,
+                     kv_token_stride=Hkv * D)
+
+
 def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bufs, problem,
                        outs, stream, on_layer=None, compute_events=None, reuse_selection=False):
     """Chunk c of every layer through the ring: history pages [0, c*chunk/block)
     of each layer are loaded into its slot, the current chunk's K/V are the
     next chunk/block pages of the same host cache (copied in the same load).
+    The slot holds the layer's pages in logical order (an identity block
+    table), so the chunk's K/V are read in place as a [tokens, Hkv, D] view
+    (`problem` from ring_problem) and the estimation reads the slot's keys
+    [0, (c+1)*chunk) in token order (xattn_estimate_seq).
 
     reuse_selection: only layer 0 estimates and selects; every later layer
     attends over the pages layer 0 selected ("XAttention BSA Policy 设计文档",
@@ -256,9 +306,8 @@ def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bu
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         with torch.cuda.stream(stream):
-            # current chunk in [Hkv, tokens, D] for the estimation / attention calls
-            kc = kp[n_hist:n_load].reshape(chunk, Hkv, D).permute(1, 0, 2).contiguous()
-            vc = vp[n_hist:n_load].reshape(chunk, Hkv, D).permute(1, 0, 2).contiguous()
+            # the chunk's K/V: its pages of the slot, [tokens, Hkv, D] in place
+            kc, vc = kp[n_hist:n_load], vp[n_hist:n_load]
             q = layers[l].q[:, c * chunk:]
             o, lse = outs[l]
             if reuse_selection and l > 0:
@@ -266,7 +315,8 @@ def ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, stride, block, tau, bu
                        stream=stream)
             else:
                 prefill_chunk(problem, q, kc, vc, kp, vp, tau, bufs, o[:, c * chunk:],
-                              lse[:, c * chunk:], stream=stream)
+                              lse[:, c * chunk:], stream=stream,
+                              k_seq=KeySeq(kp, [0], D, Hkv * D))
             if compute_events is not None:
                 e1.record(stream)
                 compute_events.append((e0, e1))

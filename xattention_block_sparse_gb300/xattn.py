@@ -26,7 +26,8 @@ STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAG
           -7: "XATTN_ETIMEOUT"}
 
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
-            "xattn_estimate", "xattn_select", "xattn_select_noalloc", "bsa_chunk_attention",
+            "xattn_estimate", "xattn_estimate_seq", "xattn_select", "xattn_select_per_kv_head",
+            "xattn_select_noalloc", "bsa_chunk_attention", "bsa_chunk_attention_per_kv_head",
             "lse_merge", "xattn_store_kv",
             "xattn_device_error", "xattn_last_device_error", "xattn_copy_rows_async",
             "xattn_status_string"]
@@ -54,6 +55,7 @@ class xattn_problem(ctypes.Structure):
         ("q_head_stride", ctypes.c_int64),
         ("kv_head_stride", ctypes.c_int64),
         ("lse_head_stride", ctypes.c_int64),
+        ("kv_token_stride", ctypes.c_int64),
     ]
 
 
@@ -78,10 +80,16 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "xattn_block_sums_count": (sz, [P]),
         "xattn_block_sums_offset": (sz, [P, i32]),
         "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
+        "xattn_estimate_seq": (ctypes.c_int, [P, vp, vp, i64, i64, ctypes.POINTER(i64), f32, vp,
+                                               sz, vp, vp]),
         "xattn_select": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp]),
+        "xattn_select_per_kv_head": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, sz, vp, vp, vp,
+                                                     vp, vp]),
         "xattn_select_noalloc": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, vp, vp, vp, vp]),
         "bsa_chunk_attention": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, sz, vp, vp,
                                                 vp]),
+        "bsa_chunk_attention_per_kv_head": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, f32, vp,
+                                                            sz, vp, vp, vp]),
         "lse_merge": (ctypes.c_int, [vp, vp, vp, vp, i64, i32, vp, i32, vp, vp]),
         "xattn_store_kv": (ctypes.c_int, [P, vp, vp, vp, vp, vp]),
         "xattn_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), i32]),
@@ -108,11 +116,12 @@ class Problem:
 
     q_lens / kh_lens: per-request query-chunk and history token counts;
     block_table: DEVICE int32 tensor [B, bt_stride] (or None without history);
-    strides are element strides between heads of q/o, k_cur/v_cur and lse."""
+    strides are element strides between heads of q/o, k_cur/v_cur and lse, and
+    between tokens of k_cur/v_cur (None: head_dim, the [Hkv, tokens, D] layout)."""
 
     def __init__(self, num_heads, num_kv_heads, head_dim, stride, block_size, q_lens, kh_lens,
                  block_table=None, num_pages=0, q_head_stride=None, kv_head_stride=None,
-                 lse_head_stride=None):
+                 lse_head_stride=None, kv_token_stride=None):
         self.q_lens = [int(x) for x in q_lens]
         self.kh_lens = [int(x) for x in kh_lens]
         B = len(self.q_lens)
@@ -134,7 +143,8 @@ class Problem:
             bt_ptr, bt_stride, num_pages,
             q_head_stride if q_head_stride is not None else tot * head_dim,
             kv_head_stride if kv_head_stride is not None else tot * head_dim,
-            lse_head_stride if lse_head_stride is not None else tot)
+            lse_head_stride if lse_head_stride is not None else tot,
+            kv_token_stride if kv_token_stride is not None else 0)
 
     @property
     def B(self):
@@ -203,6 +213,22 @@ def xattn_estimate(problem, q, k_cur, k_pool, scale, workspace, block_sums, stre
     _check(st, "xattn_estimate")
 
 
+def xattn_estimate_seq(problem, q, k_seq, k_seq_starts, scale, workspace, block_sums,
+                       stream=None, head_stride=None, token_stride=0):
+    """xattn_estimate over keys in logical token order: request r's history and
+    current keys are tokens [k_seq_starts[r], ...) of k_seq.  k_seq is a
+    [Hkv, tokens, D] tensor unless head_stride / token_stride say otherwise."""
+    starts = np.ascontiguousarray(np.asarray(k_seq_starts, dtype=np.int64))
+    hs = k_seq.stride(0) if head_stride is None else int(head_stride)
+    st = load_library().xattn_estimate_seq(problem.ref(), _dev(q, "q", _BF16),
+                                           _dev(k_seq, "k_seq", _BF16), hs, int(token_stride),
+                                           starts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                           float(scale), _dev(workspace, "workspace"),
+                                           workspace.numel() * workspace.element_size(),
+                                           _dev(block_sums, "block_sums", _F32), _stream(stream))
+    _check(st, "xattn_estimate_seq")
+
+
 def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_page, n_sel,
                  stream=None, vote=(1, 2), force_sink_last=True):
     """vote = (num, den): a history block is selected when its votes exceed
@@ -216,6 +242,20 @@ def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_p
                                      _dev(sel_page, "sel_page", _I32), _dev(n_sel, "n_sel", _I32),
                                      _stream(stream))
     _check(st, "xattn_select")
+
+
+def xattn_select_per_kv_head(problem, block_sums, threshold, workspace, mask, sel_idx, sel_page,
+                             n_sel, stream=None, vote=(1, 2), force_sink_last=True):
+    """One block set per KV head: sel_idx / sel_page [B, Hkv, bt_stride], n_sel
+    [B, Hkv]; KV head k keeps a block its own query blocks vote for by more
+    than num/den."""
+    st = load_library().xattn_select_per_kv_head(
+        problem.ref(), _dev(block_sums, "block_sums", _F32), float(threshold), int(vote[0]),
+        int(vote[1]), int(bool(force_sink_last)), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev(mask, "mask", _U8),
+        _dev(sel_idx, "sel_idx", _I32), _dev(sel_page, "sel_page", _I32),
+        _dev(n_sel, "n_sel", _I32), _stream(stream))
+    _check(st, "xattn_select_per_kv_head")
 
 
 def xattn_select_noalloc(problem, block_sums, threshold, mask, sel_idx, sel_page, n_sel,
@@ -250,6 +290,19 @@ def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_se
     _check(st, "bsa_chunk_attention")
 
 
+def bsa_chunk_attention_per_kv_head(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_sel,
+                                    softmax_scale, workspace, o, lse, stream=None):
+    """bsa_chunk_attention over a selection per KV head (sel_page [B, Hkv,
+    bt_stride], n_sel [B, Hkv])."""
+    st = load_library().bsa_chunk_attention_per_kv_head(
+        problem.ref(), _dev(q, "q", _BF16), _dev(k_cur, "k_cur", _BF16),
+        _dev(v_cur, "v_cur", _BF16), _dev(k_pool, "k_pool", _BF16), _dev(v_pool, "v_pool", _BF16),
+        _dev(sel_page, "sel_page", _I32), _dev(n_sel, "n_sel", _I32), float(softmax_scale),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(o, "o", _BF16), _dev(lse, "lse", _F32), _stream(stream))
+    _check(st, "bsa_chunk_attention_per_kv_head")
+
+
 def lse_merge(o1, lse1, o2, lse2, o_out, lse_out, stream=None):
     rows, d = o1.shape[0], o1.shape[-1]
     bf16 = 1 if str(o_out.dtype).endswith("bfloat16") else 0
@@ -275,8 +328,8 @@ def xattn_last_device_error(stream=None) -> int:
 
 
 def xattn_store_kv(problem, k_cur, v_cur, k_pool, v_pool, stream=None):
-    """Write the chunk's K/V ([Hkv, tokens, D] views, kv_head_stride apart) into
-    the pool pages the block table gives their positions."""
+    """Write the chunk's K/V (views with the problem's kv_head_stride and
+    kv_token_stride) into the pool pages the block table gives their positions."""
     st = load_library().xattn_store_kv(problem.ref(), _dev(k_cur, "k_cur", _BF16),
                                        _dev(v_cur, "v_cur", _BF16),
                                        _dev(k_pool, "k_pool", _BF16),
