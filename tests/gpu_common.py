@@ -19,6 +19,24 @@ BS_ATOL_PER_BR = 1e-6
 O_ATOL = 2e-2
 LSE_ATOL = 1e-3
 
+# For information only: the oracle's own selection (on its float64 block sums)
+# against the GPU's, per checked chunk -- (what, mask entries that differ,
+# mask entries compared, history blocks selected by one side only or None when
+# only sampled rows were estimated).  conftest.py prints them after the run.
+FLIPS = []
+
+
+def record_flips(what, ref_bs, gpu_mask, tau, Hkv=None, kbh=None, gpu_sel=None):
+    """Flip count of the oracle's threshold masks on its own block sums against
+    the GPU's masks on the same rows, and, given every row, of the vote."""
+    own = O.threshold_select(np.asarray(ref_bs, dtype=np.float32), tau)
+    mask_flips = int((own != np.asarray(gpu_mask, dtype=bool)).sum())
+    sel_flips = None
+    if gpu_sel is not None:
+        sel = O.gqa_vote(own, Hkv, kbh)
+        sel_flips = len(set(sel.tolist()) ^ set(np.asarray(gpu_sel).tolist()))
+    FLIPS.append((what, mask_flips, int(own.size), sel_flips))
+
 
 def dev():
     if not torch.cuda.is_available():
@@ -122,6 +140,7 @@ class SequenceCase:
         G = cfg.H // cfg.Hkv
         bt_row = self.wl.block_table[0]
         # estimation
+        refs = []
         for h in range(cfg.H):
             kvh = h // G
             hist = O.gather_history(kp, bt_row, kh, kvh)
@@ -133,6 +152,14 @@ class SequenceCase:
                 ref = O.block_sums_qblocks(q[h, t0:t1], hist, k[kvh, t0:t1], cfg.stride,
                                            cfg.block, scale, qblocks)
                 check_block_sums(bs32[h, qblocks], ref, br, f"chunk {c} head {h}")
+            refs.append(ref)
+        gmask = cap["mask"].reshape(bs32.shape)
+        if qblocks is None:
+            record_flips(f"{self.wl.cfg.name} tau {tau} chunk {c}", np.stack(refs), gmask, tau,
+                         cfg.Hkv, kbh, cap["sel"][:cap["n_sel"]])
+        else:
+            record_flips(f"{self.wl.cfg.name} tau {tau} chunk {c} (sampled query blocks)",
+                         np.stack(refs), gmask[:, qblocks], tau)
         # selection on the GPU's block sums
         sel, pages = check_selection(bs32, cap["mask"].reshape(bs32.shape), cap["sel"],
                                      cap["pages"], cap["n_sel"], tau, cfg.Hkv, kbh, bt_row,

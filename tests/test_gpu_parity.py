@@ -16,7 +16,7 @@ from xattention_block_sparse_gb300 import runner as RN
 from xattention_block_sparse_gb300 import xattn as X
 
 from gpu_common import (SequenceCase, check_attention, check_block_sums, check_selection, dev,
-                        to_dev_bf16)
+                        record_flips, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -258,6 +258,14 @@ def test_selection_vote_parameters(vote, force):
     check_selection(bs32, mk, b.sel_idx[0].cpu().numpy(), b.sel_page[0].cpu().numpy(),
                     int(b.n_sel[0].item()), tau, cfg.Hkv, kbh, case.wl.block_table[0],
                     f"vote {vote} force {force}", vote=vote, force=force)
+    if vote == (1, 4):  # the oracle's own block sums, for the flip report
+        q, k, _, kp, _ = case.oracle_inputs()
+        ref = O.estimate_request(q[:, t0:t0 + case.chunk], k[:, t0:t0 + case.chunk], kp,
+                                 case.wl.block_table[0], t0, cfg.H, cfg.Hkv, cfg.stride,
+                                 cfg.block, O.default_estimation_scale(cfg.D, cfg.stride))
+        check_block_sums(bs32, ref, cfg.block // cfg.stride, "q06b_4k chunk 3")
+        record_flips(f"q06b_4k tau {tau} chunk {c} (vote (1, 2))", ref, mk, tau, cfg.Hkv, kbh,
+                     O.gqa_vote(mk.astype(bool), cfg.Hkv, kbh))
 
 
 def test_prefill_from_host_matches_device_resident_run():
@@ -389,6 +397,8 @@ def test_odd_group_sizes_full_path(H, Hkv, D, Bk, S):
                              O.default_estimation_scale(D, S))
     check_block_sums(bs, ref, Bk // S, f"H={H} Hkv={Hkv}")
     mk = bufs.mask[: bs.size].cpu().numpy().reshape(bs.shape)
+    record_flips(f"H={H} Hkv={Hkv} D={D} S={S} tau {tau}", ref, mk, tau, Hkv, kbh,
+                 bufs.sel_idx[0, : int(bufs.n_sel[0].item())].cpu().numpy())
     sel, pages = check_selection(bs, mk, bufs.sel_idx[0].cpu().numpy(),
                                  bufs.sel_page[0].cpu().numpy(), int(bufs.n_sel[0].item()), tau,
                                  Hkv, kbh, bt[0], f"H={H} Hkv={Hkv}")

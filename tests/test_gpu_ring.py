@@ -110,3 +110,72 @@ def test_q4b_128k_layer_ring_parity():
                 o_g = _f64(og[kvh * G:(kvh + 1) * G][:, idx])
                 l_g = lg[kvh * G:(kvh + 1) * G][:, idx].cpu().numpy()
                 check_attention(o_g, l_g, o_ref, l_ref, f"layer {l} chunk {c} kv head {kvh}")
+
+
+def test_ring_reused_selection_parity():
+    """Layer 0's selection shared by the later layers ("XAttention BSA Policy
+    设计文档", 性能分析, 优化方向 1): layer 0 estimates and selects; layers 1
+    and 2 attend over layer 0's pages with their own queries, keys and values.
+    Their outputs must equal the oracle's attention of each layer over layer 0's
+    selected pages (and layer 0's selection the oracle's on its block sums).
+    The 128K recipe at 16K tokens, three layers through two ring slots."""
+    cfg = I.CONFIGS["q4b_128k"]
+    d = dev()
+    H, Hkv, D, S, Bk, chunk = cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, cfg.chunk
+    L = 4 * chunk
+    G = H // Hkv
+    P = L // Bk
+    tau = cfg.taus[0]
+    layers = [I.make_ring_layer(l, d, L=L) for l in range(3)]
+    ring = RN.LayerRing(2, P, Bk, Hkv, D, d)
+    BT = torch.arange(P, dtype=torch.int32, device=d)[None]
+    chunks = [1, 3]
+    problems = {c: RN.ring_problem(H, Hkv, D, S, Bk, L, chunk, c, BT, P) for c in chunks}
+    bufs = RN.ChunkBuffers.for_problems(list(problems.values()), d, with_mask=True)
+    outs = [(torch.zeros((H, L, D), dtype=torch.bfloat16, device=d),
+             torch.zeros((H, L), dtype=torch.float32, device=d)) for _ in layers]
+    stream = torch.cuda.Stream(device=d)
+    cap = {}
+
+    def on_layer(c):
+        def f(l, b):
+            if l == 0:
+                stream.synchronize()
+                n = X.xattn_block_sums_count(problems[c])
+                cap[c] = dict(bs=b.block_sums[:n].cpu().numpy().copy(),
+                              mask=b.mask[:n].cpu().numpy().copy(),
+                              sel=b.sel_idx[0].cpu().numpy().copy(),
+                              pages=b.sel_page[0].cpu().numpy().copy(),
+                              n_sel=int(b.n_sel[0].item()))
+        return f
+
+    for c in chunks:
+        RN.ring_prefill_chunk(ring, layers, c, chunk, H, Hkv, D, S, Bk, tau, bufs, problems[c],
+                              outs, stream, on_layer=on_layer(c), reuse_selection=True)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    rng = np.random.default_rng(5)
+    bt_row = np.arange(P)
+    for c in chunks:
+        t0, t1 = c * chunk, (c + 1) * chunk
+        n_hist, qb_n = t0 // Bk, chunk // Bk
+        got = cap[c]
+        bs32 = got["bs"].reshape(H, qb_n, n_hist + qb_n)
+        _, pages = check_selection(bs32, got["mask"].reshape(bs32.shape), got["sel"],
+                                   got["pages"], got["n_sel"], tau, Hkv, n_hist, bt_row,
+                                   f"layer 0 chunk {c}")
+        rows = sorted({0, chunk - 1, *rng.integers(0, chunk, 6).tolist()})
+        for l in (1, 2):
+            og, lg = outs[l]
+            for kvh in (0, Hkv - 1):
+                pk = _f64(layers[l].k_host[:, :, kvh:kvh + 1, :])
+                pv = _f64(layers[l].v_host[:, :, kvh:kvh + 1, :])
+                kc = pk[n_hist:n_hist + qb_n, :, 0, :].reshape(chunk, D)[None]
+                vc = pv[n_hist:n_hist + qb_n, :, 0, :].reshape(chunk, D)[None]
+                q = _f64(layers[l].q[kvh * G:(kvh + 1) * G, t0:t1])
+                o_ref, l_ref = O.attend_request(q, kc, vc, pk, pv, pages, G, 1,
+                                                1 / math.sqrt(D), rows=rows)
+                idx = t0 + np.asarray(rows)
+                check_attention(_f64(og[kvh * G:(kvh + 1) * G][:, idx]),
+                                lg[kvh * G:(kvh + 1) * G][:, idx].cpu().numpy(), o_ref, l_ref,
+                                f"layer {l} chunk {c} kv head {kvh}")

@@ -228,3 +228,44 @@ def test_per_kv_head_varlen():
             rows=rows)
         idx = q0 + np.asarray(rows)
         check_attention(Og[:, idx], Lg[:, idx], o_ref, l_ref, f"request {r}")
+
+
+def test_one_shot_estimate_matches_kv_chunked_estimation():
+    """GPU-only mode against the offload mode ("XAttention Offload Stream
+    Synchronization Fix", 测试结果, Density 对齐验证): the library estimates over
+    the whole resident history in one launch; the offload path takes softmax
+    statistics per KV chunk, merges them and then normalises (the oracle's
+    block_sums_chunked, four KV chunks).  The two agree to the block-sum
+    tolerance, and the selections made from them are compared (density and
+    flips, for information) on the seeded 4K and sparse 32K-shaped inputs."""
+    from gpu_common import FLIPS
+    for name, c, L in (("q06b_4k", 3, None), ("q06b_32k_sparse", 1, 8192)):
+        case = SequenceCase(name, L=L)
+        cfg = case.cfg
+        tau = 0.9
+        _, _, cap = case.run(tau, capture=[c])
+        q, k, _, kp, _ = case.oracle_inputs()
+        t0, t1 = c * case.chunk, (c + 1) * case.chunk
+        kbh, qb = t0 // cfg.block, case.chunk // cfg.block
+        bs = cap[c]["bs"].reshape(cfg.H, qb, kbh + qb)
+        scale = O.default_estimation_scale(cfg.D, cfg.stride)
+        ncol = (t1) // cfg.stride
+        cuts = np.linspace(0, ncol, 5).astype(int)
+        chunks = [(int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:])]
+        G = cfg.H // cfg.Hkv
+        ref = []
+        for h in range(cfg.H):
+            hist = O.gather_history(kp, case.wl.block_table[0], t0, h // G)
+            full, _ = O.block_sums_chunked(q[h, t0:t1], hist, k[h // G, t0:t1], cfg.stride,
+                                           cfg.block, scale, chunks)
+            ref.append(full)
+        ref = np.stack(ref)
+        check_block_sums(bs, ref, cfg.block // cfg.stride, f"{name} chunk {c}")
+        chunked = O.select_request(ref.astype(np.float32), tau, cfg.Hkv, kbh,
+                                   case.wl.block_table[0])[1]
+        gpu = cap[c]["sel"][:cap[c]["n_sel"]]
+        FLIPS.append((f"{name} chunk {c}: GPU one-shot density {len(gpu) / kbh:.4f} vs "
+                      f"KV-chunked oracle {len(chunked) / kbh:.4f}",
+                      int((O.threshold_select(ref.astype(np.float32), tau)
+                           != cap[c]["mask"].reshape(bs.shape).astype(bool)).sum()),
+                      int(bs.size), len(set(gpu.tolist()) ^ set(chunked.tolist()))))

@@ -56,7 +56,38 @@ def test_reference_arm_other_ranks_exit_without_work():
     and exits 0 (no process group, no oracle work)."""
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
-                         text=True, timeout=120, cwd=ROOT)
+                          "--gpus", "2", "--steps", "1", "--warmup", "0"], env=env,
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert res.returncode == 0, res.stderr[-2000:]
     assert res.stdout.strip() == ""
+
+
+def test_gpus_must_match_the_launched_replicas():
+    """--gpus N without N launched processes is refused before any work, so a
+    line can never report a GPU count it did not time."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                         text=True, timeout=120, cwd=ROOT)
+    assert res.returncode != 0
+    assert "WORLD_SIZE=1" in res.stderr
+
+
+def test_torchrun_launch_of_two_reference_replicas():
+    """The launch the driver uses for N > 1 (torch.distributed.run, one process
+    per rank, 127.0.0.1): rank 0 alone prints one JSON line of the oracle arm,
+    rank 1 exits 0.  On the small workload so that it takes seconds."""
+    import json
+    res = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                          "--steps", "2", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-3000:]
+    lines = [x for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    # the measured seconds of the steps are what ms_per_step reports
+    assert rec["ms_per_step"] * rec["steps"] <= rec["cpu_baseline"]["measured_s"] * 1e3 + 1e-6

@@ -47,7 +47,7 @@ def test_ring_event_discipline(monkeypatch, num_layers, num_slots):
     ring = RN.LayerRing(num_slots, P, Bk, Hkv, D, "cpu")
     compute = FS.Stream(log, "compute")
 
-    def fake_prefill(problem, q, kc, vc, kp, vp, tau, bufs, o, lse, stream=None):
+    def fake_prefill(problem, q, kc, vc, kp, vp, tau, bufs, o, lse, stream=None, k_seq=None):
         l = len([op for op in log if op[0] == "compute"])
         assert torch.equal(kp[:n_load], layers[l].k_host[:n_load])   # the slot holds layer l
         assert torch.equal(vp[:n_load], layers[l].v_host[:n_load])
@@ -107,7 +107,7 @@ def test_reused_selection_estimates_once_per_chunk(monkeypatch):
     bufs = object()
     seen = []
 
-    def full(problem, q, kc, vc, kp, vp, tau, b, o, lse, stream=None):
+    def full(problem, q, kc, vc, kp, vp, tau, b, o, lse, stream=None, k_seq=None):
         seen.append(b)
         log.append(("full", stream, len([op for op in log if op[0] in ("full", "attend")])))
 

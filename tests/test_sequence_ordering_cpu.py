@@ -67,7 +67,8 @@ def _run(monkeypatch, store_kv, n_chunks=3):
         return f
 
     monkeypatch.setattr(X, "copy_window_async", copy_window)
-    for kind, fn in (("estimate", "xattn_estimate"), ("select", "xattn_select"),
+    for kind, fn in (("estimate", "xattn_estimate"), ("estimate", "xattn_estimate_seq"),
+                     ("select", "xattn_select"),
                      ("attend", "bsa_chunk_attention"), ("store", "xattn_store_kv")):
         monkeypatch.setattr(X, fn, rec(kind))
     compute, h2d, d2h = (FS.Stream(log, n) for n in ("compute", "h2d", "d2h"))
@@ -91,6 +92,9 @@ def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatc
         assert log[est][1] is compute and log[att][1] is compute
         for name in ("q", "k"):
             assert before(_index(log, "copy", (name, c)), est)
+        # the estimate reads the keys of the whole prefix in token order
+        for c2 in range(c):
+            assert before(_index(log, "copy", ("k", c2)), est)
         assert before(_index(log, "copy", ("v", c)), att)
         assert before(est, _index(log, "select", c)) and before(_index(log, "select", c), att)
         for name in ("o", "lse"):

@@ -17,7 +17,13 @@ Recipe (all configs):
     the oracle reads exactly those bf16 values widened to float64;
   * RoPE, where a config asks for it, is the NeoX rotate-half form with
     theta = 1e6 at absolute positions 0..L-1, applied in fp32 before the
-    bf16 rounding (it is part of the synthetic workload, not of the method).
+    bf16 rounding (it is part of the synthetic workload, not of the method);
+  * heavy key blocks (q06b_32k_sparse): in every run of `heavy_every` blocks
+    one seeded block is heavy; per KV head a direction u (unit, seeded) is
+    added as a*u to every query of the group and to every key of the heavy
+    blocks, after RoPE, with a^2 / sqrt(D) = heavy_boost, so a heavy key's
+    logit gains about heavy_boost.  This concentrates attention the way the
+    pages' needle-in-a-haystack runs do, without their data.
 """
 from __future__ import annotations
 
@@ -99,6 +105,10 @@ class Config:
     local_bias: bool = False
     layers: int = 1
     ring_slots: int = 0
+    # heavy key blocks: one seeded block in every `heavy_every` blocks carries a
+    # shared direction that every query also carries (logit boost heavy_boost)
+    heavy_every: int = 0
+    heavy_boost: float = 0.0
 
 
 CONFIGS = {
@@ -114,6 +124,12 @@ CONFIGS = {
     "varlen": Config(5, "varlen", H=16, Hkv=8, D=128, stride=8, block=128, taus=(0.9,),
                      q_lens=(8192, 3072, 1024), kh_lens=(0, 16384, 65536),
                      pool_pages=640, bt_width=512),
+    # the 32K shapes with attention concentrated on a few key blocks, so that
+    # tau = 0.9 keeps about a tenth of the history (the density the stream-sync
+    # page measures for Qwen3-0.6B at 32K, ~9.8%)
+    "q06b_32k_sparse": Config(6, "q06b_32k_sparse", H=16, Hkv=8, D=128, stride=8, block=128,
+                              taus=(0.9,), L=32768, chunk=4096, rope=True, heavy_every=12,
+                              heavy_boost=6.0),
 }
 
 
@@ -238,6 +254,18 @@ def make_workload(name: str, layer: int = 0, L: int | None = None,
         q += np.repeat(u, G, axis=0)[:, win, :]
     if cfg.sink:
         k[:, 0:4, :] *= 3.0
+    if cfg.heavy_every:
+        nblk = L // Bk
+        starts = np.arange(0, nblk, cfg.heavy_every)
+        span = np.minimum(cfg.heavy_every, nblk - starts)
+        heavy = starts + (g_x.random(len(starts)) * span).astype(np.int64)
+        u = _normal(g_x, (Hkv, D)).astype(np.float64)
+        u /= np.linalg.norm(u, axis=1, keepdims=True)
+        a = np.sqrt(cfg.heavy_boost * np.sqrt(D))
+        G = H // Hkv
+        q += np.repeat((a * u).astype(np.float32), G, axis=0)[:, None, :]
+        tok = (heavy[:, None] * Bk + np.arange(Bk)[None, :]).reshape(-1)
+        k[:, tok, :] += (a * u).astype(np.float32)[:, None, :]
     P = L // Bk
     perm = g_x.permutation(P).astype(np.int32)
     kb, vb = bf16_round(k), bf16_round(v)
