@@ -6,7 +6,13 @@
   last CTA's own part in tensor memory),
 * a ragged last unit (128 rows: no second query tile), head_dim 64 with
   64-key tiles,
-* one whole unit per CTA (a small launch).
+* one whole unit per CTA (a small launch),
+* waves of whole units, one per CTA per wave, then stream-K ranges sized so
+  that every CTA carries the same total (more units than CTAs, none longer
+  than a fair share): one and two waves on one request, one wave over two
+  requests of different history lengths -- each also run as plain stream-K
+  (XATTN_ATTN_SCHEDULE chooses; by default waves run only when the keys and
+  values exceed twice L2).
 
 Every case uses a hand-made selection (a random ascending subset of the
 history pages, pages permuted in the pool) and compares sampled rows of every
@@ -33,15 +39,23 @@ CASES = {
     "ragged_last_unit": (4, 2, 128, 128, 8, 640, 12, 7),
     "head_dim_64_block_64": (2, 2, 64, 64, 8, 384, 150, 150),
     "whole_units": (16, 8, 128, 128, 8, 4096, 8, 3),
+    "one_wave_then_stream_k": (32, 8, 128, 128, 8, 1536, 200, 150),
+    "two_waves_then_stream_k": (32, 8, 128, 128, 8, 2816, 200, 150),
 }
+WAVE_CASES = ("one_wave_then_stream_k", "two_waves_then_stream_k")
+
 
 
 def _bits_to_f64(bits):
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_attention_schedule_parity(name):
+@pytest.mark.parametrize("name,schedule",
+                         [(n, None) for n in CASES if n not in WAVE_CASES]
+                         + [(n, sch) for n in WAVE_CASES for sch in ("waves", "streamk")])
+def test_attention_schedule_parity(monkeypatch, name, schedule):
+    if schedule is not None:
+        monkeypatch.setenv("XATTN_ATTN_SCHEDULE", schedule)
     H, Hkv, D, Bk, S, lq, n_hist, n_sel = CASES[name]
     d = dev()
     rng = np.random.default_rng(100 + list(CASES).index(name))
@@ -79,3 +93,57 @@ def test_attention_schedule_parity(name):
     og = O_.float().cpu().numpy()[:, idx].astype(np.float64)
     lg = LSE.cpu().numpy()[:, idx]
     check_attention(og, lg, o_ref, l_ref, name)
+
+
+@pytest.mark.parametrize("schedule", ["waves", "streamk"])
+def test_wave_over_two_requests(monkeypatch, schedule):
+    """Two requests (1024 and 512 query rows; 260 and 220 history pages, 200
+    and 180 selected): 192 units, the wave crossing from the first request's
+    units into the second's."""
+    monkeypatch.setenv("XATTN_ATTN_SCHEDULE", schedule)
+    H, Hkv, D, Bk, S = 32, 8, 128, 128, 8
+    q_lens, n_hist, n_sel = [1024, 512], [260, 220], [200, 180]
+    d = dev()
+    rng = np.random.default_rng(77)
+    tot = sum(q_lens)
+    P = sum(n_hist) + 5
+    q = I.bf16_round(rng.standard_normal((H, tot, D), dtype=np.float32))
+    kc = I.bf16_round(rng.standard_normal((Hkv, tot, D), dtype=np.float32))
+    vc = I.bf16_round(rng.standard_normal((Hkv, tot, D), dtype=np.float32))
+    kp = I.bf16_round(rng.standard_normal((P, Bk, Hkv, D), dtype=np.float32))
+    vp = I.bf16_round(rng.standard_normal((P, Bk, Hkv, D), dtype=np.float32))
+    perm = rng.permutation(P).astype(np.int32)
+    W = max(n_hist)
+    bt = np.full((2, W), -1, dtype=np.int32)
+    bt[0, :n_hist[0]] = perm[:n_hist[0]]
+    bt[1, :n_hist[1]] = perm[n_hist[0]:n_hist[0] + n_hist[1]]
+    pages = [bt[r, np.sort(rng.choice(n_hist[r], size=n_sel[r], replace=False))]
+             for r in range(2)]
+    prob = X.Problem(H, Hkv, D, S, Bk, q_lens, [n * Bk for n in n_hist],
+                     torch.from_numpy(bt).to(d), P)
+    ws = torch.empty(max(X.xattn_workspace_size(prob), 256), dtype=torch.uint8, device=d)
+    sel_page = torch.full((2, W), -7, dtype=torch.int32, device=d)
+    for r in range(2):
+        sel_page[r, :n_sel[r]] = torch.from_numpy(pages[r].astype(np.int32)).to(d)
+    n_sel_t = torch.tensor(n_sel, dtype=torch.int32, device=d)
+    O_ = torch.zeros((H, tot, D), dtype=torch.bfloat16, device=d)
+    LSE = torch.zeros((H, tot), dtype=torch.float32, device=d)
+    scale = 1.0 / math.sqrt(D)
+    X.bsa_chunk_attention(prob, to_dev_bf16(q), to_dev_bf16(kc), to_dev_bf16(vc), to_dev_bf16(kp),
+                          to_dev_bf16(vp), sel_page, n_sel_t, scale, ws, O_, LSE)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    og_all, lg_all = O_.float().cpu().numpy(), LSE.cpu().numpy()
+    q0 = 0
+    for r in range(2):
+        lq = q_lens[r]
+        edges = {e for m in range(0, lq, 128) for e in (m, m + 127)}
+        rows = sorted({x for x in edges if x < lq} | set(rng.integers(0, lq, 12).tolist()))
+        sl = slice(q0, q0 + lq)
+        o_ref, l_ref = O.attend_request(_bits_to_f64(q[:, sl]), _bits_to_f64(kc[:, sl]),
+                                        _bits_to_f64(vc[:, sl]), _bits_to_f64(kp),
+                                        _bits_to_f64(vp), pages[r], H, Hkv, scale, rows=rows)
+        idx = q0 + np.asarray(rows)
+        check_attention(og_all[:, idx].astype(np.float64), lg_all[:, idx], o_ref, l_ref,
+                        f"request {r}")
+        q0 += lq

@@ -41,6 +41,9 @@
 // unwinds (draining its TMA loads and MMAs, then freeing TMEM).  No CTA waits
 // for another: the merge of a split unit is done by whichever CTA finishes its
 // part last.
+#include <stdlib.h>
+#include <string.h>
+
 #include "tc_common.cuh"
 
 namespace xattn {
@@ -51,6 +54,8 @@ constexpr int BM = 128;       // rows per query tile (MMA M)
 constexpr int ROWS = 2 * BM;  // query rows per work unit
 static_assert(ROWS == kAttnRows, "partial-output slots assume kAttnRows rows per unit");
 constexpr int NSLOT = 5;      // K/V ring slots
+constexpr int kMaxWaves = 8;  // waves of whole units before the stream-K part
+constexpr int kStreamK = 0, kWholeUnits = 1, kWaves = 2;
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;  // S_A | S_B | O_A | O_B, 128 columns each
 
@@ -85,8 +90,13 @@ struct Bars {
   int32_t req_per_head[kMaxReq];   // work items per head of the request
   int32_t req_unit0[kMaxReq];      // first unit id of the request
   int32_t max_unit;                // largest unit (KV tiles)
-  int32_t whole_units;             // schedule: 1 = one whole unit per CTA, 0 = stream-K
-  int64_t beg, end;                // this CTA's work items
+  int32_t nunits;                  // units of the launch
+  int32_t mode;                    // schedule: kStreamK, kWholeUnits or kWaves
+  int32_t nw;                      // kWaves: waves of whole units before stream-K
+  int32_t nrg;                     // this CTA's ranges of work items
+  int64_t rg_beg[kMaxWaves + 1];   // the ranges: its units of each wave (whole),
+  int64_t rg_end[kMaxWaves + 1];   //   then its stream-K range (the last one)
+  int64_t p_waves;                 // kWaves: first item after the waves' units
   int32_t csk;                     // stream-K CTA index, -1 if this CTA has no range
 };
 
@@ -113,7 +123,7 @@ __device__ __forceinline__ Unit unit_geom(const ReqDesc &R, int n_hist, int mt) 
 // Work-item tables of the launch, from the selection counts on the device
 // (every CTA computes the same tables: no host round trip).
 template <int NK>
-__device__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
+__device__ __noinline__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
   int64_t pos = 0;
   int32_t unit = 0;
   const int sub = g.Bk / NK;
@@ -139,22 +149,58 @@ __device__ void build_tables(const Geo &g, const int32_t *n_sel, Bars &bar) {
   }
   bar.req_pos0[g.B] = pos;
   bar.total = pos;
+  bar.nunits = unit;
 }
 
-// First work item of CTA c when `total` items are split over G CTAs.
-__device__ __forceinline__ int64_t cta_begin(int64_t total, int c, int G) {
-  return total * c / G;
+// First work item of unit u (units in item order: request, head, row tile);
+// the total for u = nunits.
+template <int NK>
+__device__ __noinline__ int64_t unit_start(const Geo &g, const Bars &bar, int u) {
+  if (u >= bar.nunits) return bar.total;
+  int r = 0;
+  while (r + 1 < g.B && u >= bar.req_unit0[r + 1]) ++r;
+  const ReqDesc &R = g.req[r];
+  const int nmt = (R.lq + ROWS - 1) / ROWS;
+  const int l = u - bar.req_unit0[r];
+  const int h = l / nmt, mt = l % nmt;
+  int64_t pos = bar.req_pos0[r] + (int64_t)h * bar.req_per_head[r];
+  for (int m = 0; m < mt; ++m) pos += unit_geom<NK>(R, bar.req_hist[r], m).n_tiles;
+  return pos;
 }
 
-// The CTA whose range holds item `pos`.
-__device__ __forceinline__ int cta_of(int64_t total, int G, int64_t pos) {
-  int c = (int)(pos * G / total);
-  while (c + 1 < G && cta_begin(total, c + 1, G) <= pos) ++c;
-  while (c > 0 && cta_begin(total, c, G) > pos) --c;
-  return c;
+// First stream-K item of CTA c of the G stream-K CTAs.  kStreamK: the items
+// split evenly.  kWaves: CTA c first runs units c, c + G, ..., c + (nw-1) G
+// whole, then the items after the waves' nw G units are split so that every
+// CTA's parts add up to the same total:
+//   B_c = P(nw G) + floor(c T / G) - sum_w (P(w G + c) - P(w G)),
+// P(u) the first item of unit u (needs nw * the longest unit <= T / G, so
+// that no CTA's share is negative).
+template <int NK>
+__device__ __noinline__ int64_t cta_begin(const Geo &g, const Bars &bar, int c, int G) {
+  if (bar.mode != kWaves) return bar.total * c / G;
+  if (c >= G) return bar.total;
+  int64_t b = bar.p_waves + bar.total * c / G;
+  for (int w = 0; w < bar.nw; ++w)
+    b -= unit_start<NK>(g, bar, w * G + c) - unit_start<NK>(g, bar, w * G);
+  return b;
 }
 
-// The work of CTA blockIdx.x.  Two schedules, chosen from the tables alone
+// The stream-K CTA whose range holds item `pos` (the last c with B_c <= pos;
+// ranges may be empty).
+template <int NK>
+__device__ __noinline__ int cta_of(const Geo &g, const Bars &bar, int G, int64_t pos) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (cta_begin<NK>(g, bar, mid, G) <= pos)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// The work of CTA blockIdx.x.  Three schedules, chosen from the tables alone
 // (every CTA takes the same decision):
 //  * whole units: CTA c takes unit c of the units ordered by decreasing row
 //    tile (the larger units first within a request), the hardware handing
@@ -162,17 +208,31 @@ __device__ __forceinline__ int cta_of(int64_t total, int G, int64_t pos) {
 //    launch is small (under kWholeUnitsTiles items per SM) and no unit
 //    dwarfs a fair share, where stream-K's segment changes and merges cost
 //    more than the imbalance they remove;
+//  * waves (when the caller allows it: keys and values larger than L2): the
+//    stream-K CTAs first run nw waves of whole units -- CTA c units c, c + G,
+//    ... -- then stream-K ranges of the remaining units sized so that all
+//    CTAs carry the same total.  A wave's units are consecutive -- the query
+//    heads of a few KV heads -- and start at their first KV page together, so
+//    each page comes from DRAM once and from L2 to the other CTAs reading it,
+//    where stream-K CTAs at unrelated positions would each fetch their own;
 //  * stream-K: the last Gsk CTAs of the grid split the items evenly.
 constexpr int kWholeUnitsTiles = 160;
 template <int NK>
-__device__ void schedule(const Geo &g, Bars &bar, int Gsk) {
+__device__ __noinline__ void schedule(const Geo &g, Bars &bar, int Gsk, int waves_ok) {
   const int64_t total = bar.total;
   const int grid = gridDim.x, c = blockIdx.x;
   const int64_t share = (total + Gsk - 1) / Gsk;
-  bar.whole_units = share < kWholeUnitsTiles && 4 * (int64_t)bar.max_unit <= 5 * share;
-  bar.beg = bar.end = 0;
+  const bool whole = share < kWholeUnitsTiles && 4 * (int64_t)bar.max_unit <= 5 * share;
+  int nw = 0;
+  if (!whole && waves_ok) {
+    nw = min(bar.nunits / Gsk, kMaxWaves);
+    while (nw > 0 && (int64_t)nw * bar.max_unit * Gsk > total) --nw;
+  }
+  bar.mode = whole ? kWholeUnits : (nw > 0 ? kWaves : kStreamK);
+  bar.nw = nw;
+  bar.nrg = 0;
   bar.csk = -1;
-  if (bar.whole_units) {
+  if (bar.mode == kWholeUnits) {
     int r = 0;
     while (r + 1 < g.B && c >= bar.req_unit0[r + 1]) ++r;
     const ReqDesc &R = g.req[r];
@@ -182,12 +242,20 @@ __device__ void schedule(const Geo &g, Bars &bar, int Gsk) {
     const int mt = nmt - 1 - l / g.H, h = l % g.H;
     int64_t pos = bar.req_pos0[r] + (int64_t)h * bar.req_per_head[r];
     for (int m = 0; m < mt; ++m) pos += unit_geom<NK>(R, bar.req_hist[r], m).n_tiles;
-    bar.beg = pos;
-    bar.end = pos + unit_geom<NK>(R, bar.req_hist[r], mt).n_tiles;
+    bar.rg_beg[0] = pos;
+    bar.rg_end[0] = pos + unit_geom<NK>(R, bar.req_hist[r], mt).n_tiles;
+    bar.nrg = 1;
   } else if (c >= grid - Gsk) {
-    bar.csk = c - (grid - Gsk);
-    bar.beg = cta_begin(total, bar.csk, Gsk);
-    bar.end = cta_begin(total, bar.csk + 1, Gsk);
+    const int cs = c - (grid - Gsk);
+    bar.csk = cs;
+    bar.p_waves = unit_start<NK>(g, bar, nw * Gsk);
+    for (int w = 0; w < nw; ++w) {
+      bar.rg_beg[w] = unit_start<NK>(g, bar, w * Gsk + cs);
+      bar.rg_end[w] = unit_start<NK>(g, bar, w * Gsk + cs + 1);
+    }
+    bar.rg_beg[nw] = cta_begin<NK>(g, bar, cs, Gsk);
+    bar.rg_end[nw] = cta_begin<NK>(g, bar, cs + 1, Gsk);
+    bar.nrg = nw + 1;
   }
 }
 
@@ -198,12 +266,12 @@ struct Seg {
   int64_t ustart;  // work item of the unit's tile 0
   Unit u;
   bool partial;
-  int slot;  // partial-output slot (0: first segment of the CTA, 1: last)
+  int slot;  // partial-output slot (0: first segment of the CTA's stream-K range, 1: last)
 };
 
 template <int NK>
-__device__ __forceinline__ Seg make_seg(const Geo &g, const Bars &bar, int64_t pos, int64_t end,
-                                        int k) {
+__device__ __noinline__ Seg make_seg(const Geo &g, const Bars &bar, int64_t pos, int64_t end,
+                                        int slot) {
   Seg s;
   s.r = 0;
   while (s.r + 1 < g.B && pos >= bar.req_pos0[s.r + 1]) ++s.r;
@@ -229,7 +297,7 @@ __device__ __forceinline__ Seg make_seg(const Geo &g, const Bars &bar, int64_t p
   s.m0 = s.mt * ROWS;
   s.uid = bar.req_unit0[s.r] + s.h * ((R.lq + ROWS - 1) / ROWS) + s.mt;
   s.partial = !(s.t0 == 0 && s.t1 == s.u.n_tiles);
-  s.slot = k == 0 ? 0 : 1;
+  s.slot = slot;
   return s;
 }
 
@@ -275,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const int32_t *__restrict__ sel_page, const int32_t *__restrict__ n_sel,
                    float scale_log2, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
                    int o_v8, float *__restrict__ part_o, float *__restrict__ part_lse,
-                   int32_t *__restrict__ unit_cnt, int Gsk) {
+                   int32_t *__restrict__ unit_cnt, int Gsk, int waves_ok) {
   using LY = Layout<D, NK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -304,14 +372,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar.drain, 2);
     bar.abort = 0;
     build_tables<NK>(g, n_sel, bar);
-    schedule<NK>(g, bar, Gsk);
+    schedule<NK>(g, bar, Gsk, waves_ok);
     fence_mbar_init();
   }
   __syncthreads();
   const int64_t total = bar.total;
-  const int64_t beg = bar.beg, end = bar.end;
   const int csk = bar.csk;  // partial results only arise under stream-K
-  if (beg >= end) return;   // a CTA without work (uniform: before any TMEM use)
+  const int nrg = bar.nrg;  // ranges: whole units, then (last) the stream-K range
+  int rg0 = 0;              // the first range that holds work
+  while (rg0 < nrg && bar.rg_beg[rg0] >= bar.rg_end[rg0]) ++rg0;
+  if (rg0 == nrg) return;   // a CTA without work (uniform: before any TMEM use)
   if (warp == 1) {
     tmem_alloc(&bar.tmem_base, TMEM_COLS);
     tmem_relinquish();
@@ -336,9 +406,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     int qn[2] = {0, 0};    // Q_A / Q_B loads issued so far
     bool ok = true;
     int k = 0;
-    for (int64_t pos = beg; ok && pos < end; ++k) {
-      const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+    // the CTA's ranges in order (units of the waves, then the stream-K range);
+    // only the stream-K range's first and last segments can be partial
+    int rg = rg0;
+    for (int64_t pos = bar.rg_beg[rg0]; ok && rg < nrg; ++k) {
+      const int64_t re = bar.rg_end[rg];
+      const Seg sg = make_seg<NK>(g, bar, pos, re, rg == nrg - 1 && pos == bar.rg_beg[rg] ? 0 : 1);
       pos += sg.t1 - sg.t0;
+      if (pos >= re) {
+        do ++rg; while (rg < nrg && bar.rg_beg[rg] >= bar.rg_end[rg]);
+        if (rg < nrg) pos = bar.rg_beg[rg];
+      }
       const ReqDesc &R = g.req[sg.r];
       const int32_t *pages = sel_page + (int64_t)sg.r * g.bt_stride;
       for (int x = 0; x < (sg.u.has_b ? 2 : 1); ++x) {
@@ -471,9 +549,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       int qm = 0;   // Q loads of this tile consumed
       int k = 0;
       bool ok = true;
-      for (int64_t pos = beg; ok && pos < end; ++k) {
-        const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+      // the CTA's ranges in order (units of the waves, then the stream-K range);
+      // only the stream-K range's first and last segments can be partial
+      int rg = rg0;
+      for (int64_t pos = bar.rg_beg[rg0]; ok && rg < nrg; ++k) {
+        const int64_t re = bar.rg_end[rg];
+        const Seg sg = make_seg<NK>(g, bar, pos, re, rg == nrg - 1 && pos == bar.rg_beg[rg] ? 0 : 1);
         pos += sg.t1 - sg.t0;
+        if (pos >= re) {
+          do ++rg; while (rg < nrg && bar.rg_beg[rg] >= bar.rg_end[rg]);
+          if (rg < nrg) pos = bar.rg_beg[rg];
+        }
         const int nt = sg.t1 - sg.t0;
         const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
         const int nx = max(0, min(n_x, sg.t1) - sg.t0);
@@ -546,9 +632,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     int k = 0;
     bool ok = true;
-    for (int64_t pos = beg; ok && pos < end; ++k) {
-      const Seg sg = make_seg<NK>(g, bar, pos, end, k);
+    // the CTA's ranges in order (units of the waves, then the stream-K range);
+    // only the stream-K range's first and last segments can be partial
+    int rg = rg0;
+    for (int64_t pos = bar.rg_beg[rg0]; ok && rg < nrg; ++k) {
+      const int64_t re = bar.rg_end[rg];
+      const Seg sg = make_seg<NK>(g, bar, pos, re, rg == nrg - 1 && pos == bar.rg_beg[rg] ? 0 : 1);
       pos += sg.t1 - sg.t0;
+      if (pos >= re) {
+        do ++rg; while (rg < nrg && bar.rg_beg[rg] >= bar.rg_end[rg]);
+        if (rg < nrg) pos = bar.rg_beg[rg];
+      }
       const ReqDesc &R = g.req[sg.r];
       const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
       const int nx = max(0, min(n_x, sg.t1) - sg.t0);
@@ -693,12 +787,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // c0's last segment (slot 1) unless it starts c0's range, and the first
       // segment (slot 0) of every later CTA.
       const int64_t uend = sg.ustart + sg.u.n_tiles;
-      const int c0 = cta_of(total, G, sg.ustart), c1 = cta_of(total, G, uend - 1);
+      const int c0 = cta_of<NK>(g, bar, G, sg.ustart), c1 = cta_of<NK>(g, bar, G, uend - 1);
       __threadfence();  // this thread's part is visible GPU-wide
       if (!group_sync()) break;
       if (row == 0) {
         int nparts = 0;
-        for (int c = c0; c <= c1; ++c) nparts += cta_begin(total, c, G) < cta_begin(total, c + 1, G);
+        for (int c = c0; c <= c1; ++c)
+          nparts += cta_begin<NK>(g, bar, c, G) < cta_begin<NK>(g, bar, c + 1, G);
         __threadfence();
         const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, 1);
         __threadfence();
@@ -708,8 +803,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!*reinterpret_cast<volatile int *>(&bar.last[x])) continue;  // uniform in the group
       __threadfence();
       auto part_row = [&](int c) -> int64_t {  // -1: CTA without items
-        const int64_t bc = cta_begin(total, c, G);
-        if (bc == cta_begin(total, c + 1, G)) return -1;
+        const int64_t bc = cta_begin<NK>(g, bar, c, G);
+        if (bc == cta_begin<NK>(g, bar, c + 1, G)) return -1;
         const int slot = (c == c0 && bc < sg.ustart) ? 1 : 0;
         return ((int64_t)c * 2 + slot) * ROWS + x * BM + row;
       };
@@ -803,6 +898,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Whether large launches may run waves of whole units before stream-K.  They
+// pay where the keys and values a launch reads (at most every history and
+// chunk token of every request and KV head) are more than twice L2: stream-K
+// CTAs at unrelated positions then each stream their own pages from DRAM.
+// Below that, stream-K alone measured faster (the pages stay in L2 anyway).
+// XATTN_ATTN_SCHEDULE = "waves" or "streamk" overrides the choice (tests and
+// tuning).
+inline int waves_allowed(const Geo &g) {
+  const char *env = getenv("XATTN_ATTN_SCHEDULE");
+  if (env && strcmp(env, "waves") == 0) return 1;
+  if (env && strcmp(env, "streamk") == 0) return 0;
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+    return 0;
+  int64_t kv_bytes = 0;
+  for (int r = 0; r < g.B; ++r)
+    kv_bytes += (int64_t)g.Hkv * (g.req[r].kh + g.req[r].lq) * g.D * 2 * 2;
+  return kv_bytes > 2 * (int64_t)l2 ? 1 : 0;
+}
+
 template <int D, int NK>
 cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv_bfloat16 *kcur,
                       const __nv_bfloat16 *vcur, const __nv_bfloat16 *kpool,
@@ -853,12 +969,12 @@ cudaError_t launch_tc(const Geo &g, int grid, const __nv_bfloat16 *q, const __nv
   if (e != cudaSuccess) return e;
   const int o_v8 = (reinterpret_cast<uintptr_t>(o) % 32 == 0) && ((g.q_hs * 2) % 32 == 0);
   // one CTA per unit (the whole-units schedule), at least Gsk (stream-K): the
-  // kernel decides on the device which of the two it runs
+  // kernel decides on the device which it runs
   const int Gsk = grid;
   const int ctas = nunits > Gsk ? nunits : Gsk;
   attn_tc_kernel<D, NK><<<ctas, THREADS, LY::SMEM_ALLOC, st>>>(
       g, tm, sel_page, n_sel, scale * 1.4426950408889634f, o, lse, o_v8, part_o, part_lse,
-      unit_cnt, Gsk);
+      unit_cnt, Gsk, waves_allowed(g));
   return cudaGetLastError();
 }
 
