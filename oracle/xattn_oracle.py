@@ -230,6 +230,35 @@ def block_sums_chunked(q, k_hist, k_cur, stride, block, scale, col_chunks,
     return normalized_block_sums(s, m, l, block // stride), (m, l)
 
 
+def sampled_block_sums_one_head(q, k_hist, k_cur, stride, block, scale, samples,
+                                mode="antidiag"):
+    """Block sums estimated from a sample of each history block's keys ([BSA]
+    性能分析, 优化方向 2: estimate from part of the K blocks; the chunked
+    policy page's Phase 1 loads samples_per_chunk tokens of each history
+    chunk).  Reading: of each history block only its first `samples` reshaped
+    columns (samples * stride tokens) are scored; each sampled cell stands for
+    block/stride / samples cells of its block, so it carries the weight
+    w = (block/stride) / samples in the row's softmax sum and in the block's
+    sum; the current chunk's columns are all scored (weight 1).  With
+    samples = block/stride this is block_sums_one_head.  Returns [Qb, Kb]."""
+    rb = block // stride
+    assert 1 <= samples <= rb
+    s = estimation_scores(q, k_hist, k_cur, stride, scale, mode)
+    ch = k_hist.shape[0] // stride
+    col = np.arange(s.shape[1])
+    sampled = (col >= ch) | ((col % rb) < samples)     # history: first `samples` of a block
+    w = np.where(col < ch, rb / samples, 1.0)
+    s = np.where(sampled[None, :], s, NEG_INF)
+    m = np.max(s, axis=-1)
+    p = np.zeros_like(s)
+    fin = np.isfinite(m)
+    p[fin] = w[None, :] * np.exp(s[fin] - m[fin, None])
+    l = p.sum(axis=-1)
+    p[fin] /= l[fin, None]
+    rq, c = s.shape
+    return p.reshape(rq // rb, rb, c // rb, rb).sum(axis=(1, 3))
+
+
 # ---------------------------------------------------------------------------
 # Selection  [BSA] Steps 3-4
 # ---------------------------------------------------------------------------

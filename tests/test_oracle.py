@@ -265,6 +265,58 @@ def test_estimation_scale_decides_block_sums_and_selection():
     assert keep.tolist() == [True, False, True]
 
 
+def _sampled_bruteforce(q, kh, kc, S, block, scale, samples):
+    """Explicit loops over rows and columns of the sampled estimate: the
+    antidiagonal score of every visible cell, history cells outside a block's
+    first `samples` reshaped columns left out, the others weighted Br/samples."""
+    rb = block // S
+    rq, ch, cc = q.shape[0] // S, kh.shape[0] // S, kc.shape[0] // S
+    K = np.concatenate([kh, kc])
+    out = np.zeros((rq // rb, (ch + cc) // rb))
+    for a in range(rq):
+        cells = []
+        for b in range(ch + cc):
+            if b < ch and b % rb >= samples:
+                continue
+            if b >= ch and b - ch > a:
+                continue
+            sc = scale * sum(float(q[S * a + S - 1 - i] @ K[S * b + i]) for i in range(S))
+            cells.append((b, sc, rb / samples if b < ch else 1.0))
+        m = max(c[1] for c in cells)
+        tot = sum(wt * math.exp(sc - m) for _, sc, wt in cells)
+        for b, sc, wt in cells:
+            out[a // rb, b // rb] += wt * math.exp(sc - m) / tot
+    return out
+
+
+@pytest.mark.parametrize("samples", [1, 2, 4])
+def test_sampled_estimation_bruteforce(samples):
+    q, kh, kc, S, block = _rand_problem(31 + samples, lh=48, lq=16, S=2, block=8)
+    got = O.sampled_block_sums_one_head(q, kh, kc, S, block, 0.4, samples)
+    want = _sampled_bruteforce(q, kh, kc, S, block, 0.4, samples)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-14)
+    assert np.allclose(got.sum(axis=1), block // S, rtol=1e-12)   # rows still sum to Br
+
+
+def test_sampled_estimation_reductions():
+    """All samples -> the full estimate; keys constant within each history block
+    -> every sample size gives the full estimate (each sampled cell then equals
+    the cells it stands for)."""
+    q, kh, kc, S, block = _rand_problem(9, lh=64, lq=16, S=4, block=16)
+    rb = block // S
+    full = O.block_sums_one_head(q, kh, kc, S, block, 0.3)
+    assert np.allclose(O.sampled_block_sums_one_head(q, kh, kc, S, block, 0.3, rb), full,
+                       rtol=1e-13, atol=0)
+    # one key per block, repeated: every reshaped column of a block scores alike
+    rng = np.random.default_rng(10)
+    kb = rng.standard_normal((kh.shape[0] // block, kh.shape[1]))
+    kconst = np.repeat(kb, block, axis=0)
+    full = O.block_sums_one_head(q, kconst, kc, S, block, 0.3)
+    for samples in (1, 2, 3):
+        got = O.sampled_block_sums_one_head(q, kconst, kc, S, block, 0.3, samples)
+        assert np.allclose(got, full, rtol=1e-12, atol=1e-15)
+
+
 def test_block_sums_of_sampled_query_blocks_match_full():
     q, kh, kc, S, block = _rand_problem(5, lh=32, lq=32, S=4, block=8)
     full = O.block_sums_one_head(q, kh, kc, S, block, 0.45)

@@ -61,6 +61,8 @@ PINS = {
     "per_kv_attend": P.test_attention_with_pages_per_kv_head,
     "est_scale": P.test_default_estimation_scale_hand_values,
     "est_scale_bs": P.test_estimation_scale_decides_block_sums_and_selection,
+    "sampled_brute": _each(P.test_sampled_estimation_bruteforce, (1,), (2,), (4,)),
+    "sampled_reduce": P.test_sampled_estimation_reductions,
 }
 
 # (oracle function, exact source fragment, its mistaken replacement, pins that must catch it)
@@ -163,6 +165,15 @@ MUTANTS = [
      ["est_scale", "est_scale_bs"]),
     ("default_estimation_scale", "math.sqrt(head_dim) * stride", "head_dim * stride",
      ["est_scale", "est_scale_bs"]),
+    # sampled estimation ([BSA] 性能分析, 优化方向 2)
+    ("sampled_block_sums_one_head", "w = np.where(col < ch, rb / samples, 1.0)",
+     "w = np.where(col < ch, 1.0, 1.0)", ["sampled_brute", "sampled_reduce"]),
+    ("sampled_block_sums_one_head", "((col % rb) < samples)", "((col % rb) <= samples)",
+     ["sampled_brute", "sampled_reduce"]),
+    ("sampled_block_sums_one_head", "(col >= ch) |", "(col < 0) |",
+     ["sampled_brute", "sampled_reduce"]),
+    ("sampled_block_sums_one_head", "p[fin] /= l[fin, None]", "p[fin] /= p.shape[1]",
+     ["sampled_brute", "sampled_reduce"]),
     # layer ring ([PLAN] Phases 1.1 and 4)
     ("ring_slot", "layer % num_buffers", "layer // num_buffers", ["ring"]),
     ("ring_schedule", "if l + num_buffers < num_layers", "if l + num_buffers <= num_layers",
