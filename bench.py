@@ -183,14 +183,14 @@ class Timed:
     by step with CUDA events on one stream (estimate, select, attention of
     every chunk bracketed separately)."""
 
-    def __init__(self, name, tau, dev, est_from_pages=False, per_kv_head=False):
+    def __init__(self, name, tau, dev, est_from_pages=False, per_kv_head=False, samples=0):
         import torch
         from xattention_block_sparse_gb300 import inputs as I
         from xattention_block_sparse_gb300 import runner as RN
         from xattention_block_sparse_gb300 import xattn as X
         self.torch, self.RN, self.X = torch, RN, X
         self.name, self.tau, self.dev = name, tau, dev
-        self.est_from_pages, self.per_kv = est_from_pages, per_kv_head
+        self.est_from_pages, self.per_kv, self.samples = est_from_pages, per_kv_head, samples
         self.wl = wl = I.make_workload(name)
         self.cfg = cfg = wl.cfg
         self.L, self.chunk = cfg.L, cfg.chunk
@@ -202,7 +202,8 @@ class Timed:
         self.BT = torch.from_numpy(wl.block_table).to(dev)
         self.seq = RN.SequencePrefill(cfg.H, cfg.Hkv, cfg.D, cfg.stride, cfg.block, self.L,
                                       self.chunk, self.BT, self.KP.shape[0],
-                                      est_from_pages=est_from_pages, per_kv_head=per_kv_head)
+                                      est_from_pages=est_from_pages, per_kv_head=per_kv_head,
+                                      est_samples=samples)
         self.O = torch.empty((cfg.H, self.L, cfg.D), dtype=torch.bfloat16, device=dev)
         self.LSE = torch.empty((cfg.H, self.L), dtype=torch.float32, device=dev)
         self.stream = torch.cuda.Stream(device=dev)
@@ -221,6 +222,9 @@ class Timed:
             if self.est_from_pages:
                 X.xattn_estimate(p, Q[:, t0:], K[:, t0:], KP, scale, b.workspace, b.block_sums,
                                  st)
+            elif self.samples:
+                X.xattn_estimate_sampled(p, Q[:, t0:], K, [0], self.samples, scale, b.workspace,
+                                         b.block_sums, st)
             else:  # keys in token order: K [Hkv, L, D] holds the history and the chunk
                 X.xattn_estimate_seq(p, Q[:, t0:], K, [0], scale, b.workspace, b.block_sums, st)
             if ev is not None:
@@ -246,7 +250,11 @@ class Timed:
                 n_sel.append(float(n.mean()) if self.per_kv else int(n[0]))
         return n_sel
 
-    def run(self, steps, warmup, sample_clocks=None):
+    def run(self, steps, warmup, sample_clocks=None, graph=True):
+        """Per-stage times from eager calls (events around each call), then the
+        timed steps: one replay per step of a CUDA graph of the whole step, so
+        that the GPU never waits for the host between launches (eager launches
+        of short kernels can outrun the host)."""
         torch = self.torch
         self.n_sel = self.selections()
         for _ in range(warmup):
@@ -257,26 +265,53 @@ class Timed:
         events = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                    for _ in range(self.nchunk)] for _ in range(steps)]
         torch.cuda.synchronize()
-        clk = ClockSampler(self.dev.index or 0) if sample_clocks else None
-        t_wall = time.perf_counter()
         with torch.cuda.stream(self.stream):
             for s in range(steps):
                 self.flush.zero_()  # L2 flush between steps (outside the step events)
                 self.step(events[s])
         torch.cuda.synchronize()
-        self.wall = time.perf_counter() - t_wall
-        self.clocks = clk.stop() if clk else None
         est = sel = att = 0.0
-        self.step_ms = []
+        eager_ms = []
         for s in range(steps):
             for c in range(self.nchunk):
                 e = events[s][c]
                 est += e[0].elapsed_time(e[1])
                 sel += e[1].elapsed_time(e[2])
                 att += e[2].elapsed_time(e[3])
-            self.step_ms.append(events[s][0][0].elapsed_time(events[s][self.nchunk - 1][3]))
+            eager_ms.append(events[s][0][0].elapsed_time(events[s][self.nchunk - 1][3]))
         self.stage = {"estimate_ms_per_step": est / steps, "select_ms_per_step": sel / steps,
                       "attention_ms_per_step": att / steps}
+        self.eager_ms = float(np.mean(eager_ms))
+        self.graph, self.timing = None, "eager launches, events around each step"
+        if graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream, capture_error_mode="relaxed"):
+                    self.step()
+                torch.cuda.synchronize()
+                self.graph = g
+                self.timing = "one CUDA graph replay per step (the step's launches captured once)"
+            except Exception as e:  # capture refused: time the eager launches
+                self.timing += f" (graph capture failed: {type(e).__name__})"
+        se = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        clk = ClockSampler(self.dev.index or 0) if sample_clocks else None
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            for s in range(steps):
+                self.flush.zero_()
+                se[s][0].record(self.stream)
+                if self.graph is not None:
+                    self.graph.replay()
+                else:
+                    self.step()
+                se[s][1].record(self.stream)
+        torch.cuda.synchronize()
+        self.wall = time.perf_counter() - t_wall
+        self.clocks = clk.stop() if clk else None
+        assert self.X.xattn_device_error() == 0
+        self.step_ms = [a.elapsed_time(b) for a, b in se]
         self.steps = steps
         return self
 
@@ -298,6 +333,7 @@ class Timed:
         att_tflops = (f_att / self.nchunk) / (att_launch_ms * 1e-3) / 1e12
         est_tflops = f_est / (self.stage["estimate_ms_per_step"] * 1e-3) / 1e12
         return {"value": self.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+                "ms_per_step_eager": self.eager_ms, "timing": self.timing,
                 "density": self.density(), "n_sel_per_chunk": self.n_sel,
                 "attention": {"achieved_tflops": att_tflops,
                               "frac": att_tflops / peaks["bf16_tflops"],
@@ -307,7 +343,7 @@ class Timed:
                 **self.stage}
 
     def release(self):
-        for name in ("Q", "K", "V", "KP", "VP", "O", "LSE", "flush", "seq", "wl"):
+        for name in ("graph", "Q", "K", "V", "KP", "VP", "O", "LSE", "flush", "seq", "wl"):
             setattr(self, name, None)
         self.torch.cuda.empty_cache()
 
@@ -330,15 +366,9 @@ def run_ours(args, ws, rank, local):
     tau = args.tau
     T = Timed(args.workload, tau, dev, est_from_pages=args.est_from_pages)
     cfg, L, chunk, nchunk = T.cfg, T.L, T.chunk, T.nchunk
-    T.n_sel = T.selections()
-    for _ in range(args.warmup):
-        with torch.cuda.stream(T.stream):
-            T.step()
-    torch.cuda.synchronize()
-    assert X.xattn_device_error() == 0
     if ws > 1:
         dist.barrier()
-    T.run(args.steps, 0, sample_clocks=True)
+    T.run(args.steps, args.warmup, sample_clocks=True, graph=not args.eager)
     if ws > 1:
         dist.barrier()
     step_ms, stage, clocks, wall, n_sel = T.step_ms, T.stage, T.clocks, T.wall, T.n_sel
@@ -372,11 +402,14 @@ def run_ours(args, ws, rank, local):
     # per KV head
     extra = {}
     if not args.skip_sparse:
-        for key, per_kv in (("sparse", False), ("sparse_per_kv_head", True)):
-            S_ = Timed("q06b_32k_sparse", tau, dev, per_kv_head=per_kv)
-            S_.run(args.steps, args.warmup)
+        for key, per_kv, samples in (("sparse", False, 0), ("sparse_per_kv_head", True, 0),
+                                     ("sparse_sampled_estimate", False, 4)):
+            S_ = Timed("q06b_32k_sparse", tau, dev, per_kv_head=per_kv, samples=samples)
+            S_.run(args.steps, args.warmup, graph=not args.eager)
             extra[key] = {"workload": workload_desc("q06b_32k_sparse", tau)
-                          + (", one block set per KV head" if per_kv else ", majority vote"),
+                          + (", one block set per KV head" if per_kv else ", majority vote")
+                          + (f", history estimated from the first {samples} of each block's "
+                             f"16 reshaped columns" if samples else ""),
                           **S_.summary(peaks)}
             S_.release()
 
@@ -397,7 +430,9 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) bf16 with RoPE theta 1e6; no model weights)",
         "config": {"workload": workload_desc(args.workload, tau), "tokens_per_step": L,
                    "chunks": nchunk, "l2": "flushed between steps (256 MiB write)",
-                   "parallelism": f"replicas x{ws}"},
+                   "parallelism": f"replicas x{ws}", "timing": T.timing,
+                   "stage_times": "eager calls, CUDA events around each call"},
+        "ms_per_step_eager": T.eager_ms,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel (bsa_chunk_attention)",
                      "achieved": att_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": att_tflops / peaks["bf16_tflops"],
@@ -584,6 +619,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="q06b_32k")
     ap.add_argument("--tau", type=float, default=0.9)
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of replays of a CUDA graph of the step")
     ap.add_argument("--skip-sparse", action="store_true",
                     help="time only the headline workload (no sparse-workload lines)")
     ap.add_argument("--est-from-pages", action="store_true",

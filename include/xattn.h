@@ -187,6 +187,27 @@ xattn_status xattn_estimate_seq(const xattn_problem *p, const void *q, const voi
                                 size_t workspace_bytes, float *block_sums,
                                 xattn_stream_t stream);
 
+/* Estimation from a sample of each history block's keys (BSA policy page,
+ * 性能分析, 优化方向 2: estimate with part of the K blocks; the chunked-prefill
+ * page's Phase 1 loads samples_per_chunk tokens of each history chunk).  Of
+ * every history block only its first `samples` reshaped columns
+ * (samples * S tokens) are scored; each sampled cell stands for
+ * (block_size / S) / samples cells of its block, so it is counted with that
+ * weight in the row's softmax sum and in the block's sum.  The current chunk's
+ * columns are all scored.  With the history sampled the score GEMM does about
+ * samples / (block_size / S) of the history work.  A request whose sampled
+ * columns, rounded up to 128, would not be fewer than its history's is
+ * estimated in full.
+ *   samples   (block_size / S) / 4 or / 2, and >= 4 (XATTN_EUNSUPPORTED
+ *             otherwise)
+ *   k_seq_start[r]   a multiple of block_size (XATTN_EINVAL otherwise)
+ * Other arguments, outputs and errors as xattn_estimate_seq. */
+xattn_status xattn_estimate_sampled(const xattn_problem *p, const void *q, const void *k_seq,
+                                    int64_t k_seq_head_stride, int64_t k_seq_token_stride,
+                                    const int64_t *k_seq_start, int32_t samples, float scale,
+                                    void *workspace, size_t workspace_bytes, float *block_sums,
+                                    xattn_stream_t stream);
+
 /* Selection (BSA policy page, select_blocks Steps 3-4).
  * Per (request, head, query block) row, with integer masses
  * q_j = round_half_even(block_sums_j * 2^32), T = sum_j q_j, R = fl64(threshold*T):

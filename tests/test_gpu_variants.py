@@ -269,3 +269,124 @@ def test_one_shot_estimate_matches_kv_chunked_estimation():
                       int((O.threshold_select(ref.astype(np.float32), tau)
                            != cap[c]["mask"].reshape(bs.shape).astype(bool)).sum()),
                       int(bs.size), len(set(gpu.tolist()) ^ set(chunked.tolist()))))
+
+
+def _sampled_ref(q, hist, kcur, S, Bk, scale, samples):
+    """The library's rule: a request's history is sampled when its sampled
+    columns, rounded up to 128, are fewer than its history's columns."""
+    kbh = hist.shape[0] // Bk
+    hc = -(-kbh * samples // 128) * 128
+    if hc < hist.shape[0] // S:
+        return O.sampled_block_sums_one_head(q, hist, kcur, S, Bk, scale, samples)
+    return O.block_sums_one_head(q, hist, kcur, S, Bk, scale)
+
+
+@pytest.mark.parametrize("samples", [4, 8])
+def test_sampled_estimation_matches_oracle_q06b_4k(samples):
+    """xattn_estimate_sampled against the oracle's sampled estimate (chunks 2
+    and 3 sample their history; chunk 1's 8 blocks are estimated in full), and
+    the selection from the sampled block sums bit-exact."""
+    case = SequenceCase("q06b_4k")
+    cfg = case.cfg
+    q, k, _, kp, _ = case.oracle_inputs()
+    scale = RN.estimation_scale(cfg.D, cfg.stride)
+    br = cfg.block // cfg.stride
+    G = cfg.H // cfg.Hkv
+    for c in (1, 2, 3):
+        p, t0 = case.seq.problems[c], c * case.chunk
+        t1 = t0 + case.chunk
+        b = case.seq.bufs
+        X.xattn_estimate_sampled(p, case.Q[:, t0:], case.K, [0], samples, scale, b.workspace,
+                                 b.block_sums)
+        X.xattn_select(p, b.block_sums, 0.9, b.workspace, b.mask, b.sel_idx, b.sel_page,
+                       b.n_sel)
+        torch.cuda.synchronize()
+        assert X.xattn_device_error() == 0
+        kbh, qb = t0 // cfg.block, case.chunk // cfg.block
+        n = X.xattn_block_sums_count(p)
+        bs = b.block_sums[:n].cpu().numpy().reshape(cfg.H, qb, kbh + qb)
+        ref = np.stack([_sampled_ref(q[h, t0:t1], k[h // G, :t0], k[h // G, t0:t1], cfg.stride,
+                                     cfg.block, scale, samples) for h in range(cfg.H)])
+        check_block_sums(bs, ref, br, f"samples {samples} chunk {c}")
+        from gpu_common import check_selection
+        check_selection(bs, b.mask[:n].cpu().numpy().reshape(bs.shape), b.sel_idx[0].cpu().numpy(),
+                        b.sel_page[0].cpu().numpy(), int(b.n_sel[0].item()), 0.9, cfg.Hkv, kbh,
+                        case.wl.block_table[0], f"samples {samples} chunk {c}")
+
+
+def test_sampled_estimation_token_major_keys_and_varlen():
+    """Stride 16 (Br = 8, half of each block sampled) with keys laid out
+    [tokens, Hkv, D] as in a layer-ring slot, two requests whose key ranges
+    start at block multiples with a gap between them."""
+    d = dev()
+    rng = np.random.default_rng(61)
+    H, Hkv, D, S, Bk = 8, 2, 128, 16, 128
+    q_lens, kh_lens = [512, 256], [20 * Bk, 36 * Bk]
+    starts = [Bk, 2 * Bk + kh_lens[0] + q_lens[0]]
+    tot_k = starts[1] + kh_lens[1] + q_lens[1]
+    qq = I.bf16_round(rng.standard_normal((H, sum(q_lens), D), dtype=np.float32))
+    kt = I.bf16_round(rng.standard_normal((tot_k, Hkv, D), dtype=np.float32))
+    Q, KT = to_dev_bf16(qq), to_dev_bf16(kt)
+    # (the estimate reads no block table; the problem still describes the pool)
+    BT = torch.zeros((2, 40), dtype=torch.int32, device=d)
+    prob = X.Problem(H, Hkv, D, S, Bk, q_lens, kh_lens, BT, 1)
+    bufs = RN.ChunkBuffers.for_problems([prob], d)
+    scale = RN.estimation_scale(D, S)
+    X.xattn_estimate_sampled(prob, Q, KT, starts, 4, scale, bufs.workspace, bufs.block_sums,
+                             head_stride=D, token_stride=Hkv * D)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    f64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    qd, kd = f64(qq), f64(kt)
+    bs_all = bufs.block_sums.cpu().numpy()
+    G = H // Hkv
+    q0 = 0
+    for r in range(2):
+        lq, kh, st = q_lens[r], kh_lens[r], starts[r]
+        kbh, qb = kh // Bk, lq // Bk
+        off = X.xattn_block_sums_offset(prob, r)
+        bs = bs_all[off:off + H * qb * (kbh + qb)].reshape(H, qb, kbh + qb)
+        ref = np.stack([_sampled_ref(qd[h, q0:q0 + lq], kd[st:st + kh, h // G],
+                                     kd[st + kh:st + kh + lq, h // G], S, Bk, scale, 4)
+                        for h in range(H)])
+        check_block_sums(bs, ref, Bk // S, f"request {r}")
+        q0 += lq
+
+
+def test_chunk_captured_in_a_cuda_graph_replays_the_same_bits():
+    """Every entry point of a chunk (estimate in token order, select, attend)
+    enqueues only stream work after its host checks, so the chunk can be
+    captured once in a CUDA graph and replayed: the replays give exactly the
+    eager call's block sums, selection, O and LSE (the bench times its steps
+    this way)."""
+    case = SequenceCase("q06b_4k")
+    cfg = case.cfg
+    c, t0 = 3, 3 * case.chunk
+    p = case.seq.problems[c]
+    stream = torch.cuda.Stream(device=dev())
+
+    def outputs():
+        n = int(case.seq.bufs.n_sel[0].item())
+        return (case.seq.bufs.block_sums.clone(), case.seq.bufs.sel_page[0, :n].clone(),
+                O_[:, t0:].clone(), LSE[:, t0:].clone())
+
+    O_ = torch.zeros((cfg.H, case.L, cfg.D), dtype=torch.bfloat16, device=dev())
+    LSE = torch.zeros((cfg.H, case.L), dtype=torch.float32, device=dev())
+    with torch.cuda.stream(stream):
+        case.seq.run_chunk(c, case.Q, case.K, case.V, case.KP, case.VP, 0.9, O_, LSE, stream)
+    torch.cuda.synchronize()
+    want = outputs()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        case.seq.run_chunk(c, case.Q, case.K, case.V, case.KP, case.VP, 0.9, O_, LSE, stream)
+    for _ in range(2):
+        O_.zero_()
+        LSE.zero_()
+        case.seq.bufs.block_sums.zero_()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        assert X.xattn_device_error() == 0
+        for a, b in zip(want, outputs()):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b)

@@ -238,3 +238,21 @@ def test_runner_estimation_scale_equals_the_oracle_reading():
     for cfg in I.CONFIGS.values():
         assert RN.estimation_scale(cfg.D, cfg.stride) == O.default_estimation_scale(
             cfg.D, cfg.stride), cfg.name
+
+
+def test_sampled_estimation_argument_checks(lib):
+    """xattn_estimate_sampled refuses sample counts it has no kernel for and
+    key ranges that do not start on a block, before touching the GPU."""
+    import ctypes as C
+    p = _prob([1024], [4096])
+    starts = (C.c_int64 * 1)(0)
+    fake = C.c_void_p(0x10000)
+    # Br = 16: 4 and 8 are built; 2, 3 and 16 are not
+    for bad in (2, 3, 16):
+        assert lib.xattn_estimate_sampled(p.ref(), fake, fake, 128 * 5120, 0, starts, bad,
+                                          0.01, fake, 1 << 30, fake, None) == -5
+    assert lib.xattn_estimate_sampled(p.ref(), fake, fake, 128 * 5120, 0, starts, 0, 0.01, fake,
+                                      1 << 30, fake, None) == -1
+    off = (C.c_int64 * 1)(64)  # a multiple of the stride, not of the block
+    assert lib.xattn_estimate_sampled(p.ref(), fake, fake, 128 * 5120, 0, off, 4, 0.01, fake,
+                                      1 << 30, fake, None) == -1

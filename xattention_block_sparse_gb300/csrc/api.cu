@@ -82,6 +82,8 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
     d.bsum0 = (int32_t)bsum;
     d.sel0 = (int32_t)sel;
     d.att0 = (int32_t)att;
+    d.hc = (int32_t)(kh / S);
+    d.samp = 0;
     d.bpart_off = (int64_t)bpart;
     d.tstat_off = (int64_t)tstat;
     d.bs_off = (int64_t)bs;
@@ -310,6 +312,64 @@ static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *
                              reinterpret_cast<int32_t *>(ws + pl.ws.att_cnt), st));
 }
 
+// The estimation over keys in token order, every history column scored
+// (samples == 0) or the first `samples` reshaped columns of each history block.
+static xattn_status estimate_keys(const xattn_problem *p, const void *q, const void *k_seq,
+                                  int64_t k_seq_head_stride, int64_t k_seq_token_stride,
+                                  const int64_t *k_seq_start, int32_t samples, float scale,
+                                  void *workspace, size_t workspace_bytes, float *block_sums,
+                                  xattn_stream_t stream) {
+  Plan pl;
+  xattn_status s = make_plan(p, pl);
+  if (s != XATTN_OK) return s;
+  if (!q || !k_seq || !k_seq_start || !workspace || !block_sums) return XATTN_EINVAL;
+  const int D = p->head_dim, S = p->stride, Hkv = p->num_kv_heads, Bk = p->block_size;
+  const int br = Bk / S;
+  const int64_t hs = k_seq_head_stride, ts = k_seq_token_stride > 0 ? k_seq_token_stride : D;
+  if (k_seq_token_stride < 0 || hs < D || ts < D) return XATTN_EINVAL;
+  if (!aligned16(k_seq) || hs % 8 || ts % 8) return XATTN_EALIGN;
+  if (samples != 0 && !(samples >= 4 && (samples * 4 == br || samples * 2 == br)))
+    return XATTN_EUNSUPPORTED;
+  int64_t end = 0;
+  for (int r = 0; r < p->num_requests; ++r) {
+    const int64_t st0 = k_seq_start[r];
+    const ReqDesc &d = pl.geo.req[r];
+    if (st0 < 0 || st0 % (samples ? Bk : S)) return XATTN_EINVAL;
+    if (st0 / S + (int64_t)(d.kh + d.lq) / S > INT32_MAX) return XATTN_EINVAL;
+    pl.geo.req[r].ks0 = (int32_t)(st0 / S);
+    if (st0 + d.kh + d.lq > end) end = st0 + d.kh + d.lq;
+  }
+  // the two views of the keys must not overlap: head-major or token-major
+  if (Hkv > 1 && !(hs >= end * ts || ts >= (int64_t)Hkv * hs)) return XATTN_EINVAL;
+  if (samples) {
+    // a request samples its history when that leaves fewer columns: the
+    // sampled columns, padded to a statistics tile, before the chunk's; the
+    // score tiles are counted again on that layout
+    Geo &g = pl.geo;
+    g.ns = samples;
+    int64_t gemm = 0;
+    for (int r = 0; r < g.B; ++r) {
+      ReqDesc &d = g.req[r];
+      const int kbh = d.kh / Bk, rq = d.lq / S, ch = d.kh / S;
+      const int hc = (kbh * samples + kTileCols - 1) / kTileCols * kTileCols;
+      d.samp = hc < ch ? 1 : 0;
+      d.hc = d.samp ? hc : ch;
+      d.gemm0 = (int32_t)gemm;
+      int64_t per_head = 0;
+      for (int m0 = 0; m0 < rq; m0 += kGemmRows) {
+        const int last = (m0 + kGemmRows < rq ? m0 + kGemmRows : rq);
+        const int vis = d.hc + last;
+        per_head += (vis + kGemmCols - 1) / kGemmCols;
+      }
+      if (d.lq > 0) gemm += (int64_t)g.H * per_head;
+    }
+    pl.gemm_tiles = (int)gemm;
+  }
+  const KeySeq ks{static_cast<const __nv_bfloat16 *>(k_seq), hs, ts};
+  return run_estimate(pl, q, nullptr, nullptr, &ks, scale, workspace, workspace_bytes,
+                      block_sums, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" {
 
 size_t xattn_workspace_size(const xattn_problem *p) {
@@ -348,28 +408,18 @@ xattn_status xattn_estimate_seq(const xattn_problem *p, const void *q, const voi
                                 const int64_t *k_seq_start, float scale, void *workspace,
                                 size_t workspace_bytes, float *block_sums,
                                 xattn_stream_t stream) {
-  Plan pl;
-  xattn_status s = make_plan(p, pl);
-  if (s != XATTN_OK) return s;
-  if (!q || !k_seq || !k_seq_start || !workspace || !block_sums) return XATTN_EINVAL;
-  const int D = p->head_dim, S = p->stride, Hkv = p->num_kv_heads;
-  const int64_t hs = k_seq_head_stride, ts = k_seq_token_stride > 0 ? k_seq_token_stride : D;
-  if (k_seq_token_stride < 0 || hs < D || ts < D) return XATTN_EINVAL;
-  if (!aligned16(k_seq) || hs % 8 || ts % 8) return XATTN_EALIGN;
-  int64_t end = 0;
-  for (int r = 0; r < p->num_requests; ++r) {
-    const int64_t st0 = k_seq_start[r];
-    const ReqDesc &d = pl.geo.req[r];
-    if (st0 < 0 || st0 % S) return XATTN_EINVAL;
-    if (st0 / S + (int64_t)(d.kh + d.lq) / S > INT32_MAX) return XATTN_EINVAL;
-    pl.geo.req[r].ks0 = (int32_t)(st0 / S);
-    if (st0 + d.kh + d.lq > end) end = st0 + d.kh + d.lq;
-  }
-  // the two views of the keys must not overlap: head-major or token-major
-  if (Hkv > 1 && !(hs >= end * ts || ts >= (int64_t)Hkv * hs)) return XATTN_EINVAL;
-  const KeySeq ks{static_cast<const __nv_bfloat16 *>(k_seq), hs, ts};
-  return run_estimate(pl, q, nullptr, nullptr, &ks, scale, workspace, workspace_bytes,
-                      block_sums, reinterpret_cast<cudaStream_t>(stream));
+  return estimate_keys(p, q, k_seq, k_seq_head_stride, k_seq_token_stride, k_seq_start, 0, scale,
+                       workspace, workspace_bytes, block_sums, stream);
+}
+
+xattn_status xattn_estimate_sampled(const xattn_problem *p, const void *q, const void *k_seq,
+                                    int64_t k_seq_head_stride, int64_t k_seq_token_stride,
+                                    const int64_t *k_seq_start, int32_t samples, float scale,
+                                    void *workspace, size_t workspace_bytes, float *block_sums,
+                                    xattn_stream_t stream) {
+  if (samples <= 0) return XATTN_EINVAL;
+  return estimate_keys(p, q, k_seq, k_seq_head_stride, k_seq_token_stride, k_seq_start, samples,
+                       scale, workspace, workspace_bytes, block_sums, stream);
 }
 
 xattn_status xattn_select(const xattn_problem *p, const float *block_sums, double threshold,

@@ -29,6 +29,9 @@ struct ReqDesc {
   int32_t head0;   // first query head of the request's heads (nonzero only when a
                    // request stands for one KV head's group: per-KV-head attention)
   int32_t kvh0;    // KV head of head0 (idem)
+  int32_t hc;      // reshaped columns before the current chunk's: kh / S, or, when the
+                   // request's history is sampled, its sampled columns padded to 128
+  int32_t samp;    // 1: the history is estimated from a sample of each block's keys
   int64_t bpart_off;  // float offset of the request's [H, Qb, Kb, Br] block partial sums
   int64_t tstat_off;  // float2 offset of its [H, lq/S, ntiles] tile statistics
   int64_t bs_off;     // offset of its [H, Qb, Kb] block sums / mask
@@ -40,6 +43,8 @@ struct Geo {
   int64_t kv_ts;          // elements between tokens of k_cur / v_cur
   int32_t kv_head_inner;  // 1 when kv_hs < kv_ts (a [tokens, Hkv, D] layout)
   int32_t H_all, Hkv_all; // heads of the q / k tensors (H, Hkv unless a request is one group)
+  int32_t ns;             // sampled estimation: reshaped columns kept per history block
+                          // (0: every column)
   const int32_t *block_table;
   int32_t *err;  // device error word
   ReqDesc req[kMaxReq];

@@ -13,6 +13,10 @@
 //   A3  per KV block kb: BS = sum over the block's Br rows of
 //       P[a][kb] e^(m_t(kb) - m_a) / l_a,
 // which is the sum of exp(s - m)/l over the block's visible cells.
+// With a sampled history (ReqDesc::samp) the GEMM's columns are the sampled
+// history columns (g.ns per block, padded to hc) then the current chunk's;
+// the partials and tile sums already carry the samples' weight, and only the
+// tile of each block moves.
 #include "common.cuh"
 
 namespace xattn {
@@ -31,9 +35,10 @@ __global__ void __launch_bounds__(BTHR) block_sum_kernel(const __grid_constant__
   const int r = find_req(g, cta, [](const ReqDesc &d) { return d.bsum0; });
   const ReqDesc &R = g.req[r];
   const int S = g.S;
-  const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+  const int rq = R.lq / S, ch = R.hc, ncol = R.hc + rq;  // ch: columns before the chunk's
   const int ntile = (ncol + kTileCols - 1) / kTileCols;
-  const int Qb = R.lq / g.Bk, Kb = ncol / BR;
+  const int Qb = R.lq / g.Bk, Kbh = R.kh / g.Bk, Kb = Kbh + Qb;
+  const int hw = R.samp ? g.ns : BR;  // history columns of a block in the GEMM
   const int local = cta - R.bsum0;
   const int qb = local % Qb, h = local / Qb;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -70,7 +75,8 @@ __global__ void __launch_bounds__(BTHR) block_sum_kernel(const __grid_constant__
     float4 v[BR / 4];
 #pragma unroll
     for (int q = 0; q < BR / 4; ++q) v[q] = __ldcs(pp + q);
-    const int t = kb * BR / kTileCols;
+    // the statistics tile of the block's columns
+    const int t = (kb < Kbh ? kb * hw : ch + (kb - Kbh) * BR) / kTileCols;
     float acc = 0.f;
 #pragma unroll
     for (int q = 0; q < BR / 4; ++q) {
@@ -80,7 +86,8 @@ __global__ void __launch_bounds__(BTHR) block_sum_kernel(const __grid_constant__
         const int j = 4 * q + e, a = qb * BR + j;
         // a block starting right of the row's diagonal holds no visible cell
         // (and its partial was never written)
-        if (kb * BR <= ch + a) acc += vv[e] * __expf(ts_h[(int64_t)a * ntile + t].x - sm[j]) * sil[j];
+        if (kb < Kbh || (kb - Kbh) * BR <= a)
+          acc += vv[e] * __expf(ts_h[(int64_t)a * ntile + t].x - sm[j]) * sil[j];
       }
     }
     out[kb] = acc;

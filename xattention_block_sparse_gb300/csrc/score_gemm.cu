@@ -76,6 +76,8 @@ struct Maps {
   CUtensorMap q;         // queries (d, phase, group, head)
   CUtensorMap kp, kc;    // paged form: pool keys (5-D), current-chunk keys (4-D)
   CUtensorMap ks, ksh;   // sequence form: logical-order keys, 256- and 128-row boxes
+  CUtensorMap kh, khh;   // sampled history: the first ns groups of every block (5-D),
+                         // 256 and 128 rows a box
   int kc_head_inner;     // the current-chunk key view is (d, head, phase, group)
   int ks_head_inner;     // the key-sequence view is (d, head, phase, group)
 };
@@ -91,7 +93,7 @@ __device__ __forceinline__ Tile decode_tile(const Geo &g, int t) {
   const int r = find_req(g, t, [](const ReqDesc &d) { return d.gemm0; });
   const ReqDesc &R = g.req[r];
   const int S = g.S;
-  const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+  const int rq = R.lq / S, ch = R.hc, ncol = R.hc + rq;  // ch: columns before the chunk's
   int per_head = 0;
   for (int m0 = 0; m0 < rq; m0 += ROWS) {
     const int vis = min(ch + min(m0 + ROWS, rq), ncol);
@@ -134,7 +136,12 @@ __device__ __forceinline__ Tile decode_work(const Geo &g, int w, int nfull) {
 
 // SEQ: keys from the logical-order key sequence (one box per k-step), else
 // from the pool pages and the current chunk (one box per page per k-step).
-template <int BR, bool SEQ>
+// NS > 0 (with SEQ): requests marked samp keep the first NS reshaped columns
+// of each history block ("XAttention BSA Policy 设计文档", 性能分析,
+// 优化方向 2): their GEMM columns are the sampled history columns, padded to a
+// statistics tile, then the chunk's; each sampled cell carries the weight
+// BR / NS in the tile sums and block partials.
+template <int BR, bool SEQ, int NS>
 __global__ void __launch_bounds__(THREADS, 1)
     score_gemm_kernel(const __grid_constant__ Geo g, const __grid_constant__ Maps mp, int nwork,
                       int nfull, float scale, float *__restrict__ bpart,
@@ -221,7 +228,33 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(&bar.full[s], A_BYTES + tl.w * KSTEP * 2);
           // q rows S*a + S-1-i of this tile
           tma_load_4d(sA, &mp.q, &bar.full[s], dc, S - 1 - i, R.q0 / S + tl.m0, tl.h);
-          if (SEQ) {  // key rows S*b + i, b over the tile's columns: one box
+          bool loaded = false;
+          if constexpr (NS > 0) {
+            if (R.samp) {
+              // sampled history rows (blocks of NS groups), then chunk rows
+              uint8_t *dst = sA + A_BYTES;
+              int hrows = 0;
+              if (tl.n0 < R.hc) {
+                hrows = min(tl.w, R.hc - tl.n0);  // a whole box or half of one
+                const CUtensorMap *hm = hrows == COLS ? &mp.kh : &mp.khh;
+                const int blk = R.ks0 / BR + tl.n0 / NS;
+                if (mp.ks_head_inner)
+                  tma_load_5d(dst, hm, &bar.full[s], dc, kvh, i, 0, blk);
+                else
+                  tma_load_5d(dst, hm, &bar.full[s], dc, i, 0, blk, kvh);
+              }
+              if (hrows < tl.w) {
+                const CUtensorMap *cm = tl.w - hrows == COLS ? &mp.ks : &mp.ksh;
+                const int grp = R.ks0 + R.kh / S + max(tl.n0 - R.hc, 0);
+                if (mp.ks_head_inner)
+                  tma_load_4d(dst + hrows * 128, cm, &bar.full[s], dc, kvh, i, grp);
+                else
+                  tma_load_4d(dst + hrows * 128, cm, &bar.full[s], dc, i, grp, kvh);
+              }
+              loaded = true;
+            }
+          }
+          if (SEQ && !loaded) {  // key rows S*b + i, b over the tile's columns: one box
             const CUtensorMap *km = tl.w == COLS ? &mp.ks : &mp.ksh;
             const int grp = R.ks0 + tl.n0;
             if (mp.ks_head_inner)
@@ -298,7 +331,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = tile0; t < nwork; t += tstep, ++n) {
       const Tile tl = decode_work(g, t, nfull);
       const ReqDesc &R = g.req[tl.r];
-      const int rq = R.lq / S, ch = R.kh / S, ncol = (R.kh + R.lq) / S;
+      const int rq = R.lq / S, ch = NS > 0 ? R.hc : R.kh / S;
+      const int ncol = NS > 0 ? R.hc + rq : (R.kh + R.lq) / S;
       const int nj = tl.w / kTileCols;  // statistics tiles of the work item
       const int ntile = (ncol + kTileCols - 1) / kTileCols;
       const bool two_m = tl.m0 + TM < rq;
@@ -307,7 +341,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       if (x == 0 || two_m) {
         const bool row_ok = a < rq;
-        const int Qb = rq / BR, Kb = ncol / BR;
+        const int Qb = rq / BR, Kbh = R.kh / g.Bk;
+        const int Kb = NS > 0 ? Kbh + Qb : ncol / BR;
         // block partials are stored [H][Qb][Kb][Br]
         float *pbase = bpart + R.bpart_off +
                        ((int64_t)(tl.h * Qb + (row_ok ? a : 0) / BR) * Kb) * BR +
@@ -326,6 +361,46 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.acc_empty);
+          }
+          if constexpr (NS > 0) {
+            if (R.samp && c0 < ch) {
+              // sampled history columns [c0, c0 + nv), alike for every row;
+              // a tile of padding only gets empty statistics
+              if (!row_ok) continue;
+              const int64_t ti = R.tstat_off + ((int64_t)tl.h * rq + a) * ntile + c0 / kTileCols;
+              const int nv = min(kTileCols, Kbh * NS - c0);
+              if (nv <= 0) {
+                tstat[ti] = make_float2(-INFINITY, 0.f);
+                continue;
+              }
+              constexpr int NBH = kTileCols / NS;
+              float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int c = 0; c < kTileCols; ++c) {
+                const float f = __uint_as_float(v[c]) * scale;
+                v[c] = __float_as_uint(c < nv ? f : -INFINITY);
+                mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+              }
+              const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+              const float ml2 = m * 1.4426950408889634f;
+              float pb[NBH];
+#pragma unroll
+              for (int q = 0; q < NBH; ++q) pb[q] = 0.f;
+#pragma unroll
+              for (int c = 0; c < kTileCols; ++c)
+                pb[c / NS] += ex2(fmaf(__uint_as_float(v[c]), 1.4426950408889634f, -ml2));
+              constexpr float wgt = (float)(BR / NS);  // cells each sampled cell stands for
+              float l = 0.f;
+#pragma unroll
+              for (int q = 0; q < NBH; ++q) {
+                pb[q] *= wgt;
+                l += pb[q];
+                const int kb = c0 / NS + q;
+                if (kb < Kbh) pbase[(int64_t)kb * BR] = pb[q];
+              }
+              tstat[ti] = make_float2(m, l);
+              continue;
+            }
           }
           if (!row_ok || c0 >= ncol || c0 > ch + a) continue;
           // visible columns of the row in this tile: [c0, c0 + nv)
@@ -349,7 +424,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int q = 0; q < NB; ++q) {
             l += pb[q];
-            const int kb = c0 / BR + q;
+            // (with a sampled history the chunk's blocks follow its padded columns)
+            const int kb = (NS > 0 && c0 >= ch ? Kbh + (c0 - ch) / BR : c0 / BR) + q;
             if (kb < Kb) pbase[(int64_t)kb * BR] = pb[q];
           }
           tstat[R.tstat_off + ((int64_t)tl.h * rq + a) * ntile + c0 / kTileCols] =
@@ -420,6 +496,33 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
     if (!encode_phase_view(&mp.ksh, kseq->base, D, S, groups, g.Hkv, kseq->hs, kseq->ts,
                            COLS / 2, &hi))
       return cudaErrorInvalidValue;
+    if (g.ns > 0) {
+      // sampled history: (d, phase, group of the block, block, head), or the
+      // head second for token-major keys; a box takes the first ns groups of
+      // rows / ns consecutive blocks, landing as [block][group] rows
+      const int64_t nblk = (groups + BRc - 1) / BRc, hs = kseq->hs, ts = kseq->ts;
+      for (int half = 0; half < 2; ++half) {
+        const cuuint32_t nb = (cuuint32_t)((half ? COLS / 2 : COLS) / g.ns);
+        CUtensorMap *m = half ? &mp.khh : &mp.kh;
+        bool ok;
+        if (hi) {
+          const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)g.Hkv, (cuuint64_t)S,
+                                      (cuuint64_t)BRc, (cuuint64_t)nblk};
+          const cuuint64_t str[4] = {(cuuint64_t)hs * 2, (cuuint64_t)ts * 2,
+                                     (cuuint64_t)S * ts * 2, (cuuint64_t)g.Bk * ts * 2};
+          const cuuint32_t box[5] = {KSTEP, 1, 1, (cuuint32_t)g.ns, nb};
+          ok = encode_bf16(m, kseq->base, 5, dims, str, box);
+        } else {
+          const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BRc,
+                                      (cuuint64_t)nblk, (cuuint64_t)g.Hkv};
+          const cuuint64_t str[4] = {(cuuint64_t)ts * 2, (cuuint64_t)S * ts * 2,
+                                     (cuuint64_t)g.Bk * ts * 2, (cuuint64_t)hs * 2};
+          const cuuint32_t box[5] = {KSTEP, 1, (cuuint32_t)g.ns, nb, 1};
+          ok = encode_bf16(m, kseq->base, 5, dims, str, box);
+        }
+        if (!ok) return cudaErrorInvalidValue;
+      }
+    }
   } else {
     // current-chunk keys, Br groups per box
     if (!encode_phase_view(&mp.kc, kcur, D, S, tot_q / S, g.Hkv, g.kv_hs, g.kv_ts, BRc, &hi))
@@ -454,10 +557,21 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
     return cudaGetLastError();
   };
   const bool sq = kseq != nullptr;
+  if (g.ns > 0) {  // sampled history (keys in token order only): Br / 4 or Br / 2, >= 4
+    if (!sq) return cudaErrorInvalidValue;
+    switch (g.Bk / S * 100 + g.ns) {
+      case 804: return run(score_gemm_kernel<8, true, 4>);
+      case 1604: return run(score_gemm_kernel<16, true, 4>);
+      case 1608: return run(score_gemm_kernel<16, true, 8>);
+      case 3208: return run(score_gemm_kernel<32, true, 8>);
+      case 3216: return run(score_gemm_kernel<32, true, 16>);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (g.Bk / S) {  // Br: reshaped columns per KV block
-    case 8: return sq ? run(score_gemm_kernel<8, true>) : run(score_gemm_kernel<8, false>);
-    case 16: return sq ? run(score_gemm_kernel<16, true>) : run(score_gemm_kernel<16, false>);
-    case 32: return sq ? run(score_gemm_kernel<32, true>) : run(score_gemm_kernel<32, false>);
+    case 8: return sq ? run(score_gemm_kernel<8, true, 0>) : run(score_gemm_kernel<8, false, 0>);
+    case 16: return sq ? run(score_gemm_kernel<16, true, 0>) : run(score_gemm_kernel<16, false, 0>);
+    case 32: return sq ? run(score_gemm_kernel<32, true, 0>) : run(score_gemm_kernel<32, false, 0>);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -55,6 +55,8 @@ class KeySeq:
     starts: list
     head_stride: int
     token_stride: int = 0
+    samples: int = 0          # > 0: score the first `samples` reshaped columns of each
+                              # history block only (xattn_estimate_sampled)
 
 
 def estimate_select(problem, q, k_cur, k_pool, tau, bufs: ChunkBuffers, est_scale=None,
@@ -65,7 +67,11 @@ def estimate_select(problem, q, k_cur, k_pool, tau, bufs: ChunkBuffers, est_scal
     per_kv_head: one block set per KV head instead of the vote across them."""
     D = problem.c.head_dim
     est_scale = estimation_scale(D, problem.c.stride) if est_scale is None else est_scale
-    if k_seq is not None:
+    if k_seq is not None and k_seq.samples:
+        X.xattn_estimate_sampled(problem, q, k_seq.keys, k_seq.starts, k_seq.samples, est_scale,
+                                 bufs.workspace, bufs.block_sums, stream,
+                                 head_stride=k_seq.head_stride, token_stride=k_seq.token_stride)
+    elif k_seq is not None:
         X.xattn_estimate_seq(problem, q, k_seq.keys, k_seq.starts, est_scale, bufs.workspace,
                              bufs.block_sums, stream, head_stride=k_seq.head_stride,
                              token_stride=k_seq.token_stride)
@@ -105,12 +111,15 @@ class SequencePrefill:
     through the block table for its attention.  The estimation reads the keys
     [0, (c+1)*chunk) of K in token order (xattn_estimate_seq), or, with
     est_from_pages, the history pages and the chunk's K (xattn_estimate): the
-    two give the same bits.  per_kv_head selects one block set per KV head."""
+    two give the same bits.  per_kv_head selects one block set per KV head;
+    est_samples > 0 estimates each history block from its first est_samples
+    reshaped columns (xattn_estimate_sampled)."""
 
     def __init__(self, H, Hkv, D, stride, block, L, chunk, block_table, num_pages,
-                 with_mask=False, est_from_pages=False, per_kv_head=False):
+                 with_mask=False, est_from_pages=False, per_kv_head=False, est_samples=0):
         self.H, self.Hkv, self.D, self.L, self.chunk = H, Hkv, D, L, chunk
         self.est_from_pages = est_from_pages
+        self.est_samples = est_samples
         self.per_kv_head = per_kv_head
         self.problems = [
             X.Problem(H, Hkv, D, stride, block, [chunk], [c * chunk], block_table, num_pages,
@@ -124,7 +133,8 @@ class SequencePrefill:
             self.bufs.n_sel = torch.empty(Hkv, dtype=torch.int32, device=dev)
 
     def key_seq(self, K):
-        return None if self.est_from_pages else KeySeq(K, [0], K.stride(0))
+        return None if self.est_from_pages else KeySeq(K, [0], K.stride(0),
+                                                       samples=self.est_samples)
 
     def run_chunk(self, c, Q, K, V, kpool, vpool, tau, O, LSE, stream=None):
         t0 = c * self.chunk

@@ -26,7 +26,8 @@ STATUS = {0: "XATTN_OK", -1: "XATTN_EINVAL", -2: "XATTN_EALIGN", -3: "XATTN_EPAG
           -7: "XATTN_ETIMEOUT"}
 
 EXPORTED = ["xattn_workspace_size", "xattn_block_sums_count", "xattn_block_sums_offset",
-            "xattn_estimate", "xattn_estimate_seq", "xattn_select", "xattn_select_per_kv_head",
+            "xattn_estimate", "xattn_estimate_seq", "xattn_estimate_sampled", "xattn_select",
+            "xattn_select_per_kv_head",
             "xattn_select_noalloc", "bsa_chunk_attention", "bsa_chunk_attention_per_kv_head",
             "lse_merge", "xattn_store_kv",
             "xattn_device_error", "xattn_last_device_error", "xattn_copy_rows_async",
@@ -82,6 +83,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "xattn_estimate": (ctypes.c_int, [P, vp, vp, vp, f32, vp, sz, vp, vp]),
         "xattn_estimate_seq": (ctypes.c_int, [P, vp, vp, i64, i64, ctypes.POINTER(i64), f32, vp,
                                                sz, vp, vp]),
+        "xattn_estimate_sampled": (ctypes.c_int, [P, vp, vp, i64, i64, ctypes.POINTER(i64), i32,
+                                                   f32, vp, sz, vp, vp]),
         "xattn_select": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp]),
         "xattn_select_per_kv_head": (ctypes.c_int, [P, vp, f64, i32, i32, i32, vp, sz, vp, vp, vp,
                                                      vp, vp]),
@@ -227,6 +230,20 @@ def xattn_estimate_seq(problem, q, k_seq, k_seq_starts, scale, workspace, block_
                                            workspace.numel() * workspace.element_size(),
                                            _dev(block_sums, "block_sums", _F32), _stream(stream))
     _check(st, "xattn_estimate_seq")
+
+
+def xattn_estimate_sampled(problem, q, k_seq, k_seq_starts, samples, scale, workspace,
+                           block_sums, stream=None, head_stride=None, token_stride=0):
+    """xattn_estimate_seq scoring only the first `samples` reshaped columns of
+    each history block (each weighted Br/samples)."""
+    starts = np.ascontiguousarray(np.asarray(k_seq_starts, dtype=np.int64))
+    hs = k_seq.stride(0) if head_stride is None else int(head_stride)
+    st = load_library().xattn_estimate_sampled(
+        problem.ref(), _dev(q, "q", _BF16), _dev(k_seq, "k_seq", _BF16), hs, int(token_stride),
+        starts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(samples), float(scale),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(block_sums, "block_sums", _F32), _stream(stream))
+    _check(st, "xattn_estimate_sampled")
 
 
 def xattn_select(problem, block_sums, threshold, workspace, mask, sel_idx, sel_page, n_sel,
