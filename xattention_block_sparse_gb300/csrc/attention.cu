@@ -97,6 +97,8 @@ struct Bars {
   int64_t rg_beg[kMaxWaves + 1];   // the ranges: its units of each wave (whole),
   int64_t rg_end[kMaxWaves + 1];   //   then its stream-K range (the last one)
   int64_t p_waves;                 // kWaves: first item after the waves' units
+  int64_t sk_q;                    // total = sk_q * Gsk + sk_r: floor(c total / Gsk)
+  int32_t sk_r;                    //   without a 64-bit division
   int32_t csk;                     // stream-K CTA index, -1 if this CTA has no range
 };
 
@@ -175,20 +177,36 @@ __device__ __noinline__ int64_t unit_start(const Geo &g, const Bars &bar, int u)
 //   B_c = P(nw G) + floor(c T / G) - sum_w (P(w G + c) - P(w G)),
 // P(u) the first item of unit u (needs nw * the longest unit <= T / G, so
 // that no CTA's share is negative).
+__device__ __forceinline__ int64_t share_floor(const Bars &bar, int c, int G) {
+  return bar.sk_q * c + (bar.sk_r * c) / G;  // floor(c total / G); sk_r * c < G * (G + 1)
+}
+
 template <int NK>
-__device__ __noinline__ int64_t cta_begin(const Geo &g, const Bars &bar, int c, int G) {
-  if (bar.mode != kWaves) return bar.total * c / G;
+__device__ __noinline__ int64_t cta_begin_waves(const Geo &g, const Bars &bar, int c, int G) {
   if (c >= G) return bar.total;
-  int64_t b = bar.p_waves + bar.total * c / G;
+  int64_t b = bar.p_waves + share_floor(bar, c, G);
   for (int w = 0; w < bar.nw; ++w)
     b -= unit_start<NK>(g, bar, w * G + c) - unit_start<NK>(g, bar, w * G);
   return b;
+}
+
+template <int NK>
+__device__ __forceinline__ int64_t cta_begin(const Geo &g, const Bars &bar, int c, int G) {
+  return bar.mode != kWaves ? share_floor(bar, c, G) : cta_begin_waves<NK>(g, bar, c, G);
 }
 
 // The stream-K CTA whose range holds item `pos` (the last c with B_c <= pos;
 // ranges may be empty).
 template <int NK>
 __device__ __noinline__ int cta_of(const Geo &g, const Bars &bar, int G, int64_t pos) {
+  if (bar.mode != kWaves) {  // even split: the proportional guess (float, off by at
+    // most one), then exact integer steps
+    int c = (int)((float)pos * ((float)G / (float)bar.total));
+    c = c < 0 ? 0 : (c > G - 1 ? G - 1 : c);
+    while (c + 1 < G && share_floor(bar, c + 1, G) <= pos) ++c;
+    while (c > 0 && share_floor(bar, c, G) > pos) --c;
+    return c;
+  }
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) / 2;
@@ -230,6 +248,8 @@ __device__ __noinline__ void schedule(const Geo &g, Bars &bar, int Gsk, int wave
   }
   bar.mode = whole ? kWholeUnits : (nw > 0 ? kWaves : kStreamK);
   bar.nw = nw;
+  bar.sk_q = total / Gsk;
+  bar.sk_r = (int32_t)(total - bar.sk_q * Gsk);
   bar.nrg = 0;
   bar.csk = -1;
   if (bar.mode == kWholeUnits) {
@@ -328,13 +348,150 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
       *reinterpret_cast<uint4 *>(dst + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
   }
 }
-// 8 fp32 of another CTA's partial result, read at L2 (never a stale L1 line).
-__device__ __forceinline__ void load_part8(const float *src, float *v) {
-  asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
-                 "=f"(v[6]), "=f"(v[7])
-               : "l"(src)
-               : "memory");
+
+// Merge of a split unit's parts by the CTA whose part completed it: every
+// part, this CTA's included, read from global memory in CTA order (the same
+// arithmetic whichever CTA merges, so results are reproducible), weighted by
+// e^(lse_part - lse) into the final bf16 row and its LSE.  Out of line: cold
+// code, with registers of its own.
+template <int D, int NK>
+__device__ __noinline__ void merge_parts(const Geo &g, const Bars &bar, const Seg &sg, int x,
+                                         int row, int G, const float *__restrict__ part_o,
+                                         const float *__restrict__ part_lse,
+                                         __nv_bfloat16 *orow, float *lrow, bool o_v8) {
+  // Parts: the CTAs c0..c1 whose ranges meet the unit's items; the unit is
+  // c0's last segment (slot 1) unless it starts c0's range, and the first
+  // segment (slot 0) of every later CTA.
+  const int64_t uend = sg.ustart + sg.u.n_tiles;
+  const int c0 = cta_of<NK>(g, bar, G, sg.ustart), c1 = cta_of<NK>(g, bar, G, uend - 1);
+  auto part_row = [&](int c) -> int64_t {  // -1: CTA without items
+    const int64_t bc = cta_begin<NK>(g, bar, c, G);
+    if (bc == cta_begin<NK>(g, bar, c + 1, G)) return -1;
+    const int slot = (c == c0 && bc < sg.ustart) ? 1 : 0;
+    return ((int64_t)c * 2 + slot) * ROWS + x * BM + row;
+  };
+  // every part, this CTA's included, from global memory in CTA order: the
+  // same arithmetic whichever CTA merges, so results are reproducible
+  // (rows past the request, wr == false, are whole warps: lq is a multiple of 64)
+  // weights first, in CTA order
+  constexpr int MP = 6;  // parts whose weights are kept in registers
+  const bool few = c1 - c0 < MP;
+  int64_t pr[MP];
+  float lp[MP];
+#pragma unroll
+  for (int q = 0; q < MP; ++q) {
+    pr[q] = few && c0 + q <= c1 ? part_row(c0 + q) : -1;
+    lp[q] = pr[q] >= 0 ? __ldcg(part_lse + pr[q]) : -INFINITY;
+  }
+  float M = -INFINITY;
+  if (few) {
+#pragma unroll
+    for (int q = 0; q < MP; ++q) M = fmaxf(M, lp[q]);
+  } else {
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t r_ = part_row(c);
+      if (r_ >= 0) M = fmaxf(M, __ldcg(part_lse + r_));
+    }
+  }
+  float den = 0.f;
+  if (few) {
+#pragma unroll
+    for (int q = 0; q < MP; ++q) den += lp[q] != -INFINITY ? __expf(lp[q] - M) : 0.f;
+  } else {
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t r_ = part_row(c);
+      const float l_ = r_ >= 0 ? __ldcg(part_lse + r_) : -INFINITY;
+      den += l_ != -INFINITY ? __expf(l_ - M) : 0.f;
+    }
+  }
+  const float rden = den > 0.f ? 1.f / den : 0.f;
+  // the parts that hold keys of this row (a part without any wrote no O)
+  int nv = 0;
+  int64_t ra = 0, rb = 0;
+  float wa = 0.f, wb = 0.f;
+#pragma unroll
+  for (int q = 0; q < MP; ++q) {
+    if (lp[q] != -INFINITY) {
+      const float wq = __expf(lp[q] - M) * rden;
+      if (nv == 0) {
+        ra = pr[q];
+        wa = wq;
+      } else if (nv == 1) {
+        rb = pr[q];
+        wb = wq;
+      }
+      ++nv;
+    }
+  }
+  if (__all_sync(0xffffffffu, few && nv <= 2)) {
+    // one or two parts (the usual split).  The warp merges its 32 rows one at a
+    // time with its lanes across the columns (lane l: columns 4l..4l+3), so a
+    // part row is one coalesced 512-byte read; eight rows are in flight at
+    // once.  Row r's parts and weights come from lane r.
+    const int lane = threadIdx.x & 31;
+    for (int r0 = 0; r0 < 32; r0 += 8) {
+      float4 va[8], vb[8];
+      float wa_r[8], wb_r[8];
+      int nv_r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int r = r0 + u;
+        nv_r[u] = __shfl_sync(0xffffffffu, nv, r);
+        wa_r[u] = __shfl_sync(0xffffffffu, wa, r);
+        wb_r[u] = __shfl_sync(0xffffffffu, wb, r);
+        const int64_t ra_r = __shfl_sync(0xffffffffu, ra, r);
+        const int64_t rb_r = __shfl_sync(0xffffffffu, rb, r);
+        va[u] = nv_r[u] > 0 ? __ldcg(reinterpret_cast<const float4 *>(part_o + ra_r * D) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        vb[u] = nv_r[u] > 1 ? __ldcg(reinterpret_cast<const float4 *>(part_o + rb_r * D) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float4 acc;
+        acc.x = fmaf(wa_r[u], va[u].x, 0.f);
+        acc.y = fmaf(wa_r[u], va[u].y, 0.f);
+        acc.z = fmaf(wa_r[u], va[u].z, 0.f);
+        acc.w = fmaf(wa_r[u], va[u].w, 0.f);
+        if (nv_r[u] > 1) {
+          acc.x = fmaf(wb_r[u], vb[u].x, acc.x);
+          acc.y = fmaf(wb_r[u], vb[u].y, acc.y);
+          acc.z = fmaf(wb_r[u], vb[u].z, acc.z);
+          acc.w = fmaf(wb_r[u], vb[u].w, acc.w);
+        }
+        __nv_bfloat16 *dst = orow + (int64_t)(r0 + u - lane) * D + 4 * lane;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y),
+                                                     pack_bf16x2(acc.z, acc.w));
+      }
+    }
+  } else {
+    // more parts: the same arithmetic, one part at a time
+    for (int cb = 0; cb < D / 32; ++cb) {
+      float acc[32];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t r_ = part_row(c);
+        if (r_ < 0) continue;
+        const float l_ = __ldcg(part_lse + r_);
+        if (l_ == -INFINITY) continue;
+        const float w_ = __expf(l_ - M) * rden;
+        const float4 *src = reinterpret_cast<const float4 *>(part_o + r_ * D) + cb * 8;
+        float4 v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __ldcg(src + e);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[4 * e + 0] = fmaf(w_, v[e].x, acc[4 * e + 0]);
+          acc[4 * e + 1] = fmaf(w_, v[e].y, acc[4 * e + 1]);
+          acc[4 * e + 2] = fmaf(w_, v[e].z, acc[4 * e + 2]);
+          acc[4 * e + 3] = fmaf(w_, v[e].w, acc[4 * e + 3]);
+        }
+      }
+      store_bf16x32(orow + cb * 32, acc, o_v8);
+    }
+  }
+  *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
 }
 
 template <int D, int NK>
@@ -782,113 +939,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           *lrow = lse_v;
       }
       if (!sg.partial) continue;
-      // ---- split unit: count this part in; the last part merges them all.
-      // Parts: the CTAs c0..c1 whose ranges meet the unit's items; the unit is
-      // c0's last segment (slot 1) unless it starts c0's range, and the first
-      // segment (slot 0) of every later CTA.
-      const int64_t uend = sg.ustart + sg.u.n_tiles;
-      const int c0 = cta_of<NK>(g, bar, G, sg.ustart), c1 = cta_of<NK>(g, bar, G, uend - 1);
+      // ---- split unit: count this part's items in; the part that completes
+      // the unit's count merges them all.
       __threadfence();  // this thread's part is visible GPU-wide
       if (!group_sync()) break;
       if (row == 0) {
-        int nparts = 0;
-        for (int c = c0; c <= c1; ++c)
-          nparts += cta_begin<NK>(g, bar, c, G) < cta_begin<NK>(g, bar, c + 1, G);
+        const int mine = sg.t1 - sg.t0;
         __threadfence();
-        const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, 1);
+        const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, mine);
         __threadfence();
-        bar.last[x] = before == nparts - 1;
+        bar.last[x] = before + mine == sg.u.n_tiles;
       }
       if (!group_sync()) break;
       if (!*reinterpret_cast<volatile int *>(&bar.last[x])) continue;  // uniform in the group
       __threadfence();
-      auto part_row = [&](int c) -> int64_t {  // -1: CTA without items
-        const int64_t bc = cta_begin<NK>(g, bar, c, G);
-        if (bc == cta_begin<NK>(g, bar, c + 1, G)) return -1;
-        const int slot = (c == c0 && bc < sg.ustart) ? 1 : 0;
-        return ((int64_t)c * 2 + slot) * ROWS + x * BM + row;
-      };
-      // every part, this CTA's included, from global memory in CTA order: the
-      // same arithmetic whichever CTA merges, so results are reproducible
-      // (rows past the request, wr == false, are whole warps: lq is a multiple of 64)
-      constexpr int MP = 6;  // parts merged with all their loads in flight
-      if (wr && c1 - c0 < MP) {
-        // weights first (in CTA order), then per 8 columns the loads of every part
-        int64_t pr[MP];
-        float lp[MP];
-#pragma unroll
-        for (int q = 0; q < MP; ++q) {
-          pr[q] = c0 + q <= c1 ? part_row(c0 + q) : -1;
-          lp[q] = pr[q] >= 0 ? __ldcg(part_lse + pr[q]) : -INFINITY;
-        }
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < MP; ++q) M = fmaxf(M, lp[q]);
-        float den = 0.f, w[MP];
-#pragma unroll
-        for (int q = 0; q < MP; ++q) den += lp[q] != -INFINITY ? __expf(lp[q] - M) : 0.f;
-        const float rden = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-        for (int q = 0; q < MP; ++q) w[q] = lp[q] != -INFINITY ? __expf(lp[q] - M) * rden : 0.f;
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float acc[32];
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            float v[MP][8];
-#pragma unroll
-            for (int q = 0; q < MP; ++q) {
-              if (lp[q] != -INFINITY) {  // a part without keys of this row wrote no O
-                load_part8(part_o + pr[q] * D + cb * 32 + q8 * 8, v[q]);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[q][e] = 0.f;
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float a8 = 0.f;
-#pragma unroll
-              for (int q = 0; q < MP; ++q) a8 = fmaf(w[q], v[q][e], a8);
-              acc[q8 * 8 + e] = a8;
-            }
-          }
-          store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
-        }
-        *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
-      } else if (wr) {
-        // more parts: the same arithmetic, one part at a time
-        float M = -INFINITY;
-        for (int c = c0; c <= c1; ++c) {
-          const int64_t pr = part_row(c);
-          if (pr >= 0) M = fmaxf(M, __ldcg(part_lse + pr));
-        }
-        float den = 0.f;
-        for (int c = c0; c <= c1; ++c) {
-          const int64_t pr = part_row(c);
-          const float lp = pr >= 0 ? __ldcg(part_lse + pr) : -INFINITY;
-          den += lp != -INFINITY ? __expf(lp - M) : 0.f;
-        }
-        const float rden = den > 0.f ? 1.f / den : 0.f;
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float acc[32];
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
-          for (int c = c0; c <= c1; ++c) {
-            const int64_t pr = part_row(c);
-            if (pr < 0) continue;
-            const float lp = __ldcg(part_lse + pr);
-            if (lp == -INFINITY) continue;
-            const float w = __expf(lp - M) * rden;
-            float v[32];
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) load_part8(part_o + pr * D + cb * 32 + q8 * 8, v + q8 * 8);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc[jj] = fmaf(w, v[jj], acc[jj]);
-          }
-          store_bf16x32(orow + cb * 32, acc, o_v8 != 0);
-        }
-        *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
-      }
+      if (wr)
+        merge_parts<D, NK>(g, bar, sg, x, row, G, part_o, part_lse, orow, lrow, o_v8 != 0);
     }
   }
 
