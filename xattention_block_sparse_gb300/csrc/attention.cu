@@ -494,6 +494,223 @@ __device__ __noinline__ void merge_parts(const Geo &g, const Bars &bar, const Se
   *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
 }
 
+// The first stream-K CTA of a split unit's parts; row 0 of the query tile
+// also sets bar.last[x] when the unit has exactly two parts and the other
+// one is already counted in (this part then completes it).
+template <int NK>
+__device__ __noinline__ int direct_check(const Geo &g, Bars &bar, const Seg &sg, int x, int row,
+                                         int G, int32_t *unit_cnt) {
+  const int64_t uend = sg.ustart + sg.u.n_tiles;
+  const int c0 = cta_of<NK>(g, bar, G, sg.ustart), c1 = cta_of<NK>(g, bar, G, uend - 1);
+  if (row == 0) {
+    int d = 0;
+    if (c1 - c0 == 1) {
+      int cntv;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                   : "=r"(cntv)
+                   : "l"(unit_cnt + 2 * sg.uid + x)
+                   : "memory");
+      d = cntv + (sg.t1 - sg.t0) == sg.u.n_tiles;
+    }
+    bar.last[x] = d;
+  }
+  return c0;
+}
+
+// Merge of a split unit by its part that ends this CTA's work, when the one
+// other part (another CTA's) is already counted in: this part's rows come
+// straight from the O accumulator in TMEM (normalised) instead of a round
+// trip through the partial-result slots.  The rows go through this query
+// tile's Q buffer in shared memory (free: the CTA loads no further Q), 64
+// columns at a time, so that each warp then merges its 32 rows with its lanes
+// across the columns (coalesced reads of the other part, as in merge_parts).
+// The arithmetic is that of merge_parts: weights e^(lse_part - M) / den in
+// CTA order, fmaf(w0, v0, 0) then fmaf(w1, v1, .) over the parts holding keys.
+template <int D, int NK>
+__device__ __noinline__ void merge_direct(const Bars &bar, const Geo &g, const Seg &sg, int x,
+                                          int row, int G, uint32_t o_taddr, bool has_o,
+                                          float inv, float lse_own, int64_t own_c, int c0,
+                                          const float *__restrict__ part_o,
+                                          const float *__restrict__ part_lse,
+                                          uint8_t *stage, __nv_bfloat16 *orow, float *lrow) {
+  const int lane = threadIdx.x & 31;
+  const int oc = own_c == c0 ? c0 + 1 : c0;  // the other part's CTA
+  const int64_t boc = cta_begin<NK>(g, bar, oc, G);
+  const int slot = (oc == c0 && boc < sg.ustart) ? 1 : 0;
+  const int64_t orw = ((int64_t)oc * 2 + slot) * ROWS + x * BM + row;  // its row, this thread
+  const float lse_oth = __ldcg(part_lse + orw);
+  // parts in CTA order
+  const bool own_first = own_c == c0;
+  const float l0 = own_first ? lse_own : lse_oth, l1 = own_first ? lse_oth : lse_own;
+  const float M = fmaxf(fmaxf(-INFINITY, l0), l1);
+  float den = 0.f;
+  den += l0 != -INFINITY ? __expf(l0 - M) : 0.f;
+  den += l1 != -INFINITY ? __expf(l1 - M) : 0.f;
+  const float rden = den > 0.f ? 1.f / den : 0.f;
+  const float w0 = l0 != -INFINITY ? __expf(l0 - M) * rden : 0.f;
+  const float w1 = l1 != -INFINITY ? __expf(l1 - M) * rden : 0.f;
+  // per row: which of (part 0, part 1) hold keys; the own one is read from stage
+  const int flags = (l0 != -INFINITY ? 1 : 0) | (l1 != -INFINITY ? 2 : 0);
+  float4 *st4 = reinterpret_cast<float4 *>(stage);  // [BM rows][16 chunks of 4 fp32]
+  const int wrow0 = row - lane;                     // first row of this warp
+#pragma unroll 1
+  for (int pass = 0; pass < D / 64; ++pass) {
+    // this thread's row, 64 columns, normalised, chunk j at (j ^ (row & 15))
+    if (has_o) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t ov[32];
+        tmem_ld32(o_taddr + pass * 64 + h * 32, ov);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int j = h * 8 + q;
+          st4[row * 16 + (j ^ (row & 15))] =
+              make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
+                          __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+        }
+      }
+    }
+    __syncwarp();
+    // the warp's 32 rows, two per step (16 lanes a row), the other part's loads first
+    const int j = lane & 15;
+    float4 vo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rl = 2 * i + (lane >> 4);  // row within the warp
+      const int64_t orw_r = __shfl_sync(0xffffffffu, orw, rl);
+      const int fl = __shfl_sync(0xffffffffu, flags, rl);
+      const bool oth_ok = own_first ? (fl & 2) : (fl & 1);
+      vo[i] = oth_ok ? __ldcg(reinterpret_cast<const float4 *>(part_o + orw_r * D + pass * 64) + j)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rl = 2 * i + (lane >> 4);
+      const int r = wrow0 + rl;  // row within the query tile
+      const int fl = __shfl_sync(0xffffffffu, flags, rl);
+      const float a0 = __shfl_sync(0xffffffffu, w0, rl), a1 = __shfl_sync(0xffffffffu, w1, rl);
+      const float4 vs = (own_first ? (fl & 1) : (fl & 2)) ? st4[r * 16 + (j ^ (r & 15))]
+                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 v0 = own_first ? vs : vo[i], v1 = own_first ? vo[i] : vs;
+      float4 acc;
+      // the first part holding keys starts the sum (as merge_parts)
+      const bool h0 = fl & 1, h1 = (fl & 2) != 0;
+      const float4 f = h0 ? v0 : v1;
+      const float wf = h0 ? a0 : a1;
+      acc.x = fmaf(wf, f.x, 0.f);
+      acc.y = fmaf(wf, f.y, 0.f);
+      acc.z = fmaf(wf, f.z, 0.f);
+      acc.w = fmaf(wf, f.w, 0.f);
+      if (h0 && h1) {
+        acc.x = fmaf(a1, v1.x, acc.x);
+        acc.y = fmaf(a1, v1.y, acc.y);
+        acc.z = fmaf(a1, v1.z, acc.z);
+        acc.w = fmaf(a1, v1.w, acc.w);
+      }
+      __nv_bfloat16 *dst = orow + (int64_t)(rl - lane) * D + pass * 64 + 4 * j;
+      *reinterpret_cast<uint2 *>(dst) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+    __syncwarp();  // the stage rows are rewritten by the next pass
+  }
+  *lrow = den > 0.f ? M + __logf(den) : -INFINITY;
+}
+
+// End of a segment for query tile x (its softmax warpgroup): O normalised and
+// written -- final (bf16) when the segment is the whole unit, else a partial
+// result (fp32 O, LSE) in this CTA's slot, counted in, and merged by the part
+// that completes the unit.  Out of line, so that the tile loop's registers
+// are its own.  False when a bounded wait gave up.
+template <int D, int NK>
+__device__ __noinline__ bool segment_end(const Geo &g, Bars &bar, const Seg &sg, int x, int row,
+                                         int G, int csk, int nx, int cnt, float m_run,
+                                         float l_run, bool last_seg, uint32_t lane_addr,
+                                         uint32_t o_col, uint8_t *smem,
+                                         __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
+                                         int o_v8, float *__restrict__ part_o,
+                                         float *__restrict__ part_lse,
+                                         int32_t *__restrict__ unit_cnt, int &gb) {
+  using LY = Layout<D, NK>;
+  volatile int *abort = &bar.abort;
+  const int lane = threadIdx.x & 31;
+  const ReqDesc &R = g.req[sg.r];
+  const int qrow = sg.m0 + x * BM + row;  // chunk-local query index
+  // warpgroup barrier on an mbarrier: bounded, so a peer that gave up on a
+  // timeout cannot leave the others waiting forever
+  auto group_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.grp[x]);
+    return mbar_wait(&bar.grp[x], gb++ & 1, abort, g.err);
+  };
+  const bool wr = qrow < R.lq;
+  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+  const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+  const int64_t prow = ((int64_t)csk * 2 + sg.slot) * ROWS + x * BM + row;
+  __nv_bfloat16 *orow = o + (int64_t)sg.hq * g.q_hs + (int64_t)(R.q0 + qrow) * D;
+  float *lrow = lse + (int64_t)sg.hq * g.lse_hs + R.q0 + qrow;
+  if (sg.partial && last_seg) {
+    // the unit's other part, when it is a single CTA's and already counted
+    // in, is merged right here (merge_direct)
+    const int c0 = direct_check<NK>(g, bar, sg, x, row, G, unit_cnt);
+    if (nx > 0) {
+      if (!mbar_wait(&bar.pv_done[x], (cnt - 1) & 1, abort, g.err)) return false;
+      tc_fence_after();
+    }
+    if (!group_sync()) return false;
+    if (*reinterpret_cast<volatile int *>(&bar.last[x])) {  // uniform in the group
+      __threadfence();
+      if (wr)
+        merge_direct<D, NK>(bar, g, sg, x, row, G, lane_addr + o_col, nx > 0, inv, lse_v, csk,
+                            c0, part_o, part_lse, smem + LY::OFF_Q + x * LY::Q_BYTES, orow,
+                            lrow);
+      return true;
+    }
+  }
+  if (nx > 0) {
+    if (!mbar_wait(&bar.pv_done[x], (cnt - 1) & 1, abort, g.err)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      tmem_ld32(lane_addr + o_col + c * 32, ov);
+      tmem_ld_wait();
+      if (!wr) continue;
+      float v[32];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(ov[jj]) * inv;
+      if (sg.partial)
+        store_f32x32(part_o + prow * D + c * 32, v);
+      else
+        store_bf16x32(orow + c * 32, v, o_v8 != 0);
+    }
+  }
+  if (wr) {
+    if (sg.partial)
+      part_lse[prow] = lse_v;  // -inf marks an empty part (no tile of this query tile)
+    else
+      *lrow = lse_v;
+  }
+  if (!sg.partial) return true;
+  // ---- split unit: count this part's items in; the part that completes
+  // the unit's count merges them all.
+  __threadfence();  // this thread's part is visible GPU-wide
+  if (!group_sync()) return false;
+  if (row == 0) {
+    const int mine = sg.t1 - sg.t0;
+    __threadfence();
+    const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, mine);
+    __threadfence();
+    bar.last[x] = before + mine == sg.u.n_tiles;
+  }
+  if (!group_sync()) return false;
+  if (!*reinterpret_cast<volatile int *>(&bar.last[x])) return true;  // uniform in the group
+  __threadfence();
+  if (wr)
+    merge_parts<D, NK>(g, bar, sg, x, row, G, part_o, part_lse, orow, lrow, o_v8 != 0);
+  return true;
+}
+
 template <int D, int NK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ Geo g, const __grid_constant__ TMaps tm,
@@ -800,6 +1017,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         do ++rg; while (rg < nrg && bar.rg_beg[rg] >= bar.rg_end[rg]);
         if (rg < nrg) pos = bar.rg_beg[rg];
       }
+      const bool last_seg = rg >= nrg;  // no segment of this CTA follows
       const ReqDesc &R = g.req[sg.r];
       const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
       const int nx = max(0, min(n_x, sg.t1) - sg.t0);
@@ -904,57 +1122,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       cnt += nx;
-      // segment epilogue: O normalised and written -- final (bf16) when the
-      // segment is the whole unit, else a partial result (fp32 O, LSE) in this
-      // CTA's slot.  Tile x exists (rows below lq) iff x == 0 or has_b.
+      // segment end: O written (or merged); tile x exists (rows below lq)
+      // iff x == 0 or has_b
       if (x == 1 && !sg.u.has_b) continue;
-      const bool wr = qrow < R.lq;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-      const int64_t prow = ((int64_t)csk * 2 + sg.slot) * ROWS + x * BM + row;
-      __nv_bfloat16 *orow = o + (int64_t)sg.hq * g.q_hs + (int64_t)(R.q0 + qrow) * D;
-      float *lrow = lse + (int64_t)sg.hq * g.lse_hs + R.q0 + qrow;
-      if (nx > 0) {
-        if (!mbar_wait(&bar.pv_done[x], (cnt - 1) & 1, abort, g.err)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_addr + o_col + c * 32, ov);
-          tmem_ld_wait();
-          if (!wr) continue;
-          float v[32];
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(ov[jj]) * inv;
-          if (sg.partial)
-            store_f32x32(part_o + prow * D + c * 32, v);
-          else
-            store_bf16x32(orow + c * 32, v, o_v8 != 0);
-        }
-      }
-      if (wr) {
-        if (sg.partial)
-          part_lse[prow] = lse_v;  // -inf marks an empty part (no tile of this query tile)
-        else
-          *lrow = lse_v;
-      }
-      if (!sg.partial) continue;
-      // ---- split unit: count this part's items in; the part that completes
-      // the unit's count merges them all.
-      __threadfence();  // this thread's part is visible GPU-wide
-      if (!group_sync()) break;
-      if (row == 0) {
-        const int mine = sg.t1 - sg.t0;
-        __threadfence();
-        const int before = atomicAdd(unit_cnt + 2 * sg.uid + x, mine);
-        __threadfence();
-        bar.last[x] = before + mine == sg.u.n_tiles;
-      }
-      if (!group_sync()) break;
-      if (!*reinterpret_cast<volatile int *>(&bar.last[x])) continue;  // uniform in the group
-      __threadfence();
-      if (wr)
-        merge_parts<D, NK>(g, bar, sg, x, row, G, part_o, part_lse, orow, lrow, o_v8 != 0);
+      if (!segment_end<D, NK>(g, bar, sg, x, row, G, csk, nx, cnt, m_run, l_run, last_seg,
+                              lane_addr, o_col, smem, o, lse, o_v8, part_o, part_lse, unit_cnt,
+                              gb))
+        break;
     }
   }
 
