@@ -225,7 +225,9 @@ __device__ __noinline__ int cta_of(const Geo &g, const Bars &bar, int G, int64_t
 //    out CTAs as SMs free up -- no unit is split, no merge; used when the
 //    launch is small (under kWholeUnitsTiles items per SM) and no unit
 //    dwarfs a fair share, where stream-K's segment changes and merges cost
-//    more than the imbalance they remove;
+//    more than the imbalance they remove (at the 32K workload's chunks of 83
+//    and 136 items per SM, one CTA per unit measured 188 against 202 us and
+//    300 against 290 us);
 //  * waves (when the caller allows it: keys and values larger than L2): the
 //    stream-K CTAs first run nw waves of whole units -- CTA c units c, c + G,
 //    ... -- then stream-K ranges of the remaining units sized so that all
@@ -234,7 +236,7 @@ __device__ __noinline__ int cta_of(const Geo &g, const Bars &bar, int G, int64_t
 //    each page comes from DRAM once and from L2 to the other CTAs reading it,
 //    where stream-K CTAs at unrelated positions would each fetch their own;
 //  * stream-K: the last Gsk CTAs of the grid split the items evenly.
-constexpr int kWholeUnitsTiles = 160;
+constexpr int kWholeUnitsTiles = 110;
 template <int NK>
 __device__ __noinline__ void schedule(const Geo &g, Bars &bar, int Gsk, int waves_ok) {
   const int64_t total = bar.total;
