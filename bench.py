@@ -209,16 +209,16 @@ class Timed:
         self.stream = torch.cuda.Stream(device=dev)
         self.flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
 
-    def step(self, ev=None):
+    def stages(self, c):
+        """The three calls of chunk c: estimate, select, attention."""
         X, RN, cfg, b = self.X, self.RN, self.cfg, self.seq.bufs
         Q, K, V, KP, VP, st = self.Q, self.K, self.V, self.KP, self.VP, self.stream
         scale = RN.estimation_scale(cfg.D, cfg.stride)
         select = X.xattn_select_per_kv_head if self.per_kv else X.xattn_select
         attend = X.bsa_chunk_attention_per_kv_head if self.per_kv else X.bsa_chunk_attention
-        for c in range(self.nchunk):
-            p, t0 = self.seq.problems[c], c * self.chunk
-            if ev is not None:
-                ev[c][0].record(st)
+        p, t0 = self.seq.problems[c], c * self.chunk
+
+        def est():
             if self.est_from_pages:
                 X.xattn_estimate(p, Q[:, t0:], K[:, t0:], KP, scale, b.workspace, b.block_sums,
                                  st)
@@ -227,16 +227,60 @@ class Timed:
                                          b.block_sums, st)
             else:  # keys in token order: K [Hkv, L, D] holds the history and the chunk
                 X.xattn_estimate_seq(p, Q[:, t0:], K, [0], scale, b.workspace, b.block_sums, st)
-            if ev is not None:
-                ev[c][1].record(st)
+
+        def sel():
             select(p, b.block_sums, self.tau, b.workspace, None, b.sel_idx, b.sel_page, b.n_sel,
                    st)
-            if ev is not None:
-                ev[c][2].record(st)
+
+        def att():
             attend(p, Q[:, t0:], K[:, t0:], V[:, t0:], KP, VP, b.sel_page, b.n_sel,
                    1.0 / math.sqrt(cfg.D), b.workspace, self.O[:, t0:], self.LSE[:, t0:], st)
+
+        return est, sel, att
+
+    def step(self, ev=None):
+        st = self.stream
+        for c in range(self.nchunk):
             if ev is not None:
-                ev[c][3].record(st)
+                ev[c][0].record(st)
+            for i, fn in enumerate(self.stages(c)):
+                fn()
+                if ev is not None:
+                    ev[c][i + 1].record(st)
+
+    def stage_times(self, reps=5, rounds=3):
+        """Milliseconds per step of each stage: for every chunk, the chunk's
+        estimate and selection run once (so the buffers hold its selection),
+        then each stage alone is timed as a CUDA graph of `reps` back-to-back
+        calls (median of `rounds` replays), the way the step itself is timed:
+        no host gaps between launches."""
+        torch = self.torch
+        tot = [0.0, 0.0, 0.0]
+        st = self.stream
+        for c in range(self.nchunk):
+            fns = self.stages(c)
+            with torch.cuda.stream(st):
+                fns[0]()
+                fns[1]()
+            for i, fn in enumerate(fns):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=st, capture_error_mode="relaxed"):
+                    for _ in range(reps):
+                        fn()
+                ts = []
+                for _ in range(rounds):
+                    with torch.cuda.stream(st):
+                        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                                  torch.cuda.Event(enable_timing=True))
+                        e0.record(st)
+                        g.replay()
+                        e1.record(st)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) / reps)
+                tot[i] += float(np.median(ts))
+                del g
+        return {"estimate_ms_per_step": tot[0], "select_ms_per_step": tot[1],
+                "attention_ms_per_step": tot[2]}
 
     def selections(self):
         """History blocks attended per chunk (summed over KV heads and divided by
@@ -251,10 +295,11 @@ class Timed:
         return n_sel
 
     def run(self, steps, warmup, sample_clocks=None, graph=True):
-        """Per-stage times from eager calls (events around each call), then the
-        timed steps: one replay per step of a CUDA graph of the whole step, so
-        that the GPU never waits for the host between launches (eager launches
-        of short kernels can outrun the host)."""
+        """Eager steps (events around each step), then the timed steps: one
+        replay per step of a CUDA graph of the whole step, so that the GPU never
+        waits for the host between launches (eager launches of short kernels
+        can outrun the host); then the stage times (stage_times, or the eager
+        calls' events when no graph could be captured)."""
         torch = self.torch
         self.n_sel = self.selections()
         for _ in range(warmup):
@@ -270,18 +315,12 @@ class Timed:
                 self.flush.zero_()  # L2 flush between steps (outside the step events)
                 self.step(events[s])
         torch.cuda.synchronize()
-        est = sel = att = 0.0
-        eager_ms = []
-        for s in range(steps):
-            for c in range(self.nchunk):
-                e = events[s][c]
-                est += e[0].elapsed_time(e[1])
-                sel += e[1].elapsed_time(e[2])
-                att += e[2].elapsed_time(e[3])
-            eager_ms.append(events[s][0][0].elapsed_time(events[s][self.nchunk - 1][3]))
-        self.stage = {"estimate_ms_per_step": est / steps, "select_ms_per_step": sel / steps,
-                      "attention_ms_per_step": att / steps}
+        eager_ms = [events[s][0][0].elapsed_time(events[s][self.nchunk - 1][3])
+                    for s in range(steps)]
         self.eager_ms = float(np.mean(eager_ms))
+        eager_stage = [sum(events[s][c][i].elapsed_time(events[s][c][i + 1])
+                           for s in range(steps) for c in range(self.nchunk)) / steps
+                       for i in range(3)]
         self.graph, self.timing = None, "eager launches, events around each step"
         if graph:
             try:
@@ -312,6 +351,14 @@ class Timed:
         self.clocks = clk.stop() if clk else None
         assert self.X.xattn_device_error() == 0
         self.step_ms = [a.elapsed_time(b) for a, b in se]
+        if self.graph is not None:
+            self.stage = self.stage_times()
+            self.stage_timing = "per chunk, each stage alone as a CUDA graph of 5 calls"
+        else:
+            self.stage = {"estimate_ms_per_step": eager_stage[0],
+                          "select_ms_per_step": eager_stage[1],
+                          "attention_ms_per_step": eager_stage[2]}
+            self.stage_timing = "eager calls, CUDA events around each call"
         self.steps = steps
         return self
 
@@ -431,7 +478,7 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": workload_desc(args.workload, tau), "tokens_per_step": L,
                    "chunks": nchunk, "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{ws}", "timing": T.timing,
-                   "stage_times": "eager calls, CUDA events around each call"},
+                   "stage_times": T.stage_timing},
         "ms_per_step_eager": T.eager_ms,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel (bsa_chunk_attention)",
                      "achieved": att_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
