@@ -220,8 +220,10 @@ __device__ __noinline__ int cta_of(const Geo &g, const Bars &bar, int G, int64_t
 
 // The work of CTA blockIdx.x.  Three schedules, chosen from the tables alone
 // (every CTA takes the same decision):
-//  * whole units: CTA c takes unit c of the units ordered by decreasing row
-//    tile (the larger units first within a request), the hardware handing
+//  * whole units: CTA c takes unit c of the units ordered by their distance
+//    from their request's last row tile (the larger units first, across
+//    requests: one request per KV head when each KV head has its own
+//    selection), then by request and head, the hardware handing
 //    out CTAs as SMs free up -- no unit is split, no merge; used when the
 //    launch is small (under kWholeUnitsTiles items per SM) and no unit
 //    dwarfs a fair share, where stream-K's segment changes and merges cost
@@ -255,13 +257,26 @@ __device__ __noinline__ void schedule(const Geo &g, Bars &bar, int Gsk, int wave
   bar.nrg = 0;
   bar.csk = -1;
   if (bar.mode == kWholeUnits) {
-    int r = 0;
-    while (r + 1 < g.B && c >= bar.req_unit0[r + 1]) ++r;
+    // rank c: units by their distance d from their request's last row tile
+    // (the larger units first, across requests), then request, then head
+    if (c >= bar.nunits) return;  // past the last unit
+    int l = c, d = 0, r = -1;
+    while (r < 0) {
+      int level = 0;
+      for (int q = 0; q < g.B; ++q) level += (g.req[q].lq + ROWS - 1) / ROWS > d ? g.H : 0;
+      if (l < level) {
+        for (int q = 0; r < 0; ++q) {
+          if ((g.req[q].lq + ROWS - 1) / ROWS <= d) continue;
+          if (l < g.H) r = q; else l -= g.H;
+        }
+      } else {
+        l -= level;
+        ++d;
+      }
+    }
     const ReqDesc &R = g.req[r];
     const int nmt = (R.lq + ROWS - 1) / ROWS;
-    const int l = c - bar.req_unit0[r];
-    if (R.lq == 0 || l >= nmt * g.H) return;  // past the last unit
-    const int mt = nmt - 1 - l / g.H, h = l % g.H;
+    const int mt = nmt - 1 - d, h = l;
     int64_t pos = bar.req_pos0[r] + (int64_t)h * bar.req_per_head[r];
     for (int m = 0; m < mt; ++m) pos += unit_geom<NK>(R, bar.req_hist[r], m).n_tiles;
     bar.rg_beg[0] = pos;
@@ -752,7 +767,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  const int64_t total = bar.total;
   const int csk = bar.csk;  // partial results only arise under stream-K
   const int nrg = bar.nrg;  // ranges: whole units, then (last) the stream-K range
   int rg0 = 0;              // the first range that holds work
@@ -1020,7 +1034,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (rg < nrg) pos = bar.rg_beg[rg];
       }
       const bool last_seg = rg >= nrg;  // no segment of this CTA follows
-      const ReqDesc &R = g.req[sg.r];
       const int n_x = x ? (sg.u.has_b ? sg.u.n_b : 0) : sg.u.n_a;
       const int nx = max(0, min(n_x, sg.t1) - sg.t0);
       const int qrow = sg.m0 + x * BM + row;  // chunk-local query index
