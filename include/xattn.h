@@ -132,7 +132,11 @@ typedef struct xattn_problem {
  * holds the estimation's per-(reshaped row, KV block) partial sums and
  * per-tile softmax statistics, the selection's vote counters (and the counter
  * that tells its last CTA to run the vote) and the attention's partial
- * results; its contents between calls are unspecified. */
+ * results; its contents between calls are unspecified.  The estimation and
+ * selection use the start of the buffer they are given, the attention the end
+ * of it: with one buffer for a whole chunked prefill, a chunk's estimate does
+ * not touch what the previous chunk's attention is still using (see
+ * xattn_estimate, Ordering). */
 size_t xattn_workspace_size(const xattn_problem *p);
 
 /* Number of fp32 elements of block_sums (and bytes of the optional mask):
@@ -157,7 +161,17 @@ size_t xattn_block_sums_offset(const xattn_problem *p, int32_t r);
  *   k_pool  DEVICE bf16 paged history keys
  *   scale   logit scale; the usual choice is 1 / (sqrt(D) * S)
  *   workspace, workspace_bytes   DEVICE scratch >= xattn_workspace_size(p)
- *   block_sums  DEVICE fp32 [xattn_block_sums_count(p)], written fully. */
+ *   block_sums  DEVICE fp32 [xattn_block_sums_count(p)], written fully.
+ * Ordering: when the call right before this one on `stream` is this
+ * library's bsa_chunk_attention (a previous chunk's), and the workspace this
+ * estimate writes does not overlap the part of its workspace that attention
+ * uses (the library checks the two ranges), the estimate may start on SMs
+ * that attention has released while its last CTAs still run (programmatic
+ * dependent launch).  It finishes only after that attention has, so
+ * everything enqueued after it sees both complete.  Its inputs must not be
+ * that attention's outputs: do not pass its o or lse as q or keys here.
+ * After any other kernel or stream operation the estimate starts as usual.
+ * The same holds for xattn_estimate_seq and xattn_estimate_sampled. */
 xattn_status xattn_estimate(const xattn_problem *p, const void *q, const void *k_cur,
                             const void *k_pool, float scale, void *workspace,
                             size_t workspace_bytes, float *block_sums,
@@ -295,7 +309,10 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
  *                  on which CTA that is (the parts are merged in a fixed order):
  *                  repeated calls give identical bits.
  *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
- *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE */
+ *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE
+ * A following xattn_estimate* call on the same stream may start before this
+ * call has finished (see xattn_estimate, Ordering); every other operation
+ * enqueued after it starts when it has finished. */
 xattn_status bsa_chunk_attention(const xattn_problem *p, const void *q, const void *k_cur,
                                  const void *v_cur, const void *k_pool, const void *v_pool,
                                  const int32_t *sel_page, const int32_t *n_sel,

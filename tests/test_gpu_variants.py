@@ -390,3 +390,55 @@ def test_chunk_captured_in_a_cuda_graph_replays_the_same_bits():
         for a, b in zip(want, outputs()):
             assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                                b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+def test_estimate_started_during_the_previous_attention_gives_the_same_bits():
+    """A chunk's estimate may start while the previous chunk's attention is
+    still finishing (it is launched as a programmatic dependent and waits for
+    the attention only at its end).  The 32K-shaped sparse sequence (8K, two
+    chunks; whole-unit and stream-K attention) and the 4K one run once with the
+    host synchronising after every chunk -- no overlap possible -- and once
+    back to back, eagerly and as one CUDA graph: the block sums, selections, O
+    and LSE must be the same bits."""
+    for name, L in (("q06b_4k", None), ("q06b_32k_sparse", 8192)):
+        case = SequenceCase(name, L=L)
+        cfg = case.cfg
+        stream = torch.cuda.Stream(device=dev())
+        runs = []
+        for mode in ("synced", "back_to_back", "graph"):
+            O_ = torch.zeros((cfg.H, case.L, cfg.D), dtype=torch.bfloat16, device=dev())
+            LSE = torch.zeros((cfg.H, case.L), dtype=torch.float32, device=dev())
+            sels = []
+
+            def chunks():
+                for c in range(len(case.seq.problems)):
+                    case.seq.run_chunk(c, case.Q, case.K, case.V, case.KP, case.VP, 0.9, O_,
+                                       LSE, stream)
+                    if mode == "synced":
+                        torch.cuda.synchronize()
+                        n = int(case.seq.bufs.n_sel[0].item())
+                        sels.append(case.seq.bufs.sel_page[0, :n].clone())
+
+            if mode == "graph":
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                    chunks()
+                O_.zero_()
+                LSE.zero_()
+                with torch.cuda.stream(stream):
+                    g.replay()
+            else:
+                with torch.cuda.stream(stream):
+                    chunks()
+            torch.cuda.synchronize()
+            assert X.xattn_device_error() == 0
+            runs.append((O_.view(torch.int16).clone(), LSE.clone(),
+                         case.seq.bufs.block_sums.clone(), sels))
+        ref = runs[0]
+        for other in runs[1:]:
+            assert torch.equal(ref[0], other[0]), f"{name}: O differs"
+            assert torch.equal(ref[1], other[1]), f"{name}: LSE differs"
+            assert torch.equal(ref[2], other[2]), f"{name}: block sums differ"
+        # the last chunk's selection of the back-to-back run equals the synced one
+        n = int(case.seq.bufs.n_sel[0].item())
+        assert torch.equal(case.seq.bufs.sel_page[0, :n], ref[3][-1])

@@ -68,12 +68,14 @@ def test_workspace_and_block_sum_sizes(lib):
     tstat = H * rq * (ncol // 128) * 8
     al = lambda x: (x + 255) // 256 * 256
     counts = al(al(bpart) + tstat)
-    part_o = al(counts + (8 * 512 + 1) * 4)  # vote counters of every (request, KV head) +
-                                             # the finishing counter; then attention
-                                             # partials: 160 CTAs x 2 slots x 256 rows
-    part_lse = al(part_o + 160 * 2 * 256 * 128 * 4)
+    est = al(counts + (8 * 512 + 1) * 4)  # vote counters of every (request, KV head) +
+                                          # the finishing counter
+    # the attention's block (at the end of the caller's buffer): partials of
+    # 160 CTAs x 2 slots x 256 rows, then two part counters per 256-row unit
+    part_lse = al(160 * 2 * 256 * 128 * 4)
     att_cnt = al(part_lse + 160 * 2 * 256 * 4)
-    expect = al(att_cnt + 16 * 16 * 2 * 4)  # two part counters per 256-row attention unit
+    attn = al(att_cnt + 16 * 16 * 2 * 4)
+    expect = est + attn + 256  # + the slack that aligns the attention block
     assert X.xattn_workspace_size(p) == expect
     assert X.xattn_block_sums_count(p) == H * 32 * 256
     # varlen batch: slabs packed request after request

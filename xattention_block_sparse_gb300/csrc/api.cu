@@ -4,6 +4,8 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 
@@ -135,11 +137,16 @@ xattn_status make_plan(const xattn_problem *p, Plan &pl) {
   // vote counters of every (request, KV head) -- one row per request for the
   // vote across KV heads, one per KV head for the selection per KV head --
   // then the select kernel's finishing counter
-  w.part_o = align_up(w.counts + ((size_t)B * Hkv * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) +
-                                  1) * sizeof(int32_t));
+  w.est = align_up(w.counts + ((size_t)B * Hkv * (size_t)(p->bt_stride > 0 ? p->bt_stride : 1) +
+                               1) * sizeof(int32_t));
+  // the attention's regions, relative to their block, which sits at the END of
+  // the caller's buffer (run_attention): a chunk's estimate (the start of the
+  // buffer) can then run beside the previous chunk's attention
+  w.part_o = 0;
   w.part_lse = align_up(w.part_o + part_rows * D * sizeof(float));
   w.att_cnt = align_up(w.part_lse + part_rows * sizeof(float));
-  w.total = align_up(w.att_cnt + (size_t)att * 2 * sizeof(int32_t));  // two per attention unit
+  w.attn = align_up(w.att_cnt + (size_t)att * 2 * sizeof(int32_t));  // two per attention unit
+  w.total = w.est + w.attn + kAlign;  // + the slack that aligns the attention block
   return XATTN_OK;
 }
 
@@ -171,6 +178,30 @@ xattn_status err_word(int32_t **out) {
 }
 
 inline xattn_status cu(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XATTN_ECUDA; }
+
+// The device range [lo, hi) of workspace that the last attention launched on
+// a stream may still be using when the next kernel on that stream starts
+// early (the attention lets its programmatic dependents start before it ends).
+struct Range {
+  uintptr_t lo, hi;
+};
+std::mutex g_attn_mu;
+std::unordered_map<cudaStream_t, Range> g_attn_ws;
+
+void note_attention(cudaStream_t st, const char *lo, const char *hi) {
+  std::lock_guard<std::mutex> lk(g_attn_mu);
+  g_attn_ws[st] = Range{reinterpret_cast<uintptr_t>(lo), reinterpret_cast<uintptr_t>(hi)};
+}
+
+// Whether a kernel writing [lo, hi) may start before the last attention on st
+// has finished: no attention recorded, or its range is disjoint.
+bool clear_of_attention(cudaStream_t st, const char *lo, const char *hi) {
+  std::lock_guard<std::mutex> lk(g_attn_mu);
+  auto it = g_attn_ws.find(st);
+  if (it == g_attn_ws.end()) return true;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(lo), b = reinterpret_cast<uintptr_t>(hi);
+  return b <= it->second.lo || a >= it->second.hi;
+}
 
 }  // namespace
 }  // namespace xattn
@@ -222,10 +253,13 @@ static xattn_status run_estimate(Plan &pl, const void *q, const void *k_cur, con
   char *ws = static_cast<char *>(workspace);
   float *bpart = reinterpret_cast<float *>(ws + pl.ws.bpart);
   float2 *tstat = reinterpret_cast<float2 *>(ws + pl.ws.tstat);
+  // the score GEMM writes [bpart, counts); it may overlap a previous attention
+  // that is still finishing only if that attention's regions lie elsewhere
+  const bool early = clear_of_attention(st, ws + pl.ws.bpart, ws + pl.ws.counts);
   s = cu(launch_score_gemm(pl.geo, pl.gemm_tiles, static_cast<const __nv_bfloat16 *>(q),
                            static_cast<const __nv_bfloat16 *>(k_cur),
                            static_cast<const __nv_bfloat16 *>(k_pool), kseq, scale, bpart, tstat,
-                           st));
+                           early, st));
   if (s != XATTN_OK) return s;
   return cu(launch_block_sum(pl.geo, pl.bsum_ctas, bpart, tstat, block_sums, st));
 }
@@ -300,7 +334,12 @@ static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *
     g.H = G;
     g.Hkv = 1;
   }
-  char *ws = static_cast<char *>(workspace);
+  // the attention's regions at the end of the buffer (see make_plan), the block
+  // 256-byte aligned in memory (its partial rows take 32-byte stores)
+  char *ws = reinterpret_cast<char *>(
+      (reinterpret_cast<uintptr_t>(workspace) + workspace_bytes - pl.ws.attn) &
+      ~(uintptr_t)(kAlign - 1));
+  note_attention(st, ws, static_cast<char *>(workspace) + workspace_bytes);
   return cu(launch_attention(g, pl.att_ctas, static_cast<const __nv_bfloat16 *>(q),
                              static_cast<const __nv_bfloat16 *>(k_cur),
                              static_cast<const __nv_bfloat16 *>(v_cur),

@@ -745,6 +745,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = g.Bk / NK;
   const int G = Gsk;  // stream-K CTAs
+  // a kernel launched after this one as a programmatic dependent (the next
+  // chunk's score GEMM, which reads nothing this kernel writes) may take SMs
+  // as they free up here
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {

@@ -77,8 +77,12 @@ __device__ __forceinline__ int page_of(const Geo &g, int r, int j) {
 // ---------------------------------------------------------------------------
 // Launch entry points implemented in the kernel translation units.
 // ---------------------------------------------------------------------------
+// Workspace of one call: the estimate's and selection's regions from the
+// start of the buffer (offsets bpart, tstat, counts; est bytes), the
+// attention's in a block of attn bytes at the end of the caller's buffer
+// (offsets part_o, part_lse, att_cnt within that block).
 struct WsLayout {
-  size_t bpart, tstat, counts, part_o, part_lse, att_cnt, total;
+  size_t bpart, tstat, counts, est, part_o, part_lse, att_cnt, attn, total;
 };
 
 // Keys of every request in logical order (xattn_estimate_seq): element
@@ -91,10 +95,12 @@ struct KeySeq {
 
 // Score GEMM with its epilogue (block partial sums, tile statistics).  Keys
 // come from kseq when it is given, else from the pool pages and k_cur.
+// early: launch as a programmatic dependent of the kernel before it on st
+// (it may start while that kernel finishes; it completes after it).
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
                               const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool,
                               const KeySeq *kseq, float scale, float *bpart, float2 *tstat,
-                              cudaStream_t st);
+                              bool early, cudaStream_t st);
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
                              float *block_sums, cudaStream_t st);
 // Threshold selection of every (request, KV head, query block), then the GQA

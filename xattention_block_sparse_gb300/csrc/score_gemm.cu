@@ -443,6 +443,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream: this launch may have started while that kernel (a previous
+  // chunk's attention, which lets its dependents start early) was still
+  // running -- none of this kernel's inputs is its output.  It completes only
+  // once that kernel has, so whatever follows on the stream sees both done.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // A view (d, phase, group, head) of a [heads, tokens, D]-strided bf16 tensor,
@@ -471,7 +477,7 @@ bool encode_phase_view(CUtensorMap *m, const void *base, int D, int S, int64_t g
 cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
                               const __nv_bfloat16 *kcur, const __nv_bfloat16 *kpool,
                               const KeySeq *kseq, float scale, float *bpart, float2 *tstat,
-                              cudaStream_t st) {
+                              bool early, cudaStream_t st) {
   if (ntiles == 0) return cudaSuccess;
   const int S = g.S, D = g.D, BRc = g.Bk / S;
   const int64_t tot_q = (int64_t)g.req[g.B - 1].q0 + g.req[g.B - 1].lq;
@@ -553,8 +559,19 @@ cudaError_t launch_score_gemm(const Geo &g, int ntiles, const __nv_bfloat16 *q,
     const int nfull = (rem > 0 && 2 * rem <= sms) ? ntiles - rem : ntiles;
     const int nwork = nfull + 2 * (ntiles - nfull);
     const int n = nwork < sms ? nwork : sms;
-    kernel<<<n, THREADS, SMEM_ALLOC, st>>>(g, mp, nwork, nfull, scale, bpart, tstat);
-    return cudaGetLastError();
+    // programmatic dependent launch: free SMs of a kernel that is finishing
+    // (the previous chunk's attention) start this one (see the kernel's end)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, g, mp, nwork, nfull, scale, bpart, tstat);
   };
   const bool sq = kseq != nullptr;
   if (g.ns > 0) {  // sampled history (keys in token order only): Br / 4 or Br / 2, >= 4
