@@ -911,23 +911,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         return mbar_wait(&bar.full[i % NSLOT], (i / NSLOT) & 1, abort, g.err);
       };
       auto issue_S = [&](int i) {  // i: load index of the K tile
+        // K-step k of head_dim: byte offset (k / 4) * half + (k % 4) * 32 in
+        // both operands (one PTX block of D / 16 MMAs)
         const uint64_t b0 = dK0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16_ss(tS, dQ + (uint64_t)(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4),
-                     b0 + (uint64_t)(((kk / 4) * (NK * 128) + (kk % 4) * 32) >> 4), idS,
-                     kk > 0 ? 1u : 0u);
+        static_assert(BM == 128, "query tile of 128 rows");
+        if constexpr (D == 128 && NK == 128)
+          mma_ss_d128_nk128(tS, dQ, b0, idS, 0u);
+        else if constexpr (D == 128)
+          mma_ss_d128_nk64(tS, dQ, b0, idS, 0u);
+        else
+          mma_ss_d64(tS, dQ, b0, idS, 0u);
         mma_commit(&bar.s_full[x]);
       };
       auto issue_PV = [&](int i, bool first) {  // i: load index of the V tile
         const uint64_t b0 = dV0 + (uint64_t)(((i % NSLOT) * LY::KV_BYTES) >> 4);
         // A = P in TMEM (16 keys = 8 columns per step); B = V, MN-major
         // (d contiguous): the two 64-wide d blocks are NK*128 bytes apart,
-        // 8-key groups 1024 apart
-#pragma unroll
-        for (int kk = 0; kk < NK / 16; ++kk)
-          mma_f16_ts(tO, tS + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idPV,
-                     (!first || kk > 0) ? 1u : 0u);
+        // 8-key groups 1024 apart; one PTX block of NK / 16 MMAs
+        if constexpr (NK == 128)
+          mma_ts_nk128(tO, tS, b0, idPV, first ? 0u : 1u);
+        else
+          mma_ts_nk64(tO, tS, b0, idPV, first ? 0u : 1u);
         mma_commit(&bar.pv_done[x]);
       };
       int turn = 0;  // turns taken: A's turn n follows B's turn n-1, B's turn n follows A's turn n

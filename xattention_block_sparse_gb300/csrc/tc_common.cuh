@@ -172,6 +172,81 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// One accumulation of 4 or 8 MMAs (K = 16 each) as one block of PTX, so that
+// the issuing thread spends few instructions per MMA: a descriptor advances by
+// a 32-bit add on its low word (the start-address field, in 16-byte units:
+// shared memory is under 256 KB, so it never carries out), and the accumulate
+// predicates are set once.  The first MMA accumulates iff acc0 != 0, the rest
+// always.
+#define XATTN_GRP_DECL "{\n\t.reg .pred p0, pt;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+// S-type: D (+)= A B^T, A and B from shared memory (%1/%2 A lo/hi, %3/%4 B lo/hi)
+#define XATTN_SS_FIRST                                                  \
+  "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.b32 pt, %6, %6;\n\t"               \
+  "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"                  \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
+#define XATTN_SS_NEXT(AO, BO)                                           \
+  "add.u32 al, %1, " #AO ";\n\tadd.u32 bl, %3, " #BO ";\n\t"            \
+  "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"                  \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, pt;\n\t"
+#define XATTN_SS_ARGS                                                                \
+  "r"(d_tmem), "r"((uint32_t)a_desc), "r"((uint32_t)(a_desc >> 32)),                  \
+      "r"((uint32_t)b_desc), "r"((uint32_t)(b_desc >> 32)), "r"(idesc), "r"(acc0)
+// P.V-type: D (+)= A B^T, A (P) in tensor memory (%1), B from shared memory
+// (%2/%3 lo/hi)
+#define XATTN_TS_FIRST                                                  \
+  "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"               \
+  "mov.b64 db, {%2, %3};\n\t"                                           \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+#define XATTN_TS_NEXT(AO, BO)                                           \
+  "add.u32 al, %1, " #AO ";\n\tadd.u32 bl, %2, " #BO ";\n\t"            \
+  "mov.b64 db, {bl, %3};\n\t"                                           \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [al], db, %4, pt;\n\t"
+#define XATTN_TS_ARGS                                                                 \
+  "r"(d_tmem), "r"(a_tmem), "r"((uint32_t)b_desc), "r"((uint32_t)(b_desc >> 32)),      \
+      "r"(idesc), "r"(acc0)
+
+// S = Q K^T over head_dim 128 (two 64-wide 128B-swizzle halves per operand):
+// MMA k at K offset (k / 4) * half + (k % 4) * 32 bytes; half = 128 rows * 128 B
+// for A, NK rows * 128 B for B (1024 or 512 in 16-byte units).
+__device__ __forceinline__ void mma_ss_d128_nk128(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t acc0) {
+  asm volatile(XATTN_GRP_DECL XATTN_SS_FIRST XATTN_SS_NEXT(2, 2) XATTN_SS_NEXT(4, 4)
+                   XATTN_SS_NEXT(6, 6) XATTN_SS_NEXT(1024, 1024) XATTN_SS_NEXT(1026, 1026)
+                       XATTN_SS_NEXT(1028, 1028) XATTN_SS_NEXT(1030, 1030) "}\n" ::XATTN_SS_ARGS
+               : "memory");
+}
+__device__ __forceinline__ void mma_ss_d128_nk64(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t acc0) {
+  asm volatile(XATTN_GRP_DECL XATTN_SS_FIRST XATTN_SS_NEXT(2, 2) XATTN_SS_NEXT(4, 4)
+                   XATTN_SS_NEXT(6, 6) XATTN_SS_NEXT(1024, 512) XATTN_SS_NEXT(1026, 514)
+                       XATTN_SS_NEXT(1028, 516) XATTN_SS_NEXT(1030, 518) "}\n" ::XATTN_SS_ARGS
+               : "memory");
+}
+// head_dim 64: one swizzle half, four MMAs
+__device__ __forceinline__ void mma_ss_d64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t acc0) {
+  asm volatile(XATTN_GRP_DECL XATTN_SS_FIRST XATTN_SS_NEXT(2, 2) XATTN_SS_NEXT(4, 4)
+                   XATTN_SS_NEXT(6, 6) "}\n" ::XATTN_SS_ARGS
+               : "memory");
+}
+// O (+)= P V over NK keys: MMA k reads P columns 8k.. (16 keys) and the V rows
+// of keys 16k.. (2048 bytes on: 128 in 16-byte units)
+__device__ __forceinline__ void mma_ts_nk128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t acc0) {
+  asm volatile(XATTN_GRP_DECL XATTN_TS_FIRST XATTN_TS_NEXT(8, 128) XATTN_TS_NEXT(16, 256)
+                   XATTN_TS_NEXT(24, 384) XATTN_TS_NEXT(32, 512) XATTN_TS_NEXT(40, 640)
+                       XATTN_TS_NEXT(48, 768) XATTN_TS_NEXT(56, 896) "}\n" ::XATTN_TS_ARGS
+               : "memory");
+}
+__device__ __forceinline__ void mma_ts_nk64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t acc0) {
+  asm volatile(XATTN_GRP_DECL XATTN_TS_FIRST XATTN_TS_NEXT(8, 128) XATTN_TS_NEXT(16, 256)
+                   XATTN_TS_NEXT(24, 384) "}\n" ::XATTN_TS_ARGS
+               : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
