@@ -147,3 +147,62 @@ def test_wave_over_two_requests(monkeypatch, schedule):
         check_attention(og_all[:, idx].astype(np.float64), lg_all[:, idx], o_ref, l_ref,
                         f"request {r}")
         q0 += lq
+
+
+@pytest.mark.parametrize("schedule", [None, "streamk"])
+def test_attention_logit_jumps(monkeypatch, schedule):
+    """Key pages whose logits sit far above or below the rest: every query
+    carries a shared direction u, and the keys of some selected pages carry
+    +-beta u, which moves those pages' logits by the boost below (in nats).
+    The kernel takes exponentials against the row max as it stood when last
+    raised; a tile whose values climb 2^64 above it is taken again exactly
+    (62 nats = 89 in base 2), one that climbs less is accepted as is (30 and
+    45 nats), and tiles far below it underflow to zero as they should.  Rows
+    of every 128-row tile's edges and random rows against the float64
+    oracle."""
+    if schedule is not None:
+        monkeypatch.setenv("XATTN_ATTN_SCHEDULE", schedule)
+    H, Hkv, D, Bk, S, lq, n_hist = 4, 2, 128, 128, 8, 512, 40
+    boost = {3: 30.0, 12: 62.0, 20: 0.0, 25: -62.0, 30: 45.0, 36: 70.0}
+    d = dev()
+    rng = np.random.default_rng(4242)
+    P = n_hist + 3
+    G = H // Hkv
+    u = rng.standard_normal((Hkv, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    alpha = 8.0
+    q = rng.standard_normal((H, lq, D)) + alpha * np.repeat(u, G, axis=0)[:, None, :]
+    kc = rng.standard_normal((Hkv, lq, D))
+    vc = rng.standard_normal((Hkv, lq, D))
+    kp = rng.standard_normal((P, Bk, Hkv, D))
+    vp = rng.standard_normal((P, Bk, Hkv, D))
+    perm = rng.permutation(P).astype(np.int32)
+    bt = perm[None, :n_hist].copy()
+    for lp, b in boost.items():
+        beta = b * math.sqrt(D) / alpha
+        kp[bt[0, lp]] += beta * u[None, :, :]
+    q, kc, vc, kp, vp = (I.bf16_round(a.astype(np.float32)) for a in (q, kc, vc, kp, vp))
+    pages = bt[0, :]
+
+    prob = X.Problem(H, Hkv, D, S, Bk, [lq], [n_hist * Bk], torch.from_numpy(bt).to(d), P)
+    ws = torch.empty(max(X.xattn_workspace_size(prob), 256), dtype=torch.uint8, device=d)
+    sel_page = torch.from_numpy(pages.astype(np.int32))[None, :].to(d)
+    n_sel_t = torch.tensor([n_hist], dtype=torch.int32, device=d)
+    O_ = torch.zeros((H, lq, D), dtype=torch.bfloat16, device=d)
+    LSE = torch.zeros((H, lq), dtype=torch.float32, device=d)
+    scale = 1.0 / math.sqrt(D)
+    X.bsa_chunk_attention(prob, to_dev_bf16(q), to_dev_bf16(kc), to_dev_bf16(vc), to_dev_bf16(kp),
+                          to_dev_bf16(vp), sel_page, n_sel_t, scale, ws, O_, LSE)
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+
+    edges = {e for m in range(0, lq, 128) for e in (m, m + 1, m + 126, m + 127)}
+    rows = sorted(edges | set(rng.integers(0, lq, 16).tolist()))
+    o_ref, l_ref = O.attend_request(_bits_to_f64(q), _bits_to_f64(kc), _bits_to_f64(vc),
+                                    _bits_to_f64(kp), _bits_to_f64(vp), pages, H, Hkv, scale,
+                                    rows=rows)
+    # the boosted pages dominate: the largest LSE is near the top boost
+    assert l_ref.max() > 60.0
+    idx = np.asarray(rows)
+    check_attention(O_.float().cpu().numpy()[:, idx].astype(np.float64), LSE.cpu().numpy()[:, idx],
+                    o_ref, l_ref, "logit jumps")
