@@ -509,12 +509,14 @@ def run_ours(args, ws, rank, local):
 
 def run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk):
     """Same metric through the public API with pinned HOST buffers: every step
-    copies the layer's Q, K, V host->device chunk by chunk and reads O and LSE
-    back, the copies of later chunks overlapped with the compute of earlier
-    ones (`SequencePrefill.run_from_host`).  The page pools are this sequence's
-    own keys and values: each chunk's K/V are stored into their pages on the
-    device (xattn_store_kv) before the chunk runs, so the history the next
-    chunk reads is built in place rather than copied in."""
+    copies the layer's Q, K, V host->device chunk by chunk, the copies of later
+    chunks overlapped with the compute of earlier ones, and O and LSE reach
+    the host buffers within the step (`SequencePrefill.run_from_host`): copied
+    back per chunk on a side stream, or, with --e2e-direct-out, written there
+    by the attention kernel itself.  The page pools are this sequence's own
+    keys and values: each chunk's K/V are stored into their pages on the
+    device (xattn_store_kv) before the chunk's attention, so the history the
+    next chunk reads is built in place rather than copied in."""
     pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(
         torch.bfloat16).pin_memory()
     L = cfg.L
@@ -528,7 +530,8 @@ def run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk):
     d2h = sum(host[k].numel() * host[k].element_size() for k in ("o", "lse"))
     h2d_stream, d2h_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     def one():
-        seq.run_from_host(host, devb, tau, stream, h2d_stream, d2h_stream, store_kv=True)
+        seq.run_from_host(host, devb, tau, stream, h2d_stream, d2h_stream, store_kv=True,
+                          out_direct=args.e2e_direct_out)
 
     for _ in range(max(1, args.warmup)):
         one()
@@ -563,8 +566,10 @@ def run_e2e(args, wl, cfg, seq, tau, dev, stream, X, RN, torch, nchunk, chunk):
             "copies": "Q, K, V copied chunk by chunk on one side stream, overlapped with "
                       "earlier chunks' compute (a chunk's estimate waits for its Q and K, "
                       "its attention for V too); each chunk's K/V stored into its pool pages "
-                      "on the device (xattn_store_kv) before its attention; O and LSE read "
-                      "back per chunk on another side stream"}
+                      "on the device (xattn_store_kv) before its attention; "
+                      + ("O and LSE written into the pinned host buffers by the attention "
+                         "kernel itself (d2h bytes: those stores)" if args.e2e_direct_out else
+                         "O and LSE read back per chunk on another side stream")}
 
 
 # ---------------------------------------------------------------------------
@@ -687,6 +692,9 @@ def main():
                     help="time eager launches instead of replays of a CUDA graph of the step")
     ap.add_argument("--skip-sparse", action="store_true",
                     help="time only the headline workload (no sparse-workload lines)")
+    ap.add_argument("--e2e-direct-out", action="store_true",
+                    help="end-to-end leg: the attention writes O and LSE into the pinned "
+                         "host buffers itself instead of a copy back per chunk")
     ap.add_argument("--est-from-pages", action="store_true",
                     help="estimate from the history pages (xattn_estimate) instead of the "
                          "keys in token order (xattn_estimate_seq)")

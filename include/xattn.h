@@ -310,6 +310,11 @@ xattn_status xattn_select_noalloc(const xattn_problem *p, const float *block_sum
  *                  repeated calls give identical bits.
  *   o    DEVICE bf16 [H, tokens, D] (q_head_stride)   normalised output
  *   lse  DEVICE fp32 [H, tokens] (lse_head_stride)    natural-log LSE
+ *        Either may instead be page-locked HOST memory (cudaHostAlloc,
+ *        cudaMallocHost or cudaHostRegister): the kernel then writes it through
+ *        its device alias over the host link, each row as it is finished, and
+ *        no separate device-to-host copy is needed; the host may read it once
+ *        the stream has passed the call.  Pageable host memory: XATTN_EINVAL.
  * A following xattn_estimate* call on the same stream may start before this
  * call has finished (see xattn_estimate, Ordering); every other operation
  * enqueued after it starts when it has finished. */

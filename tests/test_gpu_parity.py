@@ -268,12 +268,14 @@ def test_selection_vote_parameters(vote, force):
                      O.gqa_vote(mk.astype(bool), cfg.Hkv, kbh))
 
 
-def test_prefill_from_host_matches_device_resident_run():
+@pytest.mark.parametrize("out_direct", [True, False])
+def test_prefill_from_host_matches_device_resident_run(out_direct):
     """SequencePrefill.run_from_host (copies of later chunks overlapped with the
-    compute of earlier ones, read-back chunk by chunk) gives exactly the O and
-    LSE of the run on device-resident inputs: a chunk that computed before its
-    inputs or history pages landed, or a read-back before the chunk finished,
-    would differ."""
+    compute of earlier ones; outputs written into the host buffers by the
+    attention, or read back chunk by chunk) gives exactly the O and LSE of the
+    run on device-resident inputs: a chunk that computed before its inputs or
+    history pages landed, or a read-back before the chunk finished, would
+    differ."""
     case = SequenceCase("q06b_4k")
     O_dev, L_dev, _ = case.run(0.9)
     pin = lambda t: t.cpu().pin_memory()
@@ -285,7 +287,7 @@ def test_prefill_from_host_matches_device_resident_run():
     stream = torch.cuda.Stream(device=dev())
     h2d, d2h = torch.cuda.Stream(device=dev()), torch.cuda.Stream(device=dev())
     for _ in range(2):  # twice: the second run reuses every buffer
-        case.seq.run_from_host(host, devb, 0.9, stream, h2d, d2h)
+        case.seq.run_from_host(host, devb, 0.9, stream, h2d, d2h, out_direct=out_direct)
     stream.synchronize()
     assert X.xattn_device_error() == 0
     assert np.array_equal(host["o"].float().numpy(), O_dev)
@@ -332,11 +334,13 @@ def test_store_kv_writes_each_chunk_block_to_its_page(Hkv, D, Bk):
     assert np.array_equal(got_v, want_v)
 
 
-def test_prefill_from_host_with_kv_store_matches_prefilled_pool():
+@pytest.mark.parametrize("out_direct", [True, False])
+def test_prefill_from_host_with_kv_store_matches_prefilled_pool(out_direct):
     """run_from_host(store_kv=True) copies only Q, K, V and builds the pools on
-    the device, chunk by chunk, from the sequence's own keys and values: its O
-    and LSE equal those of the run on the prefilled pools, and the pools end
-    equal to them.  The device pools start as NaN, so a history page read
+    the device, chunk by chunk, from the sequence's own keys and values (the
+    outputs copied back, or written into the host buffers by the attention):
+    its O and LSE equal those of the run on the prefilled pools, and the pools
+    end equal to them.  The device pools start as NaN, so a history page read
     before it was stored would show."""
     case = SequenceCase("q06b_4k")
     O_dev, L_dev, _ = case.run(0.9)
@@ -350,7 +354,8 @@ def test_prefill_from_host_with_kv_store_matches_prefilled_pool():
     stream = torch.cuda.Stream(device=dev())
     h2d, d2h = torch.cuda.Stream(device=dev()), torch.cuda.Stream(device=dev())
     for _ in range(2):
-        case.seq.run_from_host(host, devb, 0.9, stream, h2d, d2h, store_kv=True)
+        case.seq.run_from_host(host, devb, 0.9, stream, h2d, d2h, store_kv=True,
+                               out_direct=out_direct)
     stream.synchronize()
     assert X.xattn_device_error() == 0
     assert np.array_equal(host["o"].float().numpy(), O_dev)

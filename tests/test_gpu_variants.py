@@ -479,3 +479,62 @@ def test_host_fed_prefill_replayed_from_a_cuda_graph():
         assert X.xattn_device_error() == 0
         assert np.array_equal(host["o"].float().numpy(), O_dev)
         assert np.array_equal(host["lse"].numpy(), L_dev)
+
+
+def test_attention_writes_pinned_host_outputs():
+    """bsa_chunk_attention with o and lse in page-locked host memory (whole
+    tensors, and windows of them at a token offset, as the host-fed prefill
+    passes them) writes exactly the bits it writes into device buffers; the
+    per-KV-head entry point too.  Pageable host memory is refused with
+    XATTN_EINVAL before anything is launched."""
+    import ctypes
+    case = SequenceCase("q06b_4k")
+    cfg, H, L, D = case.cfg, case.cfg.H, case.L, case.cfg.D
+    # chunks 0 .. 2 on the device, then chunk 3's attention both ways
+    seq, b = case.seq, case.seq.bufs
+    O_d = torch.zeros((H, L, D), dtype=torch.bfloat16, device=dev())
+    L_d = torch.zeros((H, L), dtype=torch.float32, device=dev())
+    for c in range(4):
+        seq.run_chunk(c, case.Q, case.K, case.V, case.KP, case.VP, 0.9, O_d, L_d, None)
+    torch.cuda.synchronize()
+    c = 3
+    t0 = c * case.chunk
+    p = seq.problems[c]
+    scale = 1.0 / np.sqrt(D)
+    O_h = torch.full((H, L, D), 7.0, dtype=torch.bfloat16).pin_memory()
+    L_h = torch.full((H, L), 7.0, dtype=torch.float32).pin_memory()
+    args = (p, case.Q[:, t0:], case.K[:, t0:], case.V[:, t0:], case.KP, case.VP, b.sel_page,
+            b.n_sel, scale, b.workspace)
+    X.bsa_chunk_attention(*args, O_h[:, t0:], L_h[:, t0:])
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    assert torch.equal(O_h[:, t0:].view(torch.int16), O_d[:, t0:].cpu().view(torch.int16))
+    assert torch.equal(L_h[:, t0:], L_d[:, t0:].cpu())
+    assert torch.all(O_h[:, :t0] == 7.0) and torch.all(L_h[:, :t0] == 7.0)  # nothing else
+    # the per-KV-head entry point on the selection of every KV head
+    sel_kv = b.sel_page.repeat_interleave(cfg.Hkv, 0)[None].reshape(1, cfg.Hkv, -1).contiguous()
+    n_kv = b.n_sel.repeat_interleave(cfg.Hkv, 0)[None].reshape(1, cfg.Hkv).contiguous()
+    O_h2 = torch.zeros_like(O_h).pin_memory()
+    L_h2 = torch.zeros_like(L_h).pin_memory()
+    O_d2, L_d2 = torch.zeros_like(O_d), torch.zeros_like(L_d)
+    for o_, l_ in ((O_d2, L_d2), (O_h2, L_h2)):
+        X.bsa_chunk_attention_per_kv_head(p, *args[1:6], sel_kv, n_kv, scale, b.workspace,
+                                          o_[:, t0:], l_[:, t0:])
+    torch.cuda.synchronize()
+    assert X.xattn_device_error() == 0
+    assert torch.equal(O_h2[:, t0:].view(torch.int16), O_d2[:, t0:].cpu().view(torch.int16))
+    assert torch.equal(L_h2[:, t0:], L_d2[:, t0:].cpu())
+    # pageable host memory: the binding refuses it, and so does the library
+    pageable_o = torch.zeros((H, L, D), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        X.bsa_chunk_attention(*args, pageable_o, L_h)
+    lib = X.load_library()
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.bsa_chunk_attention(p.ref(), vp(case.Q[:, t0:]), vp(case.K[:, t0:]),
+                                 vp(case.V[:, t0:]), vp(case.KP), vp(case.VP), vp(b.sel_page),
+                                 vp(b.n_sel), float(scale), vp(b.workspace),
+                                 b.workspace.numel(), vp(pageable_o), vp(L_h),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == -1  # XATTN_EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(pageable_o == 0)

@@ -12,9 +12,10 @@ the test checks, on CUDA's happens-before order rebuilt from the log:
     with prefilled pools, of both pools when it has history);
   * its KV store and its attention follow the copy of its V;
   * with the store, the estimate of chunk c + 1 follows chunk c's store;
-  * its O and LSE leave the device only after its attention;
+  * O and LSE copied to the host only after its attention, or, the other
+    way, written by the attention straight into the host buffers;
   * the side streams start after the work already on the compute stream,
-    and the returned event follows every read-back.
+    and the returned event follows every attention, read-back and store.
 """
 import pytest
 import torch
@@ -41,7 +42,7 @@ def built():
     X.load_library()
 
 
-def _run(monkeypatch, store_kv, n_chunks=3):
+def _run(monkeypatch, store_kv, n_chunks=3, out_direct=False):
     log, _ = FS.install(monkeypatch)
     H, Hkv, D, S, Bk, chunk = 2, 1, 64, 8, 64, 64
     L = chunk * n_chunks
@@ -60,10 +61,15 @@ def _run(monkeypatch, store_kv, n_chunks=3):
         assert t1 - t0 == chunk
         log.append(("copy", stream, (names[id(dst)], t0 // chunk)))
 
+    outputs = {}
+
     def rec(kind):
         def f(p, *a, **k):
             stream = a[-1] if a else k.get("stream")
             log.append((kind, stream, chunk_of[id(p)]))
+            if kind == "attend":  # o, lse come before the stream
+                outputs[chunk_of[id(p)]] = tuple(names[id(t._base)] + ":" + (
+                    "host" if t._base is host[n] else "dev") for t, n in zip(a[-3:-1], ("o", "lse")))
         return f
 
     monkeypatch.setattr(X, "copy_window_async", copy_window)
@@ -73,8 +79,9 @@ def _run(monkeypatch, store_kv, n_chunks=3):
         monkeypatch.setattr(X, fn, rec(kind))
     compute, h2d, d2h = (FS.Stream(log, n) for n in ("compute", "h2d", "d2h"))
     log.append(("earlier work", compute, None))
-    back = seq.run_from_host(host, dev, 0.9, compute, h2d, d2h, store_kv=store_kv)
-    return log, back, (compute, h2d, d2h), n_chunks
+    back = seq.run_from_host(host, dev, 0.9, compute, h2d, d2h, store_kv=store_kv,
+                             out_direct=out_direct)
+    return log, back, (compute, h2d, d2h), n_chunks, outputs
 
 
 def _index(log, kind, payload):
@@ -83,10 +90,14 @@ def _index(log, kind, payload):
     return hits[0]
 
 
+@pytest.mark.parametrize("out_direct", [True, False])
 @pytest.mark.parametrize("store_kv", [True, False])
-def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatch, store_kv):
-    log, back, (compute, h2d, d2h), n = _run(monkeypatch, store_kv)
+def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatch, store_kv,
+                                                               out_direct):
+    log, back, (compute, h2d, side), n, outputs = _run(monkeypatch, store_kv,
+                                                       out_direct=out_direct)
     before = FS.happens_before(log)
+    end = FS.record_index(log, back)
     for c in range(n):
         est, att = _index(log, "estimate", c), _index(log, "attend", c)
         assert log[est][1] is compute and log[att][1] is compute
@@ -97,13 +108,19 @@ def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatc
             assert before(_index(log, "copy", ("k", c2)), est)
         assert before(_index(log, "copy", ("v", c)), att)
         assert before(est, _index(log, "select", c)) and before(_index(log, "select", c), att)
-        for name in ("o", "lse"):
-            rb = _index(log, "copy", (name, c))
-            assert log[rb][1] is d2h and before(att, rb)
-            assert before(rb, FS.record_index(log, back))
+        assert before(att, end)
+        if out_direct:
+            assert outputs[c] == ("o:host", "lse:host")
+            assert not any(op[0] == "copy" and op[2] == (name, c) for op in log
+                           for name in ("o", "lse"))
+        else:
+            assert outputs[c] == ("o:dev", "lse:dev")
+            for name in ("o", "lse"):
+                rb = _index(log, "copy", (name, c))
+                assert log[rb][1] is side and before(att, rb) and before(rb, end)
         if store_kv:
             st = _index(log, "store", c)
-            assert before(_index(log, "copy", ("k", c)), st)
+            assert log[st][1] is compute
             assert before(_index(log, "copy", ("v", c)), st) and before(st, att)
             if c + 1 < n:
                 assert before(st, _index(log, "estimate", c + 1))
@@ -112,7 +129,7 @@ def test_host_fed_prefill_orders_every_consumer_after_its_copy(built, monkeypatc
                 assert before(_index(log, "copy", (pool, 0)), est)
     assert any(op[0] == "store" for op in log) == store_kv
     first = _index(log, "earlier work", None)
-    for s in (h2d, d2h):
+    for s in (h2d, side):
         ops = [i for i, op in enumerate(log) if op[1] is s and op[0] != "record"]
         assert all(before(first, i) for i in ops)
 
@@ -121,7 +138,7 @@ def test_estimate_does_not_wait_for_its_v(built, monkeypatch):
     """Q and K are all the estimate reads: its wait ends at the K copy, so the
     V copy of the same chunk can still be in flight (the copies are issued
     Q, K, V)."""
-    log, _, _, n = _run(monkeypatch, True)
+    log, _, _, n, _ = _run(monkeypatch, True)
     before = FS.happens_before(log)
     for c in range(n):
         assert not before(_index(log, "copy", ("v", c)), _index(log, "estimate", c))
@@ -130,7 +147,7 @@ def test_estimate_does_not_wait_for_its_v(built, monkeypatch):
 def test_a_missing_wait_is_caught(built, monkeypatch):
     """The check has teeth: without the compute stream's waits, chunk 1's
     estimate no longer follows its copies."""
-    log, _, (compute, _, _), _ = _run(monkeypatch, True)
+    log, _, (compute, _, _), _, _ = _run(monkeypatch, True)
     log2 = [op for op in log if not (op[0] == "wait" and op[1] is compute)]
     before = FS.happens_before(log2)
     assert not before(_index(log2, "copy", ("k", 1)), _index(log2, "estimate", 1))

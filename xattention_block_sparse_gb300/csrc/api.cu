@@ -297,6 +297,28 @@ static xattn_status run_select(Plan &pl, const xattn_problem *p, const float *bl
 // Launches the attention of a validated plan; per_kv: the selection holds one
 // page list per (request, KV head), and each request's KV-head groups run as
 // requests of their own (G query heads, one KV head).
+// The address kernels write an output through: device (or managed) memory as
+// given; page-locked host memory (cudaHostAlloc, cudaMallocHost, or
+// cudaHostRegister'd) through its device alias, so the kernel's stores cross
+// the host link as they are made; anything else (pageable host memory) is
+// refused.
+static xattn_status output_address(void *ptr, void **dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();  // leave no error behind for the caller's next check
+    return XATTN_EINVAL;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *dev = ptr;
+    return XATTN_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *dev = a.devicePointer;
+    return XATTN_OK;
+  }
+  return XATTN_EINVAL;
+}
+
 static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *q,
                                   const void *k_cur, const void *v_cur, const void *k_pool,
                                   const void *v_pool, const int32_t *sel_page,
@@ -314,6 +336,9 @@ static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *
     return XATTN_EALIGN;
   if (workspace_bytes < pl.ws.total) return XATTN_EWORKSPACE;
   if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
+  void *o_dev = nullptr, *lse_dev = nullptr;
+  if ((s = output_address(o, &o_dev)) != XATTN_OK) return s;
+  if ((s = output_address(lse, &lse_dev)) != XATTN_OK) return s;
   Geo g = pl.geo;
   if (per_kv) {
     // request r, KV head k -> request r * Hkv + k with the G query heads of
@@ -345,7 +370,8 @@ static xattn_status run_attention(Plan &pl, const xattn_problem *p, const void *
                              static_cast<const __nv_bfloat16 *>(v_cur),
                              static_cast<const __nv_bfloat16 *>(k_pool),
                              static_cast<const __nv_bfloat16 *>(v_pool), sel_page, n_sel,
-                             softmax_scale, static_cast<__nv_bfloat16 *>(o), lse,
+                             softmax_scale, static_cast<__nv_bfloat16 *>(o_dev),
+                             static_cast<float *>(lse_dev),
                              reinterpret_cast<float *>(ws + pl.ws.part_o),
                              reinterpret_cast<float *>(ws + pl.ws.part_lse),
                              reinterpret_cast<int32_t *>(ws + pl.ws.att_cnt), st));

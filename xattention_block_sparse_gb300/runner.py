@@ -148,44 +148,47 @@ class SequencePrefill:
             if on_chunk is not None:
                 on_chunk(c, self.bufs)
 
-    def run_from_host(self, host, dev, tau, stream, h2d_stream, d2h_stream, store_kv=False):
+    def run_from_host(self, host, dev, tau, stream, h2d_stream, d2h_stream, store_kv=False,
+                      out_direct=False):
         """The whole prefill from pinned host memory, copies overlapped with
         compute.  Chunk c computes on `stream` once the copies it reads have
-        landed (an event), and its O and LSE go device -> host on `d2h_stream`
-        once it is done ([SYNC] 修复方案: every consumer waits on the event of
+        landed (an event) ([SYNC] 修复方案: every consumer waits on the event of
         the copy it reads).
 
-        store_kv=False: the page pools are inputs.  On `h2d_stream`: chunk 0's
-        Q, K, V, then the two pools (one copy each: a chunk's history pages are
-        scattered through the pool by the block table), then the Q, K, V of
-        chunks 1, 2, ...; chunk 0 runs while the pools are still coming in.
+        Inputs: on `h2d_stream`, chunk by chunk, Q and K (all the estimate
+        reads) then V (read by the attention only).
 
-        store_kv=True: the pools are built on the device.  Only Q, K, V cross
-        from the host, chunk by chunk; before chunk c's attention, xattn_store_kv
-        writes its K and V into the pages the block table gives their positions
-        ("Task Plan: Layerwise Offload Refactoring", Phase 1.2), which is the
-        history chunk c + 1 reads.  With a block table that maps every position
-        of the sequence, the pools end up equal to a prefilled pool of the same
-        sequence, so the results are too.
+        Outputs: O and LSE go device -> host on `d2h_stream` once the chunk is
+        done.  out_direct=True instead has the attention write them straight
+        into the pinned host buffers (bsa_chunk_attention takes page-locked
+        host memory): nothing is copied, but the kernel's row stores then cross
+        the host link as it runs.
+
+        store_kv=False: the page pools are inputs, copied on `h2d_stream` after
+        chunk 0's Q, K, V (one copy each: a chunk's history pages are scattered
+        through the pool by the block table); chunk 0 runs while they come in.
+        store_kv=True: the pools are built on the device.  Before chunk c's
+        attention, xattn_store_kv writes its K and V into the pages the block
+        table gives their positions ("Task Plan: Layerwise Offload
+        Refactoring", Phase 1.2), which is the history chunk c + 1 reads.  With
+        a block table that maps every position of the sequence, the pools end
+        up equal to a prefilled pool of the same sequence, so the results are
+        too.
 
         host, dev: dicts of tensors 'q', 'k', 'v', 'o', 'lse' (and 'kpool',
         'vpool' on the device; on the host too unless store_kv), host pinned,
         same shapes.  Work is enqueued after whatever `stream` already holds;
         the side streams start from that point too.  Returns the event recorded
-        on `stream` after the last read-back."""
+        on `stream` once every output is on the host."""
         import torch
         start = torch.cuda.Event()
         start.record(stream)
         h2d_stream.wait_event(start)
         d2h_stream.wait_event(start)
         n = len(self.problems)
-        ready = []
-
-        ready_v = []
+        ready, ready_v = [], []
 
         def chunk_inputs(c):
-            # Q and K first (all the estimate reads), then V (read by the
-            # attention): a chunk's estimate starts one third of a copy sooner
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             for name in ("q", "k", "v"):  # one 2-D copy each: a row per head
                 X.copy_window_async(dev[name], host[name], t0, t1, h2d_stream)
@@ -201,6 +204,7 @@ class SequencePrefill:
                 dev["vpool"].copy_(host["vpool"], non_blocking=True)
             for c in range(1, n):
                 chunk_inputs(c)
+        out = host if out_direct else dev
         for c in range(n):
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             p = self.problems[c]
@@ -211,16 +215,19 @@ class SequencePrefill:
             stream.wait_event(ready_v[c])
             if store_kv:  # the history of chunk c + 1, before anything reads it
                 X.xattn_store_kv(p, k, v, dev["kpool"], dev["vpool"], stream)
-            attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, dev["o"][:, t0:],
-                   dev["lse"][:, t0:], stream=stream, per_kv_head=self.per_kv_head)
-            done = torch.cuda.Event()
-            done.record(stream)
-            d2h_stream.wait_event(done)
-            X.copy_window_async(host["o"], dev["o"], t0, t1, d2h_stream)
-            X.copy_window_async(host["lse"], dev["lse"], t0, t1, d2h_stream)
+            attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, out["o"][:, t0:],
+                   out["lse"][:, t0:], stream=stream, per_kv_head=self.per_kv_head)
+            if not out_direct:
+                done = torch.cuda.Event()
+                done.record(stream)
+                d2h_stream.wait_event(done)
+                X.copy_window_async(host["o"], dev["o"], t0, t1, d2h_stream)
+                X.copy_window_async(host["lse"], dev["lse"], t0, t1, d2h_stream)
+        side_done = torch.cuda.Event()
+        side_done.record(d2h_stream)
+        stream.wait_event(side_done)
         back = torch.cuda.Event()
-        back.record(d2h_stream)
-        stream.wait_event(back)
+        back.record(stream)
         return back
 
 

@@ -178,6 +178,19 @@ def _dev(t, what, *dtypes):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out(t, what, *dtypes):
+    """Address of an attention output: a CUDA tensor, or a pinned CPU tensor
+    that the kernel writes over the host link (the library resolves its device
+    alias and refuses pageable memory)."""
+    if t is not None and not getattr(t, "is_cuda", False):
+        if not t.is_pinned():
+            raise ValueError(f"{what}: a CUDA tensor or a pinned CPU tensor is required")
+        if dtypes and str(t.dtype) not in dtypes:
+            raise TypeError(f"{what}: element type {t.dtype}, expected {' or '.join(dtypes)}")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, what, *dtypes)
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -302,7 +315,7 @@ def bsa_chunk_attention(problem, q, k_cur, v_cur, k_pool, v_pool, sel_page, n_se
                                             _dev(n_sel, "n_sel", _I32), float(softmax_scale),
                                             _dev(workspace, "workspace"),
                                             workspace.numel() * workspace.element_size(),
-                                            _dev(o, "o", _BF16), _dev(lse, "lse", _F32),
+                                            _out(o, "o", _BF16), _out(lse, "lse", _F32),
                                             _stream(stream))
     _check(st, "bsa_chunk_attention")
 
@@ -316,7 +329,7 @@ def bsa_chunk_attention_per_kv_head(problem, q, k_cur, v_cur, k_pool, v_pool, se
         _dev(v_cur, "v_cur", _BF16), _dev(k_pool, "k_pool", _BF16), _dev(v_pool, "v_pool", _BF16),
         _dev(sel_page, "sel_page", _I32), _dev(n_sel, "n_sel", _I32), float(softmax_scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _dev(o, "o", _BF16), _dev(lse, "lse", _F32), _stream(stream))
+        _out(o, "o", _BF16), _out(lse, "lse", _F32), _stream(stream))
     _check(st, "bsa_chunk_attention_per_kv_head")
 
 
