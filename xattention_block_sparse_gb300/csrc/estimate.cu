@@ -31,6 +31,9 @@ __global__ void __launch_bounds__(BTHR) block_sum_kernel(const __grid_constant__
                                                          float *__restrict__ bs) {
   static_assert(BR >= 8 && BR <= 32 && BR % 4 == 0, "block-sum geometry");
   __shared__ float sm[BR], sil[BR];
+  // launched as a programmatic dependent of the score GEMM before it: its
+  // partials and statistics are complete and visible once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int cta = blockIdx.x;
   const int r = find_req(g, cta, [](const ReqDesc &d) { return d.bsum0; });
   const ReqDesc &R = g.req[r];
@@ -99,13 +102,23 @@ __global__ void __launch_bounds__(BTHR) block_sum_kernel(const __grid_constant__
 cudaError_t launch_block_sum(const Geo &g, int nctas, const float *bpart, const float2 *tstat,
                              float *block_sums, cudaStream_t st) {
   if (nctas == 0) return cudaSuccess;
+  // a programmatic dependent of the kernel before it on the stream (the score
+  // GEMM of the same call): its CTAs take SMs as the GEMM's free up
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nctas);
+  cfg.blockDim = dim3(BTHR);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (g.Bk / g.S) {
-    case 8: block_sum_kernel<8><<<nctas, BTHR, 0, st>>>(g, bpart, tstat, block_sums); break;
-    case 16: block_sum_kernel<16><<<nctas, BTHR, 0, st>>>(g, bpart, tstat, block_sums); break;
-    case 32: block_sum_kernel<32><<<nctas, BTHR, 0, st>>>(g, bpart, tstat, block_sums); break;
+    case 8: return cudaLaunchKernelEx(&cfg, block_sum_kernel<8>, g, bpart, tstat, block_sums);
+    case 16: return cudaLaunchKernelEx(&cfg, block_sum_kernel<16>, g, bpart, tstat, block_sums);
+    case 32: return cudaLaunchKernelEx(&cfg, block_sum_kernel<32>, g, bpart, tstat, block_sums);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace xattn

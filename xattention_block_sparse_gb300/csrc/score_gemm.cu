@@ -443,6 +443,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // this CTA's work is done: the block-sum launch after this one (a
+  // programmatic dependent, which waits for this grid to complete before it
+  // reads) may start on the SMs that free up
+  asm volatile("griddepcontrol.launch_dependents;");
   // Launched as a programmatic dependent of the kernel before it on the
   // stream: this launch may have started while that kernel (a previous
   // chunk's attention, which lets its dependents start early) was still
