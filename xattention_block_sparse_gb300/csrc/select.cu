@@ -87,19 +87,34 @@ __device__ void vote_request(const Geo &g, int r, int kvh, const int32_t *counts
   const int per = (kbh + nthr - 1) / nthr;
   const int beg = min(tid * per, kbh), end = min(beg + per, kbh);
   const int32_t *cnt = counts + row * g.bt_stride;
-  auto keep = [&](int j) {
-    return (int64_t)__ldcg(cnt + j) * vote_den > (int64_t)vote_num * votes_total ||
+  const int32_t *bt = g.block_table + (int64_t)r * g.bt_stride;
+  auto keep = [&](int j, int c) {
+    return (int64_t)c * vote_den > (int64_t)vote_num * votes_total ||
            (force && (j == 0 || j == kbh - 1));
   };
+  // the thread's votes and page ids, loaded together before the scan (up to
+  // kVotePer of each held in registers; longer runs read them again)
+  constexpr int kVotePer = 4;
+  int cv[kVotePer], pv[kVotePer];
+#pragma unroll
+  for (int e = 0; e < kVotePer; ++e) {
+    const int j = beg + e;
+    cv[e] = j < end ? __ldcg(cnt + j) : 0;
+    pv[e] = j < end ? __ldg(bt + j) : 0;
+  }
   unsigned long long mine = 0;
-  for (int j = beg; j < end; ++j) mine += keep(j) ? 1 : 0;
+  for (int j = beg; j < end; ++j) {
+    const int e = j - beg;
+    mine += keep(j, e < kVotePer ? cv[e] : __ldcg(cnt + j)) ? 1 : 0;
+  }
   unsigned long long total;
   unsigned long long pos = block_excl_scan(mine, wbuf, &total);
   for (int j = beg; j < end; ++j) {
-    if (keep(j)) {
+    const int e = j - beg;
+    if (keep(j, e < kVotePer ? cv[e] : __ldcg(cnt + j))) {
       const int64_t o = row * g.bt_stride + (int64_t)pos;
       sel_idx[o] = j;
-      int p = g.block_table[(int64_t)r * g.bt_stride + j];
+      int p = e < kVotePer ? pv[e] : __ldg(bt + j);
       if (p < 0 || p >= g.num_pages) {
         record_error(g.err, XATTN_EPAGE);
         p = -1;
