@@ -538,3 +538,75 @@ def test_attention_writes_pinned_host_outputs():
     assert st == -1  # XATTN_EINVAL
     torch.cuda.synchronize()
     assert torch.all(pageable_o == 0)
+
+
+def test_pipelined_host_fed_prefills_give_each_its_own_results():
+    """HostFedPipeline: three prefills (inputs A, B, A; B's queries are A's with
+    head_dim reversed) through two device buffer sets, the next one's copies
+    overlapping the current one's compute, each into host outputs of its own:
+    every one equals the device-resident run of its inputs, bit for bit --
+    eagerly, and replayed from one CUDA graph of the three."""
+    case = SequenceCase("q06b_4k")
+    cfg, L = case.cfg, case.L
+    Qb = case.Q.flip(-1).contiguous()
+    refs = {}
+    for tag, Q in (("A", case.Q), ("B", Qb)):
+        O_ = torch.empty((cfg.H, L, cfg.D), dtype=torch.bfloat16, device=dev())
+        LSE = torch.empty((cfg.H, L), dtype=torch.float32, device=dev())
+        case.seq.run(Q, case.K, case.V, case.KP, case.VP, 0.9, O_, LSE)
+        torch.cuda.synchronize()
+        refs[tag] = (O_.cpu(), LSE.cpu())
+    pin = lambda t: t.cpu().pin_memory()
+    ins = {"A": {"q": pin(case.Q), "k": pin(case.K), "v": pin(case.V)},
+           "B": {"q": pin(Qb), "k": pin(case.K), "v": pin(case.V)}}
+    order = ["A", "B", "A"]
+    hosts = []
+    for tag in order:
+        h = dict(ins[tag])
+        h["o"] = torch.zeros((cfg.H, L, cfg.D), dtype=torch.bfloat16).pin_memory()
+        h["lse"] = torch.zeros((cfg.H, L), dtype=torch.float32).pin_memory()
+        hosts.append(h)
+    sets = []
+    for _ in range(2):
+        d = {k: torch.zeros_like(ins["A"][k], device=dev()) for k in ("q", "k", "v")}
+        d["o"] = torch.zeros((cfg.H, L, cfg.D), dtype=torch.bfloat16, device=dev())
+        d["lse"] = torch.zeros((cfg.H, L), dtype=torch.float32, device=dev())
+        sets.append(d)
+    for name, ref in (("kpool", case.KP), ("vpool", case.VP)):
+        pool = torch.full_like(ref, float("nan"))
+        for d in sets:
+            d[name] = pool
+    stream = torch.cuda.Stream(device=dev())
+    h2d, d2h = torch.cuda.Stream(device=dev()), torch.cuda.Stream(device=dev())
+
+    def many():
+        pipe = RN.HostFedPipeline(case.seq, sets, stream, h2d, d2h, store_kv=True)
+        for h in hosts:
+            pipe.submit(h, 0.9)
+        pipe.join()
+
+    def check():
+        assert X.xattn_device_error() == 0
+        for tag, h in zip(order, hosts):
+            assert torch.equal(h["o"].view(torch.int16), refs[tag][0].view(torch.int16)), tag
+            assert torch.equal(h["lse"], refs[tag][1]), tag
+
+    with torch.cuda.stream(stream):
+        many()
+    stream.synchronize()
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        many()
+    torch.cuda.synchronize()
+    for h in hosts:
+        h["o"].zero_()
+        h["lse"].zero_()
+    for d in sets:
+        for k in ("q", "k", "v", "o", "lse"):
+            d[k].zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    check()

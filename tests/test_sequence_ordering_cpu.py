@@ -151,3 +151,68 @@ def test_a_missing_wait_is_caught(built, monkeypatch):
     log2 = [op for op in log if not (op[0] == "wait" and op[1] is compute)]
     before = FS.happens_before(log2)
     assert not before(_index(log2, "copy", ("k", 1)), _index(log2, "estimate", 1))
+
+
+def test_pipelined_prefills_overlap_copies_and_reuse_buffers_in_order(built, monkeypatch):
+    """HostFedPipeline, three prefills through two device buffer sets: the
+    second prefill's inputs may cross while the first one computes (no order
+    between them), the third one's inputs overwrite the first one's set only
+    after the first one's last attention, and its outputs only after the first
+    one's last read-back; within every prefill, each chunk still follows the
+    copies it reads, and the prefills' compute stays in order."""
+    log, _ = FS.install(monkeypatch)
+    H, Hkv, D, S, Bk, chunk, n = 2, 1, 64, 8, 64, 64, 3
+    L = chunk * n
+    bt = torch.arange(L // Bk, dtype=torch.int32)[None]
+    seq = RN.SequencePrefill(H, Hkv, D, S, Bk, L, chunk, bt, L // Bk)
+    chunk_of = {id(p): c for c, p in enumerate(seq.problems)}
+    host = {nm: torch.zeros(s) for nm, s in (("q", (H, L, D)), ("k", (Hkv, L, D)),
+                                             ("v", (Hkv, L, D)), ("o", (H, L, D)),
+                                             ("lse", (H, L)))}
+    sets = [{nm: torch.zeros_like(t) for nm, t in host.items()} for _ in range(2)]
+    for st in sets:
+        st["kpool"], st["vpool"] = _Pool(log, "kpool"), _Pool(log, "vpool")
+    names = {id(t): nm for nm, t in host.items()}
+    for i, st in enumerate(sets):
+        names.update({id(t): f"{nm}{i}" for nm, t in st.items() if torch.is_tensor(t)})
+    current = [0]  # the prefill being enqueued
+
+    def copy_window(dst, src, t0, t1, stream=None):
+        nm = names[id(dst)] if dst is not host.get("o") and dst is not host.get("lse") \
+            else names[id(src)] + ">host"
+        log.append(("copy", stream, (current[0], nm, t0 // chunk)))
+
+    def rec(kind):
+        def f(p, *a, **k):
+            stream = a[-1] if a else k.get("stream")
+            log.append((kind, stream, (current[0], chunk_of[id(p)])))
+        return f
+
+    monkeypatch.setattr(X, "copy_window_async", copy_window)
+    for kind, fn in (("estimate", "xattn_estimate_seq"), ("select", "xattn_select"),
+                     ("attend", "bsa_chunk_attention"), ("store", "xattn_store_kv")):
+        monkeypatch.setattr(X, fn, rec(kind))
+    compute, h2d, d2h = (FS.Stream(log, nm) for nm in ("compute", "h2d", "d2h"))
+    pipe = RN.HostFedPipeline(seq, sets, compute, h2d, d2h, store_kv=True)
+    for i in range(3):
+        current[0] = i
+        pipe.submit(host, 0.9)
+    before = FS.happens_before(log)
+    idx = lambda kind, payload: _index(log, kind, payload)
+    s = lambda i: i % 2
+    for i in range(3):
+        for c in range(n):
+            est, att = idx("estimate", (i, c)), idx("attend", (i, c))
+            assert before(idx("copy", (i, f"k{s(i)}", c)), est)
+            assert before(idx("copy", (i, f"q{s(i)}", c)), est)
+            assert before(idx("copy", (i, f"v{s(i)}", c)), att)
+            assert before(att, idx("copy", (i, f"o{s(i)}>host", c)))
+    # consecutive prefills: compute in order, copies free to overlap
+    assert before(idx("attend", (0, n - 1)), idx("estimate", (1, 0)))
+    assert not before(idx("attend", (0, 0)), idx("copy", (1, "q1", 0)))
+    assert not before(idx("copy", (0, "o0>host", n - 1)), idx("estimate", (1, 0)))
+    # the third prefill reuses set 0: inputs after the first one's compute,
+    # outputs after its read-back
+    assert before(idx("attend", (0, n - 1)), idx("copy", (2, "q0", 0)))
+    assert before(idx("copy", (0, "o0>host", n - 1)), idx("attend", (2, 0)))
+    assert before(idx("copy", (0, "lse0>host", n - 1)), idx("attend", (2, 0)))

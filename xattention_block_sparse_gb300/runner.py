@@ -180,10 +180,21 @@ class SequencePrefill:
         same shapes.  Work is enqueued after whatever `stream` already holds;
         the side streams start from that point too.  Returns the event recorded
         on `stream` once every output is on the host."""
+        return self._host_fed(host, dev, tau, stream, h2d_stream, d2h_stream, store_kv,
+                              out_direct, None, None, True)
+
+    def _host_fed(self, host, dev, tau, stream, h2d_stream, d2h_stream, store_kv, out_direct,
+                  inputs_after, outputs_after, join):
+        """run_from_host's work.  inputs_after / outputs_after: events after
+        which the device inputs (q, k, v) / outputs (o, lse) may be overwritten
+        (None: once `stream` has done what it holds).  join: `stream` waits for
+        the read-backs and the event it then records is returned; otherwise
+        (event after the last attention on `stream`, event after the last
+        read-back on `d2h_stream`)."""
         import torch
         start = torch.cuda.Event()
         start.record(stream)
-        h2d_stream.wait_event(start)
+        h2d_stream.wait_event(inputs_after if inputs_after is not None else start)
         d2h_stream.wait_event(start)
         n = len(self.problems)
         ready, ready_v = [], []
@@ -213,6 +224,8 @@ class SequencePrefill:
             estimate_select(p, q, k, dev["kpool"], tau, self.bufs, stream=stream,
                             k_seq=self.key_seq(dev["k"]), per_kv_head=self.per_kv_head)
             stream.wait_event(ready_v[c])
+            if c == 0 and outputs_after is not None:  # the previous read-back of o, lse
+                stream.wait_event(outputs_after)
             if store_kv:  # the history of chunk c + 1, before anything reads it
                 X.xattn_store_kv(p, k, v, dev["kpool"], dev["vpool"], stream)
             attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, out["o"][:, t0:],
@@ -225,10 +238,61 @@ class SequencePrefill:
                 X.copy_window_async(host["lse"], dev["lse"], t0, t1, d2h_stream)
         side_done = torch.cuda.Event()
         side_done.record(d2h_stream)
+        if not join:
+            compute_done = torch.cuda.Event()
+            compute_done.record(stream)
+            return compute_done, side_done
         stream.wait_event(side_done)
         back = torch.cuda.Event()
         back.record(stream)
         return back
+
+
+class HostFedPipeline:
+    """Prefills of a stream of same-shaped sequences fed from pinned host
+    memory, through two device buffer sets in turn: the next prefill's Q, K, V
+    cross the host link while the current one computes, and the current one's
+    O and LSE come back while the next one computes.  Each prefill is
+    `SequencePrefill.run_from_host`'s (chunks ordered after the copies they
+    read by events); what changes is only when its copies may start: its
+    inputs once the prefill two back has finished reading that buffer set,
+    its outputs once that prefill's read-back has left it.  The compute of
+    consecutive prefills stays in order on `stream` (they share the
+    sequence's workspace and page pools).
+
+    seq: a SequencePrefill; dev_sets: two dicts of device tensors as
+    run_from_host's `dev` (the page pools may be shared)."""
+
+    def __init__(self, seq, dev_sets, stream, h2d_stream, d2h_stream, store_kv=True,
+                 out_direct=False):
+        if len(dev_sets) != 2:
+            raise ValueError("HostFedPipeline takes two device buffer sets")
+        self.seq, self.dev_sets = seq, dev_sets
+        self.stream, self.h2d, self.d2h = stream, h2d_stream, d2h_stream
+        self.store_kv, self.out_direct = store_kv, out_direct
+        import torch
+        # both sets are free once `stream` has done what it holds now
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        self.in_free = [ready, ready]   # set s's inputs no longer read
+        self.out_free = [ready, ready]  # set s's outputs read back
+        self.n = 0
+
+    def submit(self, host, tau):
+        """Enqueue one prefill of `host` (run_from_host's dict); returns the
+        event after which its O and LSE are on the host."""
+        s = self.n % 2
+        self.n += 1
+        compute_done, side_done = self.seq._host_fed(
+            host, self.dev_sets[s], tau, self.stream, self.h2d, self.d2h, self.store_kv,
+            self.out_direct, self.in_free[s], self.out_free[s], False)
+        self.in_free[s], self.out_free[s] = compute_done, side_done
+        return side_done
+
+    def join(self):
+        """`stream` waits for every read-back submitted so far."""
+        for ev in self.out_free:
+            self.stream.wait_event(ev)
 
 
 class LayerRing:
