@@ -149,17 +149,21 @@ def test_wave_over_two_requests(monkeypatch, schedule):
         q0 += lq
 
 
-@pytest.mark.parametrize("schedule", [None, "streamk"])
-def test_attention_logit_jumps(monkeypatch, schedule):
-    """Key pages whose logits sit far above or below the rest: every query
-    carries a shared direction u, and the keys of some selected pages carry
-    +-beta u, which moves those pages' logits by the boost below (in nats).
-    The kernel takes exponentials against the row max as it stood when last
-    raised; a tile whose values climb 2^64 above it is taken again exactly
-    (62 nats = 89 in base 2), one that climbs less is accepted as is (30 and
-    45 nats), and tiles far below it underflow to zero as they should.  Rows
-    of every 128-row tile's edges and random rows against the float64
-    oracle."""
+@pytest.mark.parametrize("schedule,span", [(None, "page"), ("streamk", "page"),
+                                           (None, "second_half"), ("streamk", "second_half")])
+def test_attention_logit_jumps(monkeypatch, schedule, span):
+    """Keys whose logits sit far above or below the rest: every query carries
+    a shared direction u, and the keys of some selected pages (all 128 of
+    them, or only the second 64) carry +-beta u, which moves their logits by
+    the boost below (in nats); so do 40 keys in the middle of the current
+    chunk (+60 nats), which rows reach on their causal diagonal.  The kernel
+    takes exponentials against the row max as it stood when last raised; a
+    64-key half whose values climb 2^64 above it (62 nats = 89 in base 2) is
+    finished by the retake -- with nothing of the tile stored yet, or after
+    the first half's P was stored and must be rescaled -- one that climbs
+    less is accepted as is (30 and 45 nats), and keys far below it underflow
+    to zero as they should.  Rows of every 128-row tile's edges and random
+    rows against the float64 oracle."""
     if schedule is not None:
         monkeypatch.setenv("XATTN_ATTN_SCHEDULE", schedule)
     H, Hkv, D, Bk, S, lq, n_hist = 4, 2, 128, 128, 8, 512, 40
@@ -178,9 +182,11 @@ def test_attention_logit_jumps(monkeypatch, schedule):
     vp = rng.standard_normal((P, Bk, Hkv, D))
     perm = rng.permutation(P).astype(np.int32)
     bt = perm[None, :n_hist].copy()
+    rows_of_page = slice(0, Bk) if span == "page" else slice(Bk // 2, Bk)
     for lp, b in boost.items():
         beta = b * math.sqrt(D) / alpha
-        kp[bt[0, lp]] += beta * u[None, :, :]
+        kp[bt[0, lp], rows_of_page] += beta * u[None, :, :]
+    kc[:, 300:340] += (60.0 * math.sqrt(D) / alpha) * u[:, None, :]
     q, kc, vc, kp, vp = (I.bf16_round(a.astype(np.float32)) for a in (q, kc, vc, kp, vp))
     pages = bt[0, :]
 
