@@ -207,6 +207,10 @@ def test_pipelined_prefills_overlap_copies_and_reuse_buffers_in_order(built, mon
             assert before(idx("copy", (i, f"q{s(i)}", c)), est)
             assert before(idx("copy", (i, f"v{s(i)}", c)), att)
             assert before(att, idx("copy", (i, f"o{s(i)}>host", c)))
+    # early waits: chunk c + 1's keys are waited for before chunk c's attention
+    for i in range(3):
+        for c in range(n - 1):
+            assert before(idx("copy", (i, f"k{s(i)}", c + 1)), idx("attend", (i, c)))
     # consecutive prefills: compute in order, copies free to overlap
     assert before(idx("attend", (0, n - 1)), idx("estimate", (1, 0)))
     assert not before(idx("attend", (0, 0)), idx("copy", (1, "q1", 0)))

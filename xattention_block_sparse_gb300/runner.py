@@ -184,13 +184,17 @@ class SequencePrefill:
                               out_direct, None, None, True)
 
     def _host_fed(self, host, dev, tau, stream, h2d_stream, d2h_stream, store_kv, out_direct,
-                  inputs_after, outputs_after, join):
+                  inputs_after, outputs_after, join, early_waits=False):
         """run_from_host's work.  inputs_after / outputs_after: events after
         which the device inputs (q, k, v) / outputs (o, lse) may be overwritten
         (None: once `stream` has done what it holds).  join: `stream` waits for
         the read-backs and the event it then records is returned; otherwise
         (event after the last attention on `stream`, event after the last
-        read-back on `d2h_stream`)."""
+        read-back on `d2h_stream`).  early_waits: chunk c + 1's wait for its
+        keys goes before chunk c's attention, so that its estimate follows that
+        attention with nothing in between and may start in its tail (a
+        programmatic dependent launch); for callers whose copies run well
+        ahead of the compute (HostFedPipeline)."""
         import torch
         start = torch.cuda.Event()
         start.record(stream)
@@ -220,7 +224,8 @@ class SequencePrefill:
             t0, t1 = c * self.chunk, (c + 1) * self.chunk
             p = self.problems[c]
             q, k, v = dev["q"][:, t0:], dev["k"][:, t0:], dev["v"][:, t0:]
-            stream.wait_event(ready[c])  # K of chunks 0..c have landed (one copy stream)
+            if not early_waits or c == 0:
+                stream.wait_event(ready[c])  # K of chunks 0..c have landed (one copy stream)
             estimate_select(p, q, k, dev["kpool"], tau, self.bufs, stream=stream,
                             k_seq=self.key_seq(dev["k"]), per_kv_head=self.per_kv_head)
             stream.wait_event(ready_v[c])
@@ -228,6 +233,8 @@ class SequencePrefill:
                 stream.wait_event(outputs_after)
             if store_kv:  # the history of chunk c + 1, before anything reads it
                 X.xattn_store_kv(p, k, v, dev["kpool"], dev["vpool"], stream)
+            if early_waits and c + 1 < n:
+                stream.wait_event(ready[c + 1])
             attend(p, q, k, v, dev["kpool"], dev["vpool"], self.bufs, out["o"][:, t0:],
                    out["lse"][:, t0:], stream=stream, per_kv_head=self.per_kv_head)
             if not out_direct:
@@ -285,7 +292,7 @@ class HostFedPipeline:
         self.n += 1
         compute_done, side_done = self.seq._host_fed(
             host, self.dev_sets[s], tau, self.stream, self.h2d, self.d2h, self.store_kv,
-            self.out_direct, self.in_free[s], self.out_free[s], False)
+            self.out_direct, self.in_free[s], self.out_free[s], False, early_waits=True)
         self.in_free[s], self.out_free[s] = compute_done, side_done
         return side_done
 
