@@ -220,3 +220,19 @@ def test_pipelined_prefills_overlap_copies_and_reuse_buffers_in_order(built, mon
     assert before(idx("attend", (0, n - 1)), idx("copy", (2, "q0", 0)))
     assert before(idx("copy", (0, "o0>host", n - 1)), idx("attend", (2, 0)))
     assert before(idx("copy", (0, "lse0>host", n - 1)), idx("attend", (2, 0)))
+
+
+def test_pipeline_refuses_shared_pools_copied_from_the_host(built, monkeypatch):
+    """Pools copied in from the host by every prefill cannot be shared by the
+    two buffer sets: the next prefill's copy would overwrite what the current
+    one reads."""
+    FS.install(monkeypatch)
+    H, Hkv, D, S, Bk, chunk = 2, 1, 64, 8, 64, 64
+    bt = torch.arange(2, dtype=torch.int32)[None]
+    seq = RN.SequencePrefill(H, Hkv, D, S, Bk, 2 * chunk, chunk, bt, 2)
+    pool = torch.zeros(1)
+    sets = [{"kpool": pool, "vpool": pool}, {"kpool": pool, "vpool": pool}]
+    streams = [FS.Stream([], nm) for nm in ("c", "h", "d")]
+    with pytest.raises(ValueError):
+        RN.HostFedPipeline(seq, sets, *streams, store_kv=False)
+    RN.HostFedPipeline(seq, sets, *streams, store_kv=True)  # built on the device: fine

@@ -268,12 +268,19 @@ class HostFedPipeline:
     sequence's workspace and page pools).
 
     seq: a SequencePrefill; dev_sets: two dicts of device tensors as
-    run_from_host's `dev` (the page pools may be shared)."""
+    run_from_host's `dev`.  The page pools may be shared when they are built
+    on the device (store_kv: a prefill's stores run on `stream`, after the
+    previous prefill's attentions); pools copied from the host need a pair
+    per set."""
 
     def __init__(self, seq, dev_sets, stream, h2d_stream, d2h_stream, store_kv=True,
                  out_direct=False):
         if len(dev_sets) != 2:
             raise ValueError("HostFedPipeline takes two device buffer sets")
+        if not store_kv and any(dev_sets[0][k] is dev_sets[1][k] for k in ("kpool", "vpool")):
+            # the next prefill's pool copy would overwrite the pools this one reads
+            raise ValueError("HostFedPipeline with pools copied from the host needs a pool "
+                             "pair per buffer set")
         self.seq, self.dev_sets = seq, dev_sets
         self.stream, self.h2d, self.d2h = stream, h2d_stream, d2h_stream
         self.store_kv, self.out_direct = store_kv, out_direct
