@@ -98,3 +98,34 @@ def test_long_rows_take_the_cta_sort():
 def test_vote_ratios_on_warp_path():
     _run(16, 8, 128, [4, 8], [100, 700], 0.6, seed=14, vote=(3, 4), force=False)
     _run(16, 8, 128, [4, 8], [100, 700], 0.6, seed=15, vote=(0, 1), force=True)
+
+
+@pytest.mark.parametrize("per_kv", [False, True])
+def test_no_history_and_no_mask_selects_nothing(per_kv):
+    """A call whose requests have no history block and that asks for no mask
+    (a sequence's first chunk) has empty selections: n_sel is zero for every
+    row, the lists are left as they were, and the same call with a mask gives
+    the same counts -- the mask it writes comes from the full kernel."""
+    H, Hkv, Bk = 4, 2, 128
+    q_blocks = [4, 2]
+    B = len(q_blocks)
+    rng = np.random.default_rng(11)
+    BT = torch.full((B, 4), -1, dtype=torch.int32, device=dev())
+    prob = X.Problem(H, Hkv, 128, 8, Bk, [n * Bk for n in q_blocks], [0] * B, BT, 1)
+    flat = np.concatenate([_block_sums(rng, H, qb, qb, 16, False).reshape(-1) for qb in q_blocks])
+    bs = torch.from_numpy(flat).to(dev())
+    ws = torch.empty(X.xattn_workspace_size(prob), dtype=torch.uint8, device=dev())
+    rows = B * Hkv if per_kv else B
+    shape = (B, Hkv, 4) if per_kv else (B, 4)
+    select = X.xattn_select_per_kv_head if per_kv else X.xattn_select
+    for mask in (None, torch.full((flat.size,), 7, dtype=torch.uint8, device=dev())):
+        sel_idx = torch.full(shape, -5, dtype=torch.int32, device=dev())
+        sel_page = torch.full(shape, -5, dtype=torch.int32, device=dev())
+        n_sel = torch.full(shape[:-1], 9, dtype=torch.int32, device=dev())
+        select(prob, bs, 0.9, ws, mask, sel_idx, sel_page, n_sel)
+        torch.cuda.synchronize()
+        assert X.xattn_device_error() == 0
+        assert n_sel.numel() == rows and torch.all(n_sel == 0)
+        assert torch.all(sel_idx == -5) and torch.all(sel_page == -5)
+        if mask is not None:
+            assert torch.all((mask == 0) | (mask == 1))  # written by the kernel

@@ -287,6 +287,10 @@ static xattn_status run_select(Plan &pl, const xattn_problem *p, const float *bl
   xattn_status s;
   if ((s = err_word(&pl.geo.err)) != XATTN_OK) return s;
   const size_t rows = (size_t)pl.geo.B * (per_kv ? (size_t)pl.geo.Hkv : 1);
+  bool any_hist = false;
+  for (int r = 0; r < pl.geo.B; ++r) any_hist = any_hist || pl.geo.req[r].kh > 0;
+  if (!any_hist && !mask)  // no history block to select and no mask asked for:
+    return cu(cudaMemsetAsync(n_sel, 0, rows * sizeof(int32_t), st));  // every list is empty
   s = cu(cudaMemsetAsync(counts, 0, (rows * (size_t)p->bt_stride + 1) * sizeof(int32_t), st));
   if (s != XATTN_OK) return s;
   return cu(launch_select(pl.geo, pl.sel_ctas, pl.max_kb, block_sums, threshold, mask, counts,
