@@ -497,8 +497,9 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "e2e": e2e,
         # per chunk, this library's kernels: score GEMM, block sums, select (+ vote),
-        # attention; plus two cudaMemsetAsync of counters (not counted)
-        "gpu_launches": 4 * nchunk * K_,
+        # attention -- the first chunk, with no history to select from, launches no
+        # select (n_sel cleared) -- plus cudaMemsetAsync of counters (not counted)
+        "gpu_launches": (4 * nchunk - 1) * K_,
         "wall_s_timed": wall,
         **extra,
     }
